@@ -1,0 +1,179 @@
+"""ctypes wrapper around the fp64 CPU oracle in ``fa_oracle.c``.
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, by the smoke check and by the bench's
+CPU-baseline leg, never by the product path. The oracle shares no code with the CUDA
+path; it is compiled by gcc from ``fa_oracle.c`` alone.
+
+Functions take bf16 bit arrays (``numpy.uint16``, from the shared seeded generator) or
+float64 arrays, in the [B, H, N, d] layout, and return float64 results.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "fa_oracle.c")
+_LOCK = threading.Lock()
+_LIBS: dict = {}
+
+
+def lib_path(mutant: int = 0) -> str:
+    name = "liboracle.so" if mutant == 0 else f"liboracle_mutant{mutant}.so"
+    return os.path.join(_HERE, "_build", name)
+
+
+def build(mutant: int = 0, force: bool = False) -> str:
+    """Compile the oracle (or one planted-mistake variant of it) with gcc."""
+    out = lib_path(mutant)
+    if (not force and os.path.exists(out)
+            and os.path.getmtime(out) >= os.path.getmtime(_SRC)):
+        return out
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-shared", "-fPIC", "-pthread", "-fno-fast-math",
+           f"-DORACLE_MUTANT={int(mutant)}", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def _lib(mutant: int = 0):
+    with _LOCK:
+        if mutant in _LIBS:
+            return _LIBS[mutant]
+        lib = ctypes.CDLL(build(mutant))
+        P = ctypes.c_void_p
+        L = ctypes.c_long
+        I = ctypes.c_int
+        D = ctypes.c_double
+        lib.fa_oracle_forward_bf16.argtypes = [P, P, P, P, P, L, L, L, L, I, D, I]
+        lib.fa_oracle_forward_rows_bf16.argtypes = [P, P, P, P, P, L, L, L, L, I, D, P, L, I]
+        lib.fa_oracle_forward_f64.argtypes = [P, P, P, P, P, L, L, L, L, I, D, I]
+        lib.fa_oracle_probs_f64.argtypes = [P, P, P, L, L, L, L, I, D, I]
+        lib.fa_oracle_backward_bf16.argtypes = [P, P, P, P, P, P, P, L, L, L, L, I, D, I]
+        lib.fa_oracle_backward_f64.argtypes = [P, P, P, P, P, P, P, L, L, L, L, I, D, I]
+        lib.fa_oracle_backward_rows_bf16.argtypes = [P, P, P, P, P, P, P, L, L, L, L, I, D,
+                                                     P, L, P, L, I]
+        lib.fa_oracle_mutant_id.argtypes = []
+        for fn in ("fa_oracle_forward_bf16", "fa_oracle_forward_rows_bf16",
+                   "fa_oracle_forward_f64", "fa_oracle_probs_f64", "fa_oracle_backward_bf16",
+                   "fa_oracle_backward_f64", "fa_oracle_backward_rows_bf16",
+                   "fa_oracle_mutant_id"):
+            getattr(lib, fn).restype = ctypes.c_int
+        _LIBS[mutant] = lib
+        return lib
+
+
+def default_threads() -> int:
+    return max(1, len(os.sched_getaffinity(0)))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != 0:
+        raise RuntimeError(f"oracle {what} failed with code {rc}")
+
+
+def _shape4(q: np.ndarray):
+    if q.ndim != 4:
+        raise ValueError("expected [B, H, N, d]")
+    return q.shape
+
+
+class Oracle:
+    """Handle on one build of the oracle (``mutant=0`` is the real one)."""
+
+    def __init__(self, mutant: int = 0, threads: int | None = None):
+        self.mutant = mutant
+        self.threads = threads or default_threads()
+        self.lib = _lib(mutant)
+
+    # -- forward ----------------------------------------------------------------------
+    def forward_bf16(self, q, k, v, causal: bool, scale: float):
+        B, H, N, d = _shape4(q)
+        q, k, v = (np.ascontiguousarray(x, dtype=np.uint16) for x in (q, k, v))
+        o = np.empty((B, H, N, d), dtype=np.float64)
+        lse = np.empty((B, H, N), dtype=np.float64)
+        _check(self.lib.fa_oracle_forward_bf16(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                               B, H, N, d, int(causal), float(scale),
+                                               self.threads), "forward")
+        return o, lse
+
+    def forward_rows_bf16(self, q, k, v, causal: bool, scale: float, rows):
+        B, H, N, d = _shape4(q)
+        q, k, v = (np.ascontiguousarray(x, dtype=np.uint16) for x in (q, k, v))
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        nr = rows.shape[0]
+        o = np.empty((B, H, nr, d), dtype=np.float64)
+        lse = np.empty((B, H, nr), dtype=np.float64)
+        _check(self.lib.fa_oracle_forward_rows_bf16(_ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                                    _ptr(lse), B, H, N, d, int(causal),
+                                                    float(scale), _ptr(rows), nr,
+                                                    self.threads), "forward_rows")
+        return o, lse
+
+    def forward_f64(self, q, k, v, causal: bool, scale: float):
+        B, H, N, d = _shape4(q)
+        q, k, v = (np.ascontiguousarray(x, dtype=np.float64) for x in (q, k, v))
+        o = np.empty((B, H, N, d), dtype=np.float64)
+        lse = np.empty((B, H, N), dtype=np.float64)
+        _check(self.lib.fa_oracle_forward_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                              B, H, N, d, int(causal), float(scale),
+                                              self.threads), "forward_f64")
+        return o, lse
+
+    def probs_f64(self, q, k, causal: bool, scale: float):
+        B, H, N, d = _shape4(q)
+        q, k = (np.ascontiguousarray(x, dtype=np.float64) for x in (q, k))
+        P = np.empty((B, H, N, N), dtype=np.float64)
+        _check(self.lib.fa_oracle_probs_f64(_ptr(q), _ptr(k), _ptr(P), B, H, N, d,
+                                            int(causal), float(scale), self.threads), "probs")
+        return P
+
+    # -- backward ---------------------------------------------------------------------
+    def backward_bf16(self, q, k, v, dout, causal: bool, scale: float):
+        B, H, N, d = _shape4(q)
+        q, k, v, dout = (np.ascontiguousarray(x, dtype=np.uint16) for x in (q, k, v, dout))
+        dq, dk, dv = (np.empty((B, H, N, d), dtype=np.float64) for _ in range(3))
+        _check(self.lib.fa_oracle_backward_bf16(_ptr(q), _ptr(k), _ptr(v), _ptr(dout),
+                                                _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d,
+                                                int(causal), float(scale), self.threads),
+               "backward")
+        return dq, dk, dv
+
+    def backward_f64(self, q, k, v, dout, causal: bool, scale: float):
+        B, H, N, d = _shape4(q)
+        q, k, v, dout = (np.ascontiguousarray(x, dtype=np.float64) for x in (q, k, v, dout))
+        dq, dk, dv = (np.empty((B, H, N, d), dtype=np.float64) for _ in range(3))
+        _check(self.lib.fa_oracle_backward_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(dout),
+                                               _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d,
+                                               int(causal), float(scale), self.threads),
+               "backward_f64")
+        return dq, dk, dv
+
+    def backward_rows_bf16(self, q, k, v, dout, causal: bool, scale: float, rows_q, rows_k):
+        B, H, N, d = _shape4(q)
+        q, k, v, dout = (np.ascontiguousarray(x, dtype=np.uint16) for x in (q, k, v, dout))
+        rq = np.ascontiguousarray(rows_q, dtype=np.int64)
+        rk = np.ascontiguousarray(rows_k, dtype=np.int64)
+        dq = np.empty((B, H, rq.shape[0], d), dtype=np.float64)
+        dk = np.empty((B, H, rk.shape[0], d), dtype=np.float64)
+        dv = np.empty((B, H, rk.shape[0], d), dtype=np.float64)
+        _check(self.lib.fa_oracle_backward_rows_bf16(_ptr(q), _ptr(k), _ptr(v), _ptr(dout),
+                                                     _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d,
+                                                     int(causal), float(scale), _ptr(rq),
+                                                     rq.shape[0], _ptr(rk), rk.shape[0],
+                                                     self.threads), "backward_rows")
+        return dq, dk, dv
+
+
+def oracle(threads: int | None = None) -> Oracle:
+    return Oracle(0, threads)
