@@ -1,0 +1,186 @@
+"""Python binding of ``libfa.so`` (argument marshalling only).
+
+Every function here checks tensor properties, picks output buffers and calls the C ABI
+declared in ``include/fa.h`` through ctypes. All arithmetic happens in the CUDA kernels of
+``libfa.so``; if that library is missing the functions raise ``FaLibraryMissing`` rather
+than compute anything another way.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libfa.so")
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_ALIGNMENT = 3
+FA_ERR_CUDA = 4
+FA_ERR_TIMEOUT = 5
+
+# Every symbol include/fa.h declares.
+EXPORTS = ("fa_forward", "fa_backward_workspace_bytes", "fa_backward", "fa_status_string",
+           "fa_last_cuda_error", "fa_device_error")
+
+
+class FaLibraryMissing(RuntimeError):
+    pass
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, what: str, cuda_error: int = 0):
+        self.status = status
+        self.cuda_error = cuda_error
+        name = status_string(status) if _LIB is not None else str(status)
+        extra = f" (cudaError {cuda_error})" if status == FA_ERR_CUDA else ""
+        super().__init__(f"{what} failed: {name}{extra}")
+
+
+_LIB = None
+_LOCK = threading.Lock()
+
+
+def library(path: str | None = None):
+    """Load libfa.so once and declare the C signatures."""
+    global _LIB
+    with _LOCK:
+        if _LIB is not None:
+            return _LIB
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise FaLibraryMissing(
+                f"{p} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(p)
+        P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.fa_forward.argtypes = [P, P, P, P, P, I, I, I, I, I, F, P]
+        lib.fa_forward.restype = I
+        lib.fa_backward_workspace_bytes.argtypes = [I, I, I, I]
+        lib.fa_backward_workspace_bytes.restype = Z
+        lib.fa_backward.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, P, P]
+        lib.fa_backward.restype = I
+        lib.fa_status_string.argtypes = [I]
+        lib.fa_status_string.restype = ctypes.c_char_p
+        lib.fa_last_cuda_error.argtypes = []
+        lib.fa_last_cuda_error.restype = I
+        lib.fa_device_error.argtypes = [P, ctypes.POINTER(I)]
+        lib.fa_device_error.restype = I
+        _LIB = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return library().fa_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != FA_OK:
+        lib = library()
+        raise FaError(status, what, lib.fa_last_cuda_error() if status == FA_ERR_CUDA else 0)
+
+
+# ---- raw entry points (plain integers as pointers; used by tests and the bench) ----------
+
+def forward_raw(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int, d: int,
+                causal: int, scale: float, stream: int) -> int:
+    return library().fa_forward(q, k, v, o, lse, B, H, N, d, causal, scale, stream)
+
+
+def backward_raw(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, causal, scale, workspace,
+                 stream) -> int:
+    return library().fa_backward(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, causal, scale,
+                                 workspace, stream)
+
+
+def backward_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(library().fa_backward_workspace_bytes(B, H, N, d))
+
+
+def device_error(stream: int | None = None) -> int:
+    """Synchronise ``stream`` and return (and clear) the device error word."""
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    code = ctypes.c_int(0)
+    st = library().fa_device_error(stream, ctypes.byref(code))
+    if st not in (FA_OK, FA_ERR_TIMEOUT):
+        _check(st, "fa_device_error")
+    return code.value
+
+
+# ---- torch-facing wrappers ----------------------------------------------------------------
+
+def _check_tensor(name, t, shape=None):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
+            stream=None):
+    """O, LSE = attention(q, k, v). Tensors are bf16 [B, H, N, d] on one CUDA device."""
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_tensor(name, t, q.shape if name != "q" else None)
+        if t.dtype != torch.bfloat16:
+            raise ValueError(f"{name} must be bfloat16")
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, N, d]")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _check_tensor("out", out, q.shape)
+    _check_tensor("lse", lse, (B, H, N))
+    s = stream if stream is not None else torch.cuda.current_stream(q.device).cuda_stream
+    with torch.cuda.device(q.device):
+        st = forward_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                         B, H, N, d, int(bool(causal)), float(scale), s)
+    _check(st, "fa_forward")
+    return out, lse
+
+
+def backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None, dq=None,
+             dk=None, dv=None, workspace=None, stream=None):
+    """dQ, dK, dV of sum(O * dO) given the forward's O and LSE."""
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        _check_tensor(name, t, q.shape)
+        if t.dtype != torch.bfloat16:
+            raise ValueError(f"{name} must be bfloat16")
+    B, H, N, d = q.shape
+    _check_tensor("lse", lse, (B, H, N))
+    if lse.dtype != torch.float32:
+        raise ValueError("lse must be float32")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_tensor(name, t, q.shape)
+    ws_ptr = 0
+    if workspace is not None:
+        need = backward_workspace_bytes(B, H, N, d)
+        if workspace.numel() * workspace.element_size() < need:
+            raise ValueError(f"workspace needs {need} bytes")
+        ws_ptr = workspace.data_ptr()
+    s = stream if stream is not None else torch.cuda.current_stream(q.device).cuda_stream
+    with torch.cuda.device(q.device):
+        st = backward_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                          dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d,
+                          int(bool(causal)), float(scale), ws_ptr, s)
+    _check(st, "fa_backward")
+    return dq, dk, dv

@@ -1,0 +1,237 @@
+// fa_api.cu -- the C ABI declared in include/fa.h: argument checks, TMA tensor-map
+// encoding, workspace handling and kernel launches. No compute happens here.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "fa_launch.h"
+
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+
+// The device error word the kernels write when a wait gives up (one per device).
+__device__ int g_fa_error_word;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int* g_err_ptr[kMaxDevices] = {};
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+fa_status cuda_fail(cudaError_t e) {
+    t_last_cuda_error = (int)e;
+    return FA_ERR_CUDA;
+}
+
+// Driver entry point for cuTensorMapEncodeTiled, resolved through the runtime so the
+// library does not link libcuda directly.
+fa_status get_encode(EncodeTiledFn* out) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                         cudaEnableDefault, &q);
+        if (e != cudaSuccess) return cuda_fail(e);
+        if (q != cudaDriverEntryPointSuccess || fn == nullptr) return cuda_fail(cudaErrorNotSupported);
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    *out = g_encode;
+    return FA_OK;
+}
+
+// Address of this device's error word (looked up once per device, with that device current).
+fa_status get_err_ptr(int** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_err_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_fa_error_word);
+        if (e != cudaSuccess) return cuda_fail(e);
+        g_err_ptr[dev] = static_cast<int*>(p);
+    }
+    *out = g_err_ptr[dev];
+    return FA_OK;
+}
+
+// 3-D tiled map over a contiguous bf16 [BH, N, d] tensor: dims {d, N, BH}, box {64, box_rows, 1},
+// 128-byte swizzle. Rows past N inside a box read as zero and are not written by stores.
+fa_status make_map(CUtensorMap* m, const void* base, int BH, int N, int d, int box_rows) {
+    EncodeTiledFn enc = nullptr;
+    fa_status st = get_encode(&enc);
+    if (st != FA_OK) return st;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2u, (cuuint64_t)N * (cuuint64_t)d * 2u};
+    cuuint32_t box[3] = {64u, (cuuint32_t)box_rows, 1u};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        t_last_cuda_error = (int)r;
+        return FA_ERR_CUDA;
+    }
+    return FA_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Checks shared by forward and backward. Sets *empty when there is no work.
+fa_status check_common(int B, int H, int N, int d, int causal, float scale, bool* empty) {
+    if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    const long long bh = (long long)B * (long long)H;
+    *empty = (bh == 0 || N == 0);
+    if (*empty) return FA_OK;
+    if (bh > INT_MAX) return FA_ERR_UNSUPPORTED;
+    if ((long long)N + 256 > INT_MAX) return FA_ERR_UNSUPPORTED;
+    const long long nqb = ((long long)N + 255) / 256;
+    if (nqb * bh > INT_MAX) return FA_ERR_UNSUPPORTED;
+    return FA_OK;
+}
+
+constexpr float kLog2e = 1.4426950408889634074f;
+
+}  // namespace
+
+extern "C" {
+
+const char* fa_status_string(fa_status s) {
+    switch (s) {
+        case FA_OK: return "FA_OK";
+        case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+        case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+        case FA_ERR_ALIGNMENT: return "FA_ERR_ALIGNMENT";
+        case FA_ERR_CUDA: return "FA_ERR_CUDA";
+        case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+    }
+    return "FA_ERR_UNKNOWN";
+}
+
+int fa_last_cuda_error(void) { return t_last_cuda_error; }
+
+fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int H, int N, int d, int causal, float scale, struct CUstream_st* stream) {
+    bool empty = false;
+    fa_status st = check_common(B, H, N, d, causal, scale, &empty);
+    if (st != FA_OK || empty) return st;
+    if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+        return FA_ERR_ALIGNMENT;
+    const int BH = B * H;
+    fa::FwdLaunch a;
+    std::memset(&a, 0, sizeof a);
+    if ((st = make_map(&a.tm_q, q, BH, N, d, 128)) != FA_OK) return st;
+    if ((st = make_map(&a.tm_k, k, BH, N, d, 128)) != FA_OK) return st;
+    if ((st = make_map(&a.tm_v, v, BH, N, d, 128)) != FA_OK) return st;
+    if ((st = make_map(&a.tm_o, o, BH, N, d, 128)) != FA_OK) return st;
+    if ((st = get_err_ptr(&a.err)) != FA_OK) return st;
+    a.N = N;
+    a.BH = BH;
+    a.c = scale * kLog2e;
+    a.lse = lse;
+    cudaError_t e = fa::launch_forward(a, d, causal != 0, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return FA_OK;
+}
+
+size_t fa_backward_workspace_bytes(int B, int H, int N, int d) {
+    if (B <= 0 || H <= 0 || N <= 0 || (d != 64 && d != 128)) return 0;
+    const size_t bh = (size_t)B * (size_t)H;
+    const size_t npad = ((size_t)N + 127) / 128 * 128;
+    return 2 * bh * npad * sizeof(float) + bh * npad * (size_t)d * sizeof(float);
+}
+
+fa_status fa_backward(const void* q, const void* k, const void* v, const void* o,
+                      const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                      int H, int N, int d, int causal, float scale, void* workspace,
+                      struct CUstream_st* stream) {
+    bool empty = false;
+    fa_status st = check_common(B, H, N, d, causal, scale, &empty);
+    if (st != FA_OK || empty) return st;
+    if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+        !aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
+        !aligned(lse, 4))
+        return FA_ERR_ALIGNMENT;
+    if (workspace && !aligned(workspace, 256)) return FA_ERR_ALIGNMENT;
+    const int BH = B * H;
+    const int Npad = (N + 127) / 128 * 128;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    fa::BwdLaunch a;
+    std::memset(&a, 0, sizeof a);
+    const int q_rows = (d == 128) ? 64 : 128;  // query rows per backward step
+    if ((st = make_map(&a.tm_q, q, BH, N, d, q_rows)) != FA_OK) return st;
+    if ((st = make_map(&a.tm_do, dout, BH, N, d, q_rows)) != FA_OK) return st;
+    if ((st = make_map(&a.tm_k, k, BH, N, d, 128)) != FA_OK) return st;
+    if ((st = make_map(&a.tm_v, v, BH, N, d, 128)) != FA_OK) return st;
+    if ((st = make_map(&a.tm_dk, dk, BH, N, d, 128)) != FA_OK) return st;
+    if ((st = make_map(&a.tm_dv, dv, BH, N, d, 128)) != FA_OK) return st;
+    if ((st = get_err_ptr(&a.err)) != FA_OK) return st;
+    const size_t ws_bytes = fa_backward_workspace_bytes(B, H, N, d);
+    void* ws = workspace;
+    bool owned = false;
+    if (!ws) {
+        cudaError_t e = cudaMallocAsync(&ws, ws_bytes, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+        owned = true;
+    }
+    a.o = o;
+    a.dout = dout;
+    a.lse = lse;
+    a.dq = dq;
+    a.stats = static_cast<float*>(ws);
+    a.dq_acc = static_cast<float*>(ws) + 2 * (size_t)BH * (size_t)Npad;
+    a.N = N;
+    a.Npad = Npad;
+    a.BH = BH;
+    a.d = d;
+    a.scale = scale;
+    a.c = scale * kLog2e;
+    cudaError_t e = fa::launch_backward(a, causal != 0, s);
+    if (owned) {
+        cudaError_t e2 = cudaFreeAsync(ws, s);
+        if (e == cudaSuccess) e = e2;
+    }
+    if (e != cudaSuccess) return cuda_fail(e);
+    return FA_OK;
+}
+
+fa_status fa_device_error(struct CUstream_st* stream, int* code) {
+    if (!code) return FA_ERR_INVALID_ARG;
+    *code = 0;
+    int* p = nullptr;
+    fa_status st = get_err_ptr(&p);
+    if (st != FA_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    int h = 0;
+    e = cudaMemcpy(&h, p, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (h != 0) {
+        const int zero = 0;
+        e = cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    *code = h;
+    return h ? FA_ERR_TIMEOUT : FA_OK;
+}
+
+}  // extern "C"

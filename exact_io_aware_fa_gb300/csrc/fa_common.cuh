@@ -1,0 +1,48 @@
+// fa_common.cuh -- pieces shared by the forward and backward attention kernels:
+// bounded mbarrier waits with a CTA-wide abort path, the device error codes, and the
+// 128-byte swizzle used by TMA tiles and tcgen05 operands.
+#pragma once
+
+#include "sm100_ptx.cuh"
+
+namespace fa {
+
+// Device-side error codes written to the library's error word (first error wins).
+enum DeviceError : int {
+    kDevOk = 0,
+    kDevTimeoutLoad = 1,     // a TMA load never completed
+    kDevTimeoutMma = 2,      // an MMA completion never arrived
+    kDevTimeoutConsumer = 3, // a consumer never released a buffer
+    kDevTimeoutSoftmax = 4,  // softmax/epilogue warps never signalled
+};
+
+// A wait gives up after this long (the kernels' real waits last microseconds).
+constexpr uint64_t kWaitLimitNs = 4000000000ull;
+
+// Wait for phase `parity` of mbarrier `bar`. Returns false (and raises the CTA abort flag
+// and the global error word) if the limit expires, or if another role already aborted.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                           int* err, int code) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if ((it & 15u) == 0) {
+            if (*abort_flag) return false;
+            if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+                *abort_flag = 1;
+                atomicCAS(err, 0, code);
+                return false;
+            }
+        }
+    }
+}
+
+// Byte offset of the 16-byte unit `u` (0..7) of row `r` inside a 128-byte-swizzled tile whose
+// rows are 128 bytes apart (the layout TMA writes with CU_TENSOR_MAP_SWIZZLE_128B and the
+// tcgen05 descriptors read with layout type 2). The tile base must be 1024-byte aligned.
+__device__ __forceinline__ uint32_t sw128_offset(uint32_t r, uint32_t u) {
+    return r * 128u + ((u ^ (r & 7u)) << 4);
+}
+
+}  // namespace fa

@@ -1,0 +1,422 @@
+// fa_fwd.cu -- exact attention forward for sm_103a: O = softmax(scale * Q K^T) V and the
+// per-row log-sum-exp, computed tile by tile with the online-softmax recurrence so that
+// the N x N score and probability matrices never leave the SM.
+//
+// Method ("15. FlashAttention", inference.shantanugoel.com, sections "Online softmax:
+// normalize as you go" and "The algorithm in plain PyTorch"; "FlashAttention: from
+// IO-Aware Attention to GPU work partitioning", blog.euler0525.cn, sections
+// "FlashAttention-2" and "Tile Size 与 Causal Attention"):
+//   per query row keep m (running max), l (running sum of exp(s - m)) and an
+//   unnormalised accumulator a; for each key tile m_new = max(m, rowmax(s)),
+//   alpha = exp(m - m_new), p = exp(s - m_new), l = alpha l + sum p, a = alpha a + p V;
+//   at the end O = a / l and LSE = m + ln l. Tiles wholly above the causal diagonal are
+//   skipped; only the diagonal tile and the ragged last tile are masked elementwise.
+//
+// GB300 mapping (one CTA = 256 query rows of one (batch, head) = two 128-row Q tiles):
+//   warp 0      TMA producer: Q tiles once, then K_j / V_j into separate mbarrier rings
+//   warp 1      MMA issuer: S_t = Q_t K_j^T and O_t += P_t V_j with tcgen05.mma (fp32 in TMEM)
+//   warp 2      TMEM allocation / release
+//   warps 4-7   softmax for Q tile 0, warps 8-11 softmax for Q tile 1: one thread per row,
+//               the whole row of S read from TMEM into registers (no cross-thread reduction),
+//               exp2 with log2(e) folded into the scale, P written back to TMEM as bf16
+//               over the S columns, O rescaled in TMEM when the row max moves, and the
+//               epilogue (O / l -> bf16 -> swizzled smem -> TMA store; LSE -> global).
+// TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 and O_1 after column 256.
+#include "fa_common.cuh"
+#include "fa_launch.h"
+
+namespace fa {
+namespace {
+
+constexpr float kLn2 = 0.69314718055994530942f;
+
+template <int D>
+struct FwdCfg {
+    static constexpr int BM = 128;        // rows per Q tile (one TMEM lane per row)
+    static constexpr int BN = 128;        // keys per KV tile
+    static constexpr int ROWS = 2 * BM;   // rows per CTA
+    static constexpr int DCH = D / 64;    // 64-column (128-byte) chunks per row
+    static constexpr int NS = (D == 64) ? 3 : 2;  // K and V ring depth
+    static constexpr uint32_t TILE_BYTES = 128u * D * 2u;  // one 128-row bf16 tile
+    static constexpr uint32_t CHUNK_BYTES = 128u * 128u;   // one 128-row x 64-col chunk
+    static constexpr uint32_t OFF_Q = 0;
+    static constexpr uint32_t OFF_K = OFF_Q + 2 * TILE_BYTES;
+    static constexpr uint32_t OFF_V = OFF_K + NS * TILE_BYTES;
+    static constexpr uint32_t OFF_BAR = OFF_V + NS * TILE_BYTES;
+    static constexpr uint32_t SMEM_BYTES = OFF_BAR + 512 + 1024;  // + alignment slack
+    static constexpr int THREADS = 384;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t TMEM_O = 256;  // first O column
+};
+
+struct FwdBars {
+    uint64_t q_full;
+    uint64_t k_full[3], k_empty[3];
+    uint64_t v_full[3], v_empty[3];
+    uint64_t s_full[2], p_full[2], o_done[2];
+    uint64_t mma_final;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+    return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// Wait that ignores the abort flag (used only to drain copies already in flight).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (!ptx::mbar_try_wait(bar, parity)) {
+        if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) break;
+    }
+}
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(384, 1)
+fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+              const int N, const int nqb, const float c, float* __restrict__ lse_out, int* err) {
+    using C = FwdCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align1024(smem_raw);
+    FwdBars* bars = reinterpret_cast<FwdBars*>(smem + C::OFF_BAR);
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+
+    // ---- work unit: (bh, 256-row block), heaviest causal blocks of a head first ----------
+    const int bh = blockIdx.x / nqb;
+    int qb = blockIdx.x % nqb;
+    if (CAUSAL) qb = nqb - 1 - qb;
+    const int nk_total = (N + C::BN - 1) / C::BN;
+    int ntile[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const int r0 = qb * C::ROWS + t * C::BM;
+        ntile[t] = (r0 >= N) ? 0 : (CAUSAL ? min(nk_total, qb * 2 + t + 1) : nk_total);
+    }
+    const int nkv = max(ntile[0], ntile[1]);
+
+    const uint32_t b_q_full = ptx::smem_addr(&bars->q_full);
+    if (tid == 0) {
+        ptx::mbar_init(b_q_full, 1);
+        for (int s = 0; s < C::NS; ++s) {
+            ptx::mbar_init(ptx::smem_addr(&bars->k_full[s]), 1);
+            ptx::mbar_init(ptx::smem_addr(&bars->k_empty[s]), 1);
+            ptx::mbar_init(ptx::smem_addr(&bars->v_full[s]), 1);
+            ptx::mbar_init(ptx::smem_addr(&bars->v_empty[s]), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            ptx::mbar_init(ptx::smem_addr(&bars->s_full[t]), 1);
+            ptx::mbar_init(ptx::smem_addr(&bars->p_full[t]), C::BM);
+            ptx::mbar_init(ptx::smem_addr(&bars->o_done[t]), 1);
+        }
+        ptx::mbar_init(ptx::smem_addr(&bars->mma_final), 1);
+        bars->abort_flag = 0;
+        ptx::fence_barrier_init();
+        ptx::tma_prefetch_desc(&tm_q);
+        ptx::tma_prefetch_desc(&tm_k);
+        ptx::tma_prefetch_desc(&tm_v);
+        ptx::tma_prefetch_desc(&tm_o);
+    }
+    if (warp == 2) {
+        ptx::tmem_alloc(ptx::smem_addr(&bars->tmem_base), C::TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tbase = bars->tmem_base;
+    volatile int* abort_flag = &bars->abort_flag;
+
+    const uint32_t s_q = ptx::smem_addr(smem + C::OFF_Q);
+    const uint32_t s_k = ptx::smem_addr(smem + C::OFF_K);
+    const uint32_t s_v = ptx::smem_addr(smem + C::OFF_V);
+
+    if (warp == 0) {
+        // ================================ TMA producer ================================
+        if (lane == 0 && nkv > 0) {
+            const uint64_t pol_kv = ptx::l2_policy_evict_last();
+            const uint64_t pol_q = ptx::l2_policy_evict_first();
+            const int ntl = (ntile[0] > 0) + (ntile[1] > 0);
+            ptx::mbar_arrive_expect_tx(b_q_full, ntl * C::TILE_BYTES);
+            for (int t = 0; t < 2; ++t) {
+                if (ntile[t] == 0) continue;
+                for (int ch = 0; ch < C::DCH; ++ch)
+                    ptx::tma_load_3d_hint(s_q + t * C::TILE_BYTES + ch * C::CHUNK_BYTES, &tm_q,
+                                          b_q_full, ch * 64, qb * C::ROWS + t * C::BM, bh, pol_q);
+            }
+            int jk = 0, jv = 0;
+            for (int j = 0; j < nkv; ++j) {
+                const int s = j % C::NS;
+                const uint32_t ph = (uint32_t)(j / C::NS) & 1u;
+                const uint32_t bkf = ptx::smem_addr(&bars->k_full[s]);
+                const uint32_t bvf = ptx::smem_addr(&bars->v_full[s]);
+                if (!wait_phase(ptx::smem_addr(&bars->k_empty[s]), ph ^ 1u, abort_flag, err,
+                                kDevTimeoutConsumer))
+                    break;
+                ptx::mbar_arrive_expect_tx(bkf, C::TILE_BYTES);
+                for (int ch = 0; ch < C::DCH; ++ch)
+                    ptx::tma_load_3d_hint(s_k + s * C::TILE_BYTES + ch * C::CHUNK_BYTES, &tm_k, bkf,
+                                          ch * 64, j * C::BN, bh, pol_kv);
+                ++jk;
+                if (!wait_phase(ptx::smem_addr(&bars->v_empty[s]), ph ^ 1u, abort_flag, err,
+                                kDevTimeoutConsumer))
+                    break;
+                ptx::mbar_arrive_expect_tx(bvf, C::TILE_BYTES);
+                for (int ch = 0; ch < C::DCH; ++ch)
+                    ptx::tma_load_3d_hint(s_v + s * C::TILE_BYTES + ch * C::CHUNK_BYTES, &tm_v, bvf,
+                                          ch * 64, j * C::BN, bh, pol_kv);
+                ++jv;
+            }
+            // Drain: every copy issued must have landed before the CTA can exit.
+            drain_wait(b_q_full, 0);
+            for (int j = max(0, jk - C::NS); j < jk; ++j)
+                drain_wait(ptx::smem_addr(&bars->k_full[j % C::NS]), (uint32_t)(j / C::NS) & 1u);
+            for (int j = max(0, jv - C::NS); j < jv; ++j)
+                drain_wait(ptx::smem_addr(&bars->v_full[j % C::NS]), (uint32_t)(j / C::NS) & 1u);
+        }
+    } else if (warp == 1) {
+        // ================================ MMA issuer ==================================
+        if (lane == 0 && nkv > 0) {
+            constexpr uint32_t idesc_s = ptx::idesc_bf16(128, C::BN, false, false);
+            constexpr uint32_t idesc_o = ptx::idesc_bf16(128, D, false, true);
+            auto issue_s = [&](int t, int stage) {
+                const uint32_t d_tmem = tbase + (uint32_t)(t * 128);
+                const uint32_t qa = s_q + t * C::TILE_BYTES;
+                const uint32_t ka = s_k + stage * C::TILE_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
+                    ptx::mma_ss(d_tmem, ptx::sdesc_sw128(qa + off, 16, 1024),
+                                ptx::sdesc_sw128(ka + off, 16, 1024), idesc_s, kk > 0);
+                }
+            };
+            auto issue_pv = [&](int t, int stage, bool acc) {
+                const uint32_t d_tmem = tbase + C::TMEM_O + (uint32_t)(t * D);
+                const uint32_t p_tmem = tbase + (uint32_t)(t * 128);
+                const uint32_t va = s_v + stage * C::TILE_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < C::BN / 16; ++kk)
+                    ptx::mma_ts(d_tmem, p_tmem + kk * 8,
+                                ptx::sdesc_sw128(va + kk * 2048, C::CHUNK_BYTES, 1024), idesc_o,
+                                (acc || kk > 0) ? 1u : 0u);
+            };
+            bool ok = wait_phase(b_q_full, 0, abort_flag, err, kDevTimeoutLoad);
+            if (ok) ok = wait_phase(ptx::smem_addr(&bars->k_full[0]), 0, abort_flag, err,
+                                    kDevTimeoutLoad);
+            if (ok) {
+                ptx::tc_fence_after();
+                for (int t = 0; t < 2; ++t) {
+                    if (ntile[t] == 0) continue;
+                    issue_s(t, 0);
+                    ptx::mma_commit(ptx::smem_addr(&bars->s_full[t]));
+                }
+                ptx::mma_commit(ptx::smem_addr(&bars->k_empty[0]));
+            }
+            for (int j = 0; ok && j < nkv; ++j) {
+                const int s = j % C::NS;
+                const uint32_t ph = (uint32_t)(j / C::NS) & 1u;
+                ok = wait_phase(ptx::smem_addr(&bars->v_full[s]), ph, abort_flag, err,
+                                kDevTimeoutLoad);
+                if (!ok) break;
+                for (int t = 0; t < 2 && ok; ++t) {
+                    if (j >= ntile[t]) continue;
+                    ok = wait_phase(ptx::smem_addr(&bars->p_full[t]), (uint32_t)j & 1u, abort_flag,
+                                    err, kDevTimeoutSoftmax);
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+                    issue_pv(t, s, j > 0);
+                    ptx::mma_commit(ptx::smem_addr(&bars->o_done[t]));
+                }
+                if (!ok) break;
+                ptx::mma_commit(ptx::smem_addr(&bars->v_empty[s]));
+                if (j + 1 < nkv) {
+                    const int s1 = (j + 1) % C::NS;
+                    const uint32_t ph1 = (uint32_t)((j + 1) / C::NS) & 1u;
+                    ok = wait_phase(ptx::smem_addr(&bars->k_full[s1]), ph1, abort_flag, err,
+                                    kDevTimeoutLoad);
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+                    for (int t = 0; t < 2 && ok; ++t) {
+                        if (j + 1 >= ntile[t]) continue;
+                        // P_t(j) lives in the S_t columns: wait until O_t += P_t V_j has read it.
+                        ok = wait_phase(ptx::smem_addr(&bars->o_done[t]), (uint32_t)j & 1u,
+                                        abort_flag, err, kDevTimeoutMma);
+                        if (!ok) break;
+                        ptx::tc_fence_after();
+                        issue_s(t, s1);
+                        ptx::mma_commit(ptx::smem_addr(&bars->s_full[t]));
+                    }
+                    if (!ok) break;
+                    ptx::mma_commit(ptx::smem_addr(&bars->k_empty[s1]));
+                }
+            }
+            // Every MMA issued (and every commit arrive) must be done before TMEM and the
+            // barriers are released.
+            ptx::mma_commit(ptx::smem_addr(&bars->mma_final));
+            drain_wait(ptx::smem_addr(&bars->mma_final), 0);
+        }
+    } else if (warp >= 4) {
+        // ============================ softmax + epilogue ==============================
+        const int t = (warp - 4) >> 2;  // Q tile of this warpgroup
+        const int wq = warp & 3;        // TMEM lane quarter
+        const int r = wq * 32 + lane;   // row within the tile
+        const int row0 = qb * C::ROWS + t * C::BM;
+        const int row = row0 + r;
+        const int n = ntile[t];
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        const uint32_t t_s = tbase + lane_off + (uint32_t)(t * 128);
+        const uint32_t t_o = tbase + lane_off + C::TMEM_O + (uint32_t)(t * D);
+        const uint32_t b_s_full = ptx::smem_addr(&bars->s_full[t]);
+        const uint32_t b_p_full = ptx::smem_addr(&bars->p_full[t]);
+        const uint32_t b_o_done = ptx::smem_addr(&bars->o_done[t]);
+
+        float m = -INFINITY;  // running max of scale*log2(e)*s
+        float l = 0.f;        // running sum of exp2(c*s - m)
+        bool ok = true;
+        for (int j = 0; j < n; ++j) {
+            ok = __all_sync(0xffffffffu, wait_phase(b_s_full, (uint32_t)j & 1u, abort_flag, err,
+                                                    kDevTimeoutMma));
+            if (!ok) break;
+            ptx::tc_fence_after();
+            float s[C::BN];
+            {
+                uint32_t u0[32], u1[32], u2[32], u3[32];
+                ptx::tmem_ld32_nowait(t_s + 0, u0);
+                ptx::tmem_ld32_nowait(t_s + 32, u1);
+                ptx::tmem_ld32_nowait(t_s + 64, u2);
+                ptx::tmem_ld32_nowait(t_s + 96, u3);
+                ptx::tmem_wait_ld(u0);
+                ptx::tmem_wait_ld(u1);
+                ptx::tmem_wait_ld(u2);
+                ptx::tmem_wait_ld(u3);
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    s[k] = __uint_as_float(u0[k]);
+                    s[32 + k] = __uint_as_float(u1[k]);
+                    s[64 + k] = __uint_as_float(u2[k]);
+                    s[96 + k] = __uint_as_float(u3[k]);
+                }
+            }
+            const int key0 = j * C::BN;
+            const bool need_mask = (key0 + C::BN > N) || (CAUSAL && key0 + C::BN - 1 > row0);
+            if (need_mask) {
+#pragma unroll
+                for (int k = 0; k < C::BN; ++k) {
+                    const int key = key0 + k;
+                    if (key >= N || (CAUSAL && key > row)) s[k] = -INFINITY;
+                }
+            }
+            float mx = s[0];
+#pragma unroll
+            for (int k = 1; k < C::BN; ++k) mx = fmaxf(mx, s[k]);
+            const float m_new = fmaxf(m, mx * c);
+            const float m_ref = (m_new == -INFINITY) ? 0.f : m_new;  // safe reference
+            const float alpha = ptx::ex2_approx(m - m_ref);
+            float rs = 0.f;
+#pragma unroll
+            for (int k = 0; k < C::BN; ++k) {
+                s[k] = ptx::ex2_approx(fmaf(s[k], c, -m_ref));
+                rs += s[k];
+            }
+            l = l * alpha + rs;
+            m = m_new;
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) pk[i] = ptx::pack_bf16x2(s[32 * g + 2 * i], s[32 * g + 2 * i + 1]);
+                ptx::tmem_st16(t_s + 16 * g, pk);
+            }
+            ptx::tmem_wait_st();
+            if (j > 0) {
+                // O_t += P_t(j-1) V must be complete before O_t is rescaled.
+                ok = __all_sync(0xffffffffu, wait_phase(b_o_done, (uint32_t)(j - 1) & 1u,
+                                                        abort_flag, err, kDevTimeoutMma));
+                if (!ok) break;
+                ptx::tc_fence_after();
+                if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        uint32_t o[32];
+                        ptx::tmem_ld32(t_o + cc * 32, o);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        ptx::tmem_st32(t_o + cc * 32, o);
+                    }
+                    ptx::tmem_wait_st();
+                }
+            }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(b_p_full);
+        }
+        if (ok && n > 0) {
+            ok = __all_sync(0xffffffffu, wait_phase(b_o_done, (uint32_t)(n - 1) & 1u, abort_flag,
+                                                    err, kDevTimeoutMma));
+        }
+        if (ok && n > 0) {
+            ptx::tc_fence_after();
+            // ---- epilogue: O = a / l as bf16 into the (now idle) Q tile buffer, TMA store ----
+            const float inv_l = 1.f / l;
+            uint8_t* stage = smem + C::OFF_Q + t * C::TILE_BYTES;
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+                uint32_t o[32];
+                ptx::tmem_ld32(t_o + cc * 32, o);
+                uint8_t* chunk = stage + (cc >> 1) * C::CHUNK_BYTES;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    uint4 w;
+                    w.x = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 0]) * inv_l, __uint_as_float(o[8 * u + 1]) * inv_l);
+                    w.y = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 2]) * inv_l, __uint_as_float(o[8 * u + 3]) * inv_l);
+                    w.z = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 4]) * inv_l, __uint_as_float(o[8 * u + 5]) * inv_l);
+                    w.w = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 6]) * inv_l, __uint_as_float(o[8 * u + 7]) * inv_l);
+                    *reinterpret_cast<uint4*>(chunk + sw128_offset((uint32_t)r, (uint32_t)((cc & 1) * 4 + u))) = w;
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::named_bar_sync(1 + t, C::BM);
+            if (r == 0) {
+                for (int ch = 0; ch < C::DCH; ++ch)
+                    ptx::tma_store_3d(&tm_o, ptx::smem_addr(stage + ch * C::CHUNK_BYTES), ch * 64,
+                                      row0, bh);
+                ptx::bulk_commit();
+            }
+            if (row < N) lse_out[(size_t)bh * N + row] = (m + __log2f(l)) * kLn2;
+            if (r == 0) ptx::bulk_wait_read_all();
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tbase, C::TMEM_COLS);
+    }
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
+    using C = FwdCfg<D>;
+    auto kern = fa_fwd_kernel<D, CAUSAL>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int nqb = (a.N + C::ROWS - 1) / C::ROWS;
+    const long long blocks = (long long)nqb * a.BH;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    kern<<<(unsigned)blocks, C::THREADS, C::SMEM_BYTES, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o,
+                                                                  a.N, nqb, a.c, a.lse, a.err);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_forward(const FwdLaunch& a, int d, bool causal, cudaStream_t stream) {
+    if (d == 64) return causal ? launch_fwd_t<64, true>(a, stream) : launch_fwd_t<64, false>(a, stream);
+    if (d == 128) return causal ? launch_fwd_t<128, true>(a, stream) : launch_fwd_t<128, false>(a, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace fa

@@ -1,0 +1,115 @@
+/*
+ * fa.h -- C ABI of libfa.so: exact IO-aware attention (forward with log-sum-exp, and the
+ * recompute-based backward) for NVIDIA GB300 (sm_103a).
+ *
+ * Operation (the plain definition; the kernels reach it up to rounding order):
+ *   S = scale * Q K^T,  P = softmax(S) row-wise,  O = P V,  LSE_i = ln sum_j exp(S_ij)
+ *   -- "FlashAttention: from IO-Aware Attention to GPU work partitioning"
+ *      (blog.euler0525.cn), sections "Attention 的性能瓶颈" (S, P, O) and "FlashAttention-2"
+ *      (L_i = m_i + log l_i); "15. FlashAttention" (inference.shantanugoel.com), sections
+ *      "Online softmax: normalize as you go" and "The algorithm in plain PyTorch".
+ *   With causal != 0, key j is visible to query i iff j <= i (query and key sequences
+ *   have the same length N), as in blog.euler0525.cn, section "Tile Size 与 Causal
+ *   Attention" (S_ij = -inf for j > i).
+ *
+ * Layout: Q, K, V, O, dO, dQ, dK, dV are bf16, contiguous row-major [B, H, N, d]
+ * (element (b,h,n,e) at ((b*H + h)*N + n)*d + e). LSE is fp32 [B, H, N], natural log of
+ * the scaled scores. Every pointer is a device pointer unless stated otherwise.
+ *
+ * Ownership: the caller owns every buffer; the library keeps no state between calls
+ * besides one device error word per device (see fa_device_error).
+ *
+ * Execution: calls only enqueue work on `stream` (a cudaStream_t; NULL = legacy default
+ * stream) and return; they never synchronise. FA_OK means the launch was accepted;
+ * device-side faults surface at the caller's next synchronisation. A kernel that waits
+ * on an internal barrier for longer than a few seconds gives up, records an error code
+ * in the device error word and exits without faulting.
+ *
+ * Errors: arguments are checked on the host before anything is launched; a call that
+ * returns an error has launched nothing.
+ *   FA_ERR_INVALID_ARG  null pointer (when there is work), negative B/H/N, causal not 0/1,
+ *                       scale not finite or not > 0, workspace too small
+ *   FA_ERR_UNSUPPORTED  d not 64 or 128; sizes beyond the int32 range of the kernels
+ *   FA_ERR_ALIGNMENT    a bf16 tensor not 16-byte aligned, LSE not 4-byte aligned,
+ *                       workspace not 256-byte aligned (TMA needs 16-byte bases)
+ *   FA_ERR_CUDA         a CUDA runtime/driver call failed (fa_last_cuda_error gives it)
+ * B*H*N == 0 is valid: nothing is launched and FA_OK is returned.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t is `struct CUstream_st *` */
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,
+    FA_ERR_UNSUPPORTED = 2,
+    FA_ERR_ALIGNMENT = 3,
+    FA_ERR_CUDA = 4,
+    FA_ERR_TIMEOUT = 5
+} fa_status;
+
+/*
+ * Forward: O = softmax(scale Q K^T) V and LSE, computed tile by tile with the online-softmax
+ * recurrence (running max m, running sum l, rescale alpha = exp(m_old - m_new) applied to l
+ * and to the unnormalised accumulator; O = acc / l at the end; LSE = m + ln l), so the N x N
+ * matrices never reach HBM ("15. FlashAttention", section "Online softmax: normalize as you
+ * go"; blog.euler0525.cn, section "FlashAttention-2").
+ *   q, k, v  in : bf16 [B,H,N,d]
+ *   o        out: bf16 [B,H,N,d]
+ *   lse      out: fp32 [B,H,N]  (natural log, of scale * q.k)
+ *   d in {64, 128}; causal in {0, 1}; scale > 0 (1/sqrt(d) for standard attention).
+ */
+fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int H, int N, int d, int causal, float scale, struct CUstream_st* stream);
+
+/*
+ * Bytes of device workspace fa_backward needs for these sizes: two fp32 row statistics
+ * [B*H, Npad] and an fp32 dQ accumulator [B*H, Npad, d], Npad = N rounded up to 128.
+ * Returns 0 for invalid sizes or when B*H*N == 0.
+ */
+size_t fa_backward_workspace_bytes(int B, int H, int N, int d);
+
+/*
+ * Backward by recomputation: rebuilds S and P = exp(S - LSE) tile by tile from Q, K, V and
+ * the saved LSE, then dV = P^T dO, dP = dO V^T, D_i = O_i . dO_i, dS = P (.) (dP - D),
+ * dQ = scale dS K, dK = scale dS^T Q (blog.euler0525.cn, sections "Tiling、Fusion 与
+ * Backward Recomputation" and "FlashAttention-2"; the scale factor on dQ and dK follows from
+ * the chain rule through S = scale Q K^T). dQ partial sums from different key tiles are
+ * added in fp32 (section "Sequence Parallelism": column-oriented partition with atomic add).
+ *   q, k, v, o, dout in : bf16 [B,H,N,d];  lse in : fp32 [B,H,N] from fa_forward
+ *   dq, dk, dv       out: bf16 [B,H,N,d]
+ *   workspace: device buffer of >= fa_backward_workspace_bytes(B,H,N,d) bytes, 256-byte
+ *              aligned, used for the duration of the call's work on `stream`; or NULL, in
+ *              which case the library allocates and frees it on `stream` (cudaMallocAsync).
+ */
+fa_status fa_backward(const void* q, const void* k, const void* v, const void* o,
+                      const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                      int H, int N, int d, int causal, float scale, void* workspace,
+                      struct CUstream_st* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* fa_status_string(fa_status s);
+
+/* The cudaError_t of the last FA_ERR_CUDA returned on this thread (0 if none). */
+int fa_last_cuda_error(void);
+
+/*
+ * Synchronises `stream`, then reads and clears this device's error word. *code receives 0
+ * when no kernel gave up on a wait since the last call, else the first error code
+ * (1 load, 2 MMA completion, 3 buffer release, 4 softmax signal). Returns FA_ERR_TIMEOUT
+ * when *code != 0, FA_ERR_CUDA if synchronisation or the read failed, else FA_OK.
+ */
+fa_status fa_device_error(struct CUstream_st* stream, int* code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

@@ -1,0 +1,103 @@
+"""Host-side checks of the C ABI (no GPU): the library loads, exports every symbol the
+header declares, and rejects bad arguments before launching anything."""
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_io_aware_fa_gb300 import build
+    build.build()
+    from exact_io_aware_fa_gb300 import api
+    return api.library()
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "fa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_declares_expected_api():
+    from exact_io_aware_fa_gb300 import api
+    assert set(header_functions()) == set(api.EXPORTS)
+
+
+def test_library_exports_every_header_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    from exact_io_aware_fa_gb300 import api
+    assert api.status_string(0) == "FA_OK"
+    assert api.status_string(3) == "FA_ERR_ALIGNMENT"
+    assert api.status_string(99) == "FA_ERR_UNKNOWN"
+
+
+A = 1 << 20  # a fake, 16-byte-aligned device address: never dereferenced by these checks
+
+
+def fwd(lib, q=A, k=A, v=A, o=A, lse=A, B=1, H=1, N=128, d=64, causal=0, scale=0.125):
+    return lib.fa_forward(q, k, v, o, lse, B, H, N, d, causal, scale, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(B=-1), 1), (dict(H=-2), 1), (dict(N=-5), 1),
+    (dict(causal=2), 1), (dict(scale=0.0), 1), (dict(scale=-1.0), 1),
+    (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1),
+    (dict(d=32), 2), (dict(d=96), 2), (dict(d=256), 2),
+    (dict(q=0), 1), (dict(lse=0), 1),
+    (dict(q=A + 8), 3), (dict(o=A + 2), 3), (dict(lse=A + 2), 3),
+])
+def test_forward_rejects(lib, kw, status):
+    assert fwd(lib, **kw) == status
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(H=0), dict(N=0), dict(N=0, q=0, k=0, v=0, o=0, lse=0)])
+def test_forward_empty_is_ok(lib, kw):
+    assert fwd(lib, **kw) == 0
+
+
+def bwd(lib, B=1, H=1, N=128, d=64, causal=0, scale=0.125, ws=0, **ptrs):
+    p = {n: A for n in ("q", "k", "v", "o", "lse", "do", "dq", "dk", "dv")}
+    p.update(ptrs)
+    return lib.fa_backward(p["q"], p["k"], p["v"], p["o"], p["lse"], p["do"], p["dq"], p["dk"],
+                           p["dv"], B, H, N, d, causal, scale, ws, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(B=-1), 1), (dict(causal=3), 1), (dict(scale=0.0), 1), (dict(d=80), 2),
+    (dict(dq=0), 1), (dict(do=0), 1), (dict(dk=A + 4), 3), (dict(lse=A + 1), 3),
+    (dict(ws=A + 16), 3),
+])
+def test_backward_rejects(lib, kw, status):
+    assert bwd(lib, **kw) == status
+
+
+def test_backward_empty_is_ok(lib):
+    assert bwd(lib, N=0) == 0 and bwd(lib, B=0) == 0
+
+
+def test_workspace_bytes(lib):
+    from exact_io_aware_fa_gb300 import api
+    assert api.backward_workspace_bytes(1, 1, 128, 64) == 2 * 128 * 4 + 128 * 64 * 4
+    # N is padded to a multiple of 128
+    assert api.backward_workspace_bytes(2, 3, 129, 128) == 6 * 256 * 4 * 2 + 6 * 256 * 128 * 4
+    assert api.backward_workspace_bytes(0, 1, 128, 64) == 0
+    assert api.backward_workspace_bytes(1, 1, 128, 48) == 0
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    from exact_io_aware_fa_gb300 import api
+    saved = api._LIB
+    try:
+        api._LIB = None
+        with pytest.raises(api.FaLibraryMissing):
+            api.library(str(tmp_path / "nope.so"))
+    finally:
+        api._LIB = saved
