@@ -1,0 +1,376 @@
+"""Benchmark: exact attention forward + backward (one training step of the attention op)
+on the non-causal workload B=4, H=16, N=2048, d=64 (bf16, scale 1/sqrt(d)), through the C ABI.
+
+Prints ONE JSON line (rank 0). ``value`` is whole-job TFLOPS: forward FLOPs 4*B*H*N^2*d
+(halved for causal) plus backward FLOPs 2.5x that, divided by the device time of the timed
+steps (max over ranks). Each timed step runs fa_forward then fa_backward on inputs resident
+in HBM; L2 is flushed (a 512 MiB write) between timed steps, outside the timed events.
+
+``--impl reference`` times the fp64 CPU oracle (the reference arm of this repository) on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = dict(name="B4 H16 N2048 d64 non-causal fwd+bwd", B=4, H=16, N=2048, d=64,
+                causal=False, seed=1002)
+FWD_KERNEL_SRC = os.path.join(ROOT, "exact_io_aware_fa_gb300", "csrc", "fa_fwd.cu")
+BWD_KERNEL_SRC = os.path.join(ROOT, "exact_io_aware_fa_gb300", "csrc", "fa_bwd.cu")
+TRAFFIC_JSON = os.path.join(ROOT, "profiles", "traffic.json")
+L2_FLUSH_BYTES = 512 << 20
+
+
+def fwd_flops(B, H, N, d, causal):
+    f = 4.0 * B * H * N * N * d
+    return f / 2 if causal else f
+
+
+def bwd_flops(B, H, N, d, causal):
+    return 2.5 * fwd_flops(B, H, N, d, causal)
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def file_sha(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return dict(hbm_gbs=j["hbm_gbs"], bf16_tflops=j["bf16_tflops"],
+                    bf16_tflops_sustained=j.get("bf16_tflops_sustained"), source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0,
+                source="fallback")
+
+
+# ---- distributed plumbing (one process per GPU; no data-path collective) -----------------
+
+def dist_init(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", init_method="env://")
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---- clocks sampling ------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ---- oracle CPU baseline (bounded sample of the workload) -------------------------------------
+
+def oracle_sample_time(heads, want_seconds=None):
+    """Time the fp64 oracle forward + backward on `heads` heads of the workload; returns
+    (seconds, flops_of_sample, cores)."""
+    import oracle
+    from exact_io_aware_fa_gb300 import synthetic
+    w = WORKLOAD
+    bits = synthetic.attention_inputs(1, heads, w["N"], w["d"], seed=w["seed"], with_dout=True)
+    cores = oracle.default_threads()
+    orc = oracle.Oracle(0, threads=cores)
+    scale = 1.0 / math.sqrt(w["d"])
+    t0 = time.perf_counter()
+    orc.forward_bf16(bits["q"], bits["k"], bits["v"], w["causal"], scale)
+    orc.backward_bf16(bits["q"], bits["k"], bits["v"], bits["do"], w["causal"], scale)
+    dt = time.perf_counter() - t0
+    fl = fwd_flops(1, heads, w["N"], w["d"], w["causal"]) + bwd_flops(1, heads, w["N"], w["d"], w["causal"])
+    return dt, fl, cores
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    w = WORKLOAD
+    heads = 16
+    for _ in range(args.warmup):
+        oracle_sample_time(heads)
+    total_t, total_f = 0.0, 0.0
+    cores = 1
+    for _ in range(args.steps):
+        dt, fl, cores = oracle_sample_time(heads)
+        total_t += dt
+        total_f += fl
+    value = total_f / total_t / 1e12
+    line = {
+        "impl": "reference", "metric": "attention fwd+bwd TFLOPS (fp64 CPU oracle, sampled heads)",
+        "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w["name"], "global_batch": w["B"], "seq_len": w["N"],
+                   "heads": w["H"], "head_dim": w["d"], "causal": w["causal"],
+                   "sample": f"{heads} of {w['B'] * w['H']} heads per step", "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{heads} heads of B4 H16 N2048 d64, fwd+bwd, per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---- GPU arm -------------------------------------------------------------------------------------
+
+def run_ours(args, rank, world, local):
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    if rank == 0 or world == 1:
+        __graft_entry__.build()
+    barrier(world)
+    from exact_io_aware_fa_gb300 import api, synthetic
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = WORKLOAD
+    B, H, N, d, causal = w["B"], w["H"], w["N"], w["d"], w["causal"]
+    scale = 1.0 / math.sqrt(d)
+    # Weak scaling: every rank runs the full workload on its own heads (its own seed).
+    bits = synthetic.attention_inputs(B, H, N, d, seed=w["seed"] + 1000 * rank, with_dout=True)
+
+    def dev_t(b):
+        return torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    q, k, v, do = (dev_t(bits[n]) for n in ("q", "k", "v", "do"))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    ws = torch.empty(api.backward_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    s = stream.cuda_stream
+    ci = int(bool(causal))
+
+    def step_fwd():
+        st = api.forward_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                             lse.data_ptr(), B, H, N, d, ci, scale, s)
+        assert st == 0, api.status_string(st)
+
+    def step_bwd():
+        st = api.backward_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                              lse.data_ptr(), do.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                              dv.data_ptr(), B, H, N, d, ci, scale, ws.data_ptr(), s)
+        assert st == 0, api.status_string(st)
+
+    for _ in range(args.warmup):
+        step_fwd()
+        step_bwd()
+        flush.zero_()
+    torch.cuda.synchronize()
+    assert api.device_error() == 0
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        e0, e1, e2 = ev[i]
+        e0.record(stream)
+        step_fwd()
+        e1.record(stream)
+        step_bwd()
+        e2.record(stream)
+        flush.zero_()  # L2 flush between timed steps (outside the events)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    assert api.device_error() == 0
+    fwd_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
+    bwd_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
+    total_ms = sum(fwd_ms) + sum(bwd_ms)
+    total_ms = max_over_ranks(total_ms, world)
+    ff = fwd_flops(B, H, N, d, causal)
+    bf = bwd_flops(B, H, N, d, causal)
+    value = world * args.steps * (ff + bf) / (total_ms * 1e-3) / 1e12
+    peaks = load_peaks()
+    fwd_avg = sum(fwd_ms) / len(fwd_ms)
+    bwd_avg = sum(bwd_ms) / len(bwd_ms)
+    fwd_tf = ff / (fwd_avg * 1e-3) / 1e12
+    bwd_tf = bf / (bwd_avg * 1e-3) / 1e12
+    dominant = "fa_bwd" if bwd_avg >= fwd_avg else "fa_fwd"
+    dom_tf = bwd_tf if dominant == "fa_bwd" else fwd_tf
+
+    traffic = None
+    if os.path.exists(TRAFFIC_JSON):
+        with open(TRAFFIC_JSON) as f:
+            tj = json.load(f)
+        ent = tj.get(dominant)
+        src = BWD_KERNEL_SRC if dominant == "fa_bwd" else FWD_KERNEL_SRC
+        if ent and ent.get("source_sha") == file_sha(src) and ent.get("workload") == w["name"]:
+            traffic = ent.get("bytes_per_launch")
+
+    # ---- end to end through the public API with host buffers ----------------------------------
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv, hdo = (torch.from_numpy(bits[n].view(np.int16)).view(torch.bfloat16).pin_memory()
+                           for n in ("q", "k", "v", "do"))
+        ho = torch.empty_like(hq).pin_memory()
+        hlse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+        hdq, hdk, hdv = (torch.empty_like(hq).pin_memory() for _ in range(3))
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+        d2h = sum(t.numel() * t.element_size() for t in (ho, hlse, hdq, hdk, hdv))
+
+        def e2e_step():
+            for dst, src in ((q, hq), (k, hk), (v, hv), (do, hdo)):
+                dst.copy_(src, non_blocking=True)
+            api.forward(q, k, v, causal=causal, scale=scale, out=o, lse=lse)
+            api.backward(q, k, v, o, lse, do, causal=causal, scale=scale, dq=dq, dk=dk, dv=dv,
+                         workspace=ws)
+            for dst, src in ((ho, o), (hlse, lse), (hdq, dq), (hdk, dk), (hdv, dv)):
+                dst.copy_(src, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ea.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        eb.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(ea.elapsed_time(eb), world)
+        e2e = {"value": world * args.steps * (ff + bf) / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e2e_ms / args.steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        heads = 8
+        dt, fl, cores = oracle_sample_time(heads)
+        cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": f"{heads} of 64 heads of the workload, fwd+bwd, {dt:.1f} s"}
+
+    if rank != 0:
+        return
+    line = {
+        "metric": "attention fwd+bwd TFLOPS (bf16 in, fp32 accumulate), 1 step = fa_forward + fa_backward",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w["name"], "global_batch": w["B"] * world, "seq_len": N,
+                   "heads": H, "head_dim": d, "causal": causal,
+                   "parallelism": f"heads-replica x{world}" if world > 1 else "single",
+                   "l2": "flushed between timed steps (512 MiB write outside the events)"},
+        "fwd": {"ms": fwd_avg, "tflops": fwd_tf, "frac_of_peak": fwd_tf / peaks["bf16_tflops"]},
+        "bwd": {"ms": bwd_avg, "tflops": bwd_tf, "frac_of_peak": bwd_tf / peaks["bf16_tflops"]},
+        "roofline": {"kernel": dominant, "bound": "tensor", "achieved": dom_tf,
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": dom_tf / peaks["bf16_tflops"], "traffic": traffic,
+                     "peak_source": f"{peaks['source']} bf16 burst"},
+        "e2e": e2e,
+        "gpu_launches": args.steps * 4,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_init(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,7 +1,566 @@
-// fa_bwd.cu -- backward kernels (placeholder until the recompute kernels land).
+// fa_bwd.cu -- exact attention backward for sm_103a, by recomputation from the saved LSE.
+//
+// Method ("FlashAttention: from IO-Aware Attention to GPU work partitioning",
+// blog.euler0525.cn, sections "Tiling、Fusion 与 Backward Recomputation",
+// "FlashAttention-2" and "Sequence Parallelism"):
+//   P_ij = exp(S_ij - L_i) rebuilt tile by tile from Q, K and the saved L = LSE;
+//   dV = P^T dO,  dP = dO V^T,  D_i = O_i . dO_i,  dS = P (.) (dP - D),
+//   dQ = scale dS K,  dK = scale dS^T Q  (the scale factors follow from S = scale Q K^T).
+//   Work is partitioned over key tiles (column-oriented): each CTA owns one 128-key tile
+//   K_j, V_j and its dK_j, dV_j; contributions to dQ from different key tiles are added in
+//   fp32 with atomic reductions.
+//
+// Three kernels:
+//   fa_bwd_pre_kernel   D_i = sum_e dO_ie O_ie, LSE * log2(e) into a padded row-statistics
+//                       buffer (+inf / 0 on padded rows), dQ accumulator zeroed.
+//   fa_bwd_kernel<D>    per key tile: loop over query steps (from the diagonal when causal):
+//                       S^T = K Q_i^T and dP^T = V dO_i^T (tcgen05, TMEM), P^T and dS^T by the
+//                       compute warpgroup (one thread per key row), dV += P^T dO_i and
+//                       dK += dS^T Q_i (A operand from TMEM), dQ_i partial (A/B from smem),
+//                       drained from TMEM and reduced into the fp32 dQ accumulator.
+//   fa_bwd_dq_kernel    dQ = bf16(scale * dQacc).
+//
+// d = 128: query steps of 64 rows, the dQ partial computed transposed (dQ^T = K^T dS^T,
+//          M = d = 128) so its TMEM lanes are head-dim columns.
+// d = 64:  query steps of 128 rows, dQ = dS K with M = 128 query rows.
 #include "fa_common.cuh"
 #include "fa_launch.h"
 
 namespace fa {
-cudaError_t launch_backward(const BwdLaunch&, bool, cudaStream_t) { return cudaErrorNotSupported; }
+namespace {
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+    return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (!ptx::mbar_try_wait(bar, parity)) {
+        if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) break;
+    }
+}
+
+constexpr float kLog2e = 1.4426950408889634074f;
+
+// ----------------------------------------------------------------------------------------
+// Preprocess: one warp per row.
+// ----------------------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256)
+fa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
+                  const float* __restrict__ lse, float* __restrict__ stats,
+                  float* __restrict__ dq_acc, int N, int Npad, int BH) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long row_global = (long long)blockIdx.x * 8 + warp;  // over BH * Npad
+    if (row_global >= (long long)BH * Npad) return;
+    const int bh = (int)(row_global / Npad);
+    const int n = (int)(row_global % Npad);
+    constexpr int PER = D / 32;  // bf16 per lane
+    float dot = 0.f;
+    if (n < N) {
+        const size_t base = ((size_t)bh * N + n) * D + lane * PER;
+        if (PER == 4) {
+            const uint2 a = *reinterpret_cast<const uint2*>(o + base);
+            const uint2 b = *reinterpret_cast<const uint2*>(dout + base);
+            const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
+            const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
+            for (int i = 0; i < 2; ++i) {
+                const float2 fa = __bfloat1622float2(pa[i]);
+                const float2 fb = __bfloat1622float2(pb[i]);
+                dot = fmaf(fa.x, fb.x, dot);
+                dot = fmaf(fa.y, fb.y, dot);
+            }
+        } else {
+            const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(o + base);
+            const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(dout + base);
+            const float2 fa = __bfloat1622float2(a);
+            const float2 fb = __bfloat1622float2(b);
+            dot = fmaf(fa.x, fb.x, dot);
+            dot = fmaf(fa.y, fb.y, dot);
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+    if (lane == 0) {
+        const size_t si = (size_t)bh * Npad + n;
+        stats[si] = (n < N) ? lse[(size_t)bh * N + n] * kLog2e : __int_as_float(0x7f800000);
+        stats[(size_t)BH * Npad + si] = (n < N) ? dot : 0.f;
+    }
+    float4* acc = reinterpret_cast<float4*>(dq_acc + ((size_t)bh * Npad + n) * D);
+    if (lane < D / 4) acc[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// ----------------------------------------------------------------------------------------
+// dQ convert.
+// ----------------------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256)
+fa_bwd_dq_kernel(const float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dq, int N, int Npad,
+                 int BH, float scale) {
+    const long long idx8 = (long long)blockIdx.x * blockDim.x + threadIdx.x;  // 8 elements each
+    const long long total8 = (long long)BH * N * (D / 8);
+    if (idx8 >= total8) return;
+    const long long row = idx8 / (D / 8);
+    const int col8 = (int)(idx8 % (D / 8));
+    const int bh = (int)(row / N);
+    const int n = (int)(row % N);
+    const float4* src = reinterpret_cast<const float4*>(dq_acc + ((size_t)bh * Npad + n) * D + col8 * 8);
+    const float4 a = src[0], b = src[1];
+    uint4 w;
+    w.x = ptx::pack_bf16x2(a.x * scale, a.y * scale);
+    w.y = ptx::pack_bf16x2(a.z * scale, a.w * scale);
+    w.z = ptx::pack_bf16x2(b.x * scale, b.y * scale);
+    w.w = ptx::pack_bf16x2(b.z * scale, b.w * scale);
+    *reinterpret_cast<uint4*>(dq + ((size_t)bh * N + n) * D + col8 * 8) = w;
+}
+
+// ----------------------------------------------------------------------------------------
+// Main backward kernel.
+// ----------------------------------------------------------------------------------------
+template <int D>
+struct BwdCfg {
+    static constexpr int KT = 128;                    // keys per CTA
+    static constexpr int BMQ = (D == 128) ? 64 : 128; // query rows per step
+    static constexpr int NQS = 2;                     // Q/dO ring depth
+    static constexpr uint32_t KTILE = 128u * D * 2u;  // K or V tile bytes
+    static constexpr uint32_t KCHUNK = 128u * 128u;   // 128 rows x 64 cols
+    static constexpr uint32_t QTILE = (uint32_t)BMQ * D * 2u;
+    static constexpr uint32_t QCHUNK = (uint32_t)BMQ * 128u;  // BMQ rows x 64 cols
+    static constexpr uint32_t STAT_BYTES = (uint32_t)BMQ * 4u;
+    // stage: [Q][dO][LSE2][Dvec], padded to 1024
+    static constexpr uint32_t STAGE_BYTES = ((2 * QTILE + 2 * STAT_BYTES) + 1023u) / 1024u * 1024u;
+    static constexpr uint32_t DS_BYTES = (uint32_t)BMQ * 128u * 2u;  // dS tile (128 keys x BMQ)
+    static constexpr uint32_t OFF_K = 0;
+    static constexpr uint32_t OFF_V = OFF_K + KTILE;
+    static constexpr uint32_t OFF_ST = OFF_V + KTILE;
+    static constexpr uint32_t OFF_DS = OFF_ST + NQS * STAGE_BYTES;
+    static constexpr uint32_t OFF_BAR = OFF_DS + 2 * DS_BYTES;
+    static constexpr uint32_t SMEM_BYTES = OFF_BAR + 512 + 1024;
+    static constexpr int THREADS = 384;
+    // TMEM columns
+    static constexpr uint32_t DV_COL = 0;
+    static constexpr uint32_t DK_COL = (uint32_t)D;
+    static constexpr uint32_t S_COL = 2u * D;
+    static constexpr uint32_t DP_COL = S_COL + BMQ;
+    static constexpr uint32_t DQ_COL = 384;
+};
+
+struct BwdBars {
+    uint64_t kv_full;
+    uint64_t q_full[2], q_empty[2];
+    uint64_t s_full, p_ready, mma_done;
+    uint64_t ds_free[2];
+    uint64_t dq_full, dq_free;
+    uint64_t final_bar;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(384, 1)
+fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+              const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
+              const float* __restrict__ stats, float* __restrict__ dq_acc, const int N,
+              const int Npad, const int BH, const int nkb, const float c, const float scale,
+              int* err) {
+    using C = BwdCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align1024(smem_raw);
+    BwdBars* bars = reinterpret_cast<BwdBars*>(smem + C::OFF_BAR);
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+
+    const int bh = blockIdx.x / nkb;
+    const int kb = blockIdx.x % nkb;
+    const int key0 = kb * C::KT;
+    const int nq_total = (N + C::BMQ - 1) / C::BMQ;
+    const int i0 = CAUSAL ? (key0 / C::BMQ) : 0;
+    const int nsteps = nq_total - i0;  // >= 1 because key0 < N
+
+    if (tid == 0) {
+        ptx::mbar_init(ptx::smem_addr(&bars->kv_full), 1);
+        for (int s = 0; s < C::NQS; ++s) {
+            ptx::mbar_init(ptx::smem_addr(&bars->q_full[s]), 1);
+            ptx::mbar_init(ptx::smem_addr(&bars->q_empty[s]), 1);
+        }
+        ptx::mbar_init(ptx::smem_addr(&bars->s_full), 1);
+        ptx::mbar_init(ptx::smem_addr(&bars->p_ready), 128);
+        ptx::mbar_init(ptx::smem_addr(&bars->mma_done), 1);
+        ptx::mbar_init(ptx::smem_addr(&bars->ds_free[0]), 1);
+        ptx::mbar_init(ptx::smem_addr(&bars->ds_free[1]), 1);
+        ptx::mbar_init(ptx::smem_addr(&bars->dq_full), 1);
+        ptx::mbar_init(ptx::smem_addr(&bars->dq_free), 128);
+        ptx::mbar_init(ptx::smem_addr(&bars->final_bar), 1);
+        bars->abort_flag = 0;
+        ptx::fence_barrier_init();
+        ptx::tma_prefetch_desc(&tm_q);
+        ptx::tma_prefetch_desc(&tm_k);
+        ptx::tma_prefetch_desc(&tm_v);
+        ptx::tma_prefetch_desc(&tm_do);
+        ptx::tma_prefetch_desc(&tm_dk);
+        ptx::tma_prefetch_desc(&tm_dv);
+    }
+    if (warp == 2) {
+        ptx::tmem_alloc(ptx::smem_addr(&bars->tmem_base), 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tbase = bars->tmem_base;
+    volatile int* abort_flag = &bars->abort_flag;
+    const uint32_t s_k = ptx::smem_addr(smem + C::OFF_K);
+    const uint32_t s_v = ptx::smem_addr(smem + C::OFF_V);
+    const uint32_t s_st = ptx::smem_addr(smem + C::OFF_ST);
+    const uint32_t s_ds = ptx::smem_addr(smem + C::OFF_DS);
+
+    if (warp == 0) {
+        // ================================ TMA producer ================================
+        if (lane == 0) {
+            const uint64_t pol_keep = ptx::l2_policy_evict_last();
+            const uint32_t b_kv = ptx::smem_addr(&bars->kv_full);
+            ptx::mbar_arrive_expect_tx(b_kv, 2 * C::KTILE);
+            for (int ch = 0; ch < D / 64; ++ch) {
+                ptx::tma_load_3d(s_k + ch * C::KCHUNK, &tm_k, b_kv, ch * 64, key0, bh);
+                ptx::tma_load_3d(s_v + ch * C::KCHUNK, &tm_v, b_kv, ch * 64, key0, bh);
+            }
+            int issued = 0;
+            for (int si = 0; si < nsteps; ++si) {
+                const int st = si % C::NQS;
+                const uint32_t ph = (uint32_t)(si / C::NQS) & 1u;
+                if (!wait_phase(ptx::smem_addr(&bars->q_empty[st]), ph ^ 1u, abort_flag, err,
+                                kDevTimeoutConsumer))
+                    break;
+                const int q0 = (i0 + si) * C::BMQ;
+                const uint32_t b_q = ptx::smem_addr(&bars->q_full[st]);
+                const uint32_t base = s_st + st * C::STAGE_BYTES;
+                ptx::mbar_arrive_expect_tx(b_q, 2 * C::QTILE + 2 * C::STAT_BYTES);
+                for (int ch = 0; ch < D / 64; ++ch) {
+                    ptx::tma_load_3d_hint(base + ch * C::QCHUNK, &tm_q, b_q, ch * 64, q0, bh, pol_keep);
+                    ptx::tma_load_3d_hint(base + C::QTILE + ch * C::QCHUNK, &tm_do, b_q, ch * 64, q0,
+                                          bh, pol_keep);
+                }
+                const float* lse2 = stats + (size_t)bh * Npad + q0;
+                const float* dvec = stats + (size_t)BH * Npad + (size_t)bh * Npad + q0;
+                ptx::bulk_load(base + 2 * C::QTILE, lse2, C::STAT_BYTES, b_q);
+                ptx::bulk_load(base + 2 * C::QTILE + C::STAT_BYTES, dvec, C::STAT_BYTES, b_q);
+                ++issued;
+            }
+            drain_wait(b_kv, 0);
+            for (int si = max(0, issued - C::NQS); si < issued; ++si)
+                drain_wait(ptx::smem_addr(&bars->q_full[si % C::NQS]), (uint32_t)(si / C::NQS) & 1u);
+        }
+    } else if (warp == 1) {
+        // ================================ MMA issuer ==================================
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = ptx::idesc_bf16(128, C::BMQ, false, false);  // S^T, dP^T
+            constexpr uint32_t idesc_kv = ptx::idesc_bf16(128, D, false, true);       // dV, dK
+            // dQ: d=128 -> dQ^T = K^T dS^T (M=d, N=BMQ); d=64 -> dQ = dS K (M=BMQ, N=d)
+            constexpr uint32_t idesc_q = (D == 128) ? ptx::idesc_bf16(128, C::BMQ, true, true)
+                                                    : ptx::idesc_bf16(128, D, true, true);
+            bool ok = wait_phase(ptx::smem_addr(&bars->kv_full), 0, abort_flag, err, kDevTimeoutLoad);
+            for (int si = 0; ok && si < nsteps; ++si) {
+                const int st = si % C::NQS;
+                const uint32_t ph = (uint32_t)(si / C::NQS) & 1u;
+                const uint32_t qa = s_st + st * C::STAGE_BYTES;
+                const uint32_t doa = qa + C::QTILE;
+                ok = wait_phase(ptx::smem_addr(&bars->q_full[st]), ph, abort_flag, err, kDevTimeoutLoad);
+                if (!ok) break;
+                if (si > 0) {
+                    // dV/dK of the previous step read P^T/dS^T from the S/dP columns.
+                    ok = wait_phase(ptx::smem_addr(&bars->mma_done), (uint32_t)(si - 1) & 1u,
+                                    abort_flag, err, kDevTimeoutMma);
+                    if (!ok) break;
+                }
+                ptx::tc_fence_after();
+                // S^T = K Q^T and dP^T = V dO^T (K-major operands, K dimension = d).
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t koff = (kk >> 2) * C::KCHUNK + (kk & 3) * 32;
+                    const uint32_t qoff = (kk >> 2) * C::QCHUNK + (kk & 3) * 32;
+                    ptx::mma_ss(tbase + C::S_COL, ptx::sdesc_sw128(s_k + koff, 16, 1024),
+                                ptx::sdesc_sw128(qa + qoff, 16, 1024), idesc_s, kk > 0);
+                }
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t koff = (kk >> 2) * C::KCHUNK + (kk & 3) * 32;
+                    const uint32_t qoff = (kk >> 2) * C::QCHUNK + (kk & 3) * 32;
+                    ptx::mma_ss(tbase + C::DP_COL, ptx::sdesc_sw128(s_v + koff, 16, 1024),
+                                ptx::sdesc_sw128(doa + qoff, 16, 1024), idesc_s, kk > 0);
+                }
+                ptx::mma_commit(ptx::smem_addr(&bars->s_full));
+                ok = wait_phase(ptx::smem_addr(&bars->p_ready), (uint32_t)si & 1u, abort_flag, err,
+                                kDevTimeoutSoftmax);
+                if (!ok) break;
+                ptx::tc_fence_after();
+                // dV += P^T dO and dK += dS^T Q (A from TMEM, B MN-major, K dimension = BMQ).
+#pragma unroll
+                for (int kk = 0; kk < C::BMQ / 16; ++kk) {
+                    ptx::mma_ts(tbase + C::DV_COL, tbase + C::S_COL + kk * 8,
+                                ptx::sdesc_sw128(doa + kk * 2048, C::QCHUNK, 1024), idesc_kv,
+                                (si > 0 || kk > 0) ? 1u : 0u);
+                }
+#pragma unroll
+                for (int kk = 0; kk < C::BMQ / 16; ++kk) {
+                    ptx::mma_ts(tbase + C::DK_COL, tbase + C::DP_COL + kk * 8,
+                                ptx::sdesc_sw128(qa + kk * 2048, C::QCHUNK, 1024), idesc_kv,
+                                (si > 0 || kk > 0) ? 1u : 0u);
+                }
+                ptx::mma_commit(ptx::smem_addr(&bars->mma_done));
+                ptx::mma_commit(ptx::smem_addr(&bars->q_empty[st]));
+                if (si > 0) {
+                    ok = wait_phase(ptx::smem_addr(&bars->dq_free), (uint32_t)(si - 1) & 1u,
+                                    abort_flag, err, kDevTimeoutSoftmax);
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+                }
+                const uint32_t dsa = s_ds + (uint32_t)(si & 1) * C::DS_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < C::KT / 16; ++kk) {
+                    if (D == 128) {
+                        // dQ^T = K^T dS^T: A = K as MN-major [d x keys], B = dS as MN-major [q x keys]
+                        ptx::mma_ss(tbase + C::DQ_COL, ptx::sdesc_sw128(s_k + kk * 2048, C::KCHUNK, 1024),
+                                    ptx::sdesc_sw128(dsa + kk * 2048, 128u * 128u, 1024), idesc_q,
+                                    kk > 0);
+                    } else {
+                        // dQ = dS K: A = dS as MN-major [q x keys], B = K as MN-major [d x keys]
+                        ptx::mma_ss(tbase + C::DQ_COL, ptx::sdesc_sw128(dsa + kk * 2048, 128u * 128u, 1024),
+                                    ptx::sdesc_sw128(s_k + kk * 2048, C::KCHUNK, 1024), idesc_q,
+                                    kk > 0);
+                    }
+                }
+                ptx::mma_commit(ptx::smem_addr(&bars->dq_full));
+                ptx::mma_commit(ptx::smem_addr(&bars->ds_free[si & 1]));
+            }
+            ptx::mma_commit(ptx::smem_addr(&bars->final_bar));
+            drain_wait(ptx::smem_addr(&bars->final_bar), 0);
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // ============== compute warpgroup: P^T and dS^T, one thread per key row ==============
+        const int wq = warp & 3;
+        const int k = wq * 32 + lane;  // key row within the tile
+        const int key = key0 + k;
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        const uint32_t t_s = tbase + lane_off + C::S_COL;
+        const uint32_t t_dp = tbase + lane_off + C::DP_COL;
+        bool ok = true;
+        for (int si = 0; si < nsteps; ++si) {
+            const int st = si % C::NQS;
+            const int q0 = (i0 + si) * C::BMQ;
+            ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->s_full), (uint32_t)si & 1u,
+                                                    abort_flag, err, kDevTimeoutMma));
+            if (!ok) break;
+            ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->q_full[st]),
+                                                    (uint32_t)(si / C::NQS) & 1u, abort_flag, err,
+                                                    kDevTimeoutLoad));
+            if (!ok) break;
+            if (si >= 2) {
+                ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->ds_free[si & 1]),
+                                                        (uint32_t)((si >> 1) - 1) & 1u, abort_flag,
+                                                        err, kDevTimeoutMma));
+                if (!ok) break;
+            }
+            ptx::tc_fence_after();
+            const float* lse2 = reinterpret_cast<const float*>(smem + C::OFF_ST + st * C::STAGE_BYTES + 2 * C::QTILE);
+            const float* dvec = lse2 + C::BMQ;
+            uint8_t* dsbuf = smem + C::OFF_DS + (si & 1) * C::DS_BYTES;
+            const bool need_mask = CAUSAL && (q0 < key0 + C::KT - 1);
+#pragma unroll 1
+            for (int cc = 0; cc < C::BMQ / 32; ++cc) {
+                uint32_t sv[32], dpv[32];
+                ptx::tmem_ld32_nowait(t_s + 32 * cc, sv);
+                ptx::tmem_ld32_nowait(t_dp + 32 * cc, dpv);
+                ptx::tmem_wait_ld(sv);
+                ptx::tmem_wait_ld(dpv);
+                float p[32], ds[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int qi = 32 * cc + j;
+                    float pj = ptx::ex2_approx(fmaf(__uint_as_float(sv[j]), c, -lse2[qi]));
+                    if (need_mask && key > q0 + qi) pj = 0.f;
+                    p[j] = pj;
+                    ds[j] = pj * (__uint_as_float(dpv[j]) - dvec[qi]);
+                }
+                uint32_t pk[16], dk[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    pk[j] = ptx::pack_bf16x2(p[2 * j], p[2 * j + 1]);
+                    dk[j] = ptx::pack_bf16x2(ds[2 * j], ds[2 * j + 1]);
+                }
+                ptx::tmem_st16(t_s + 16 * cc, pk);
+                ptx::tmem_st16(t_dp + 16 * cc, dk);
+                // dS row k (queries contiguous) into the 128B-swizzled dS tile.
+                uint8_t* region = dsbuf + (cc >> 1) * (128u * 128u);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    uint4 w = make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
+                    *reinterpret_cast<uint4*>(region + sw128_offset((uint32_t)k, (uint32_t)((cc & 1) * 4 + u))) = w;
+                }
+            }
+            ptx::tmem_wait_st();
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(ptx::smem_addr(&bars->p_ready));
+        }
+        // ---- epilogue: dV -> bf16 -> smem (stage 0 area) -> TMA store ----
+        if (ok) ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->mma_done),
+                                                        (uint32_t)(nsteps - 1) & 1u, abort_flag,
+                                                        err, kDevTimeoutMma));
+        if (ok) {
+            ptx::tc_fence_after();
+            uint8_t* stage = smem + C::OFF_ST;
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+                uint32_t v[32];
+                ptx::tmem_ld32(tbase + lane_off + C::DV_COL + 32 * cc, v);
+                uint8_t* chunk = stage + (cc >> 1) * C::KCHUNK;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    uint4 w;
+                    w.x = ptx::pack_bf16x2(__uint_as_float(v[8 * u + 0]), __uint_as_float(v[8 * u + 1]));
+                    w.y = ptx::pack_bf16x2(__uint_as_float(v[8 * u + 2]), __uint_as_float(v[8 * u + 3]));
+                    w.z = ptx::pack_bf16x2(__uint_as_float(v[8 * u + 4]), __uint_as_float(v[8 * u + 5]));
+                    w.w = ptx::pack_bf16x2(__uint_as_float(v[8 * u + 6]), __uint_as_float(v[8 * u + 7]));
+                    *reinterpret_cast<uint4*>(chunk + sw128_offset((uint32_t)k, (uint32_t)((cc & 1) * 4 + u))) = w;
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::named_bar_sync(1, 128);
+            if (k == 0) {
+                for (int ch = 0; ch < D / 64; ++ch)
+                    ptx::tma_store_3d(&tm_dv, ptx::smem_addr(stage + ch * C::KCHUNK), ch * 64, key0, bh);
+                ptx::bulk_commit();
+                ptx::bulk_wait_read_all();
+            }
+        }
+    } else if (warp >= 8) {
+        // ============== dQ drain warpgroup, then the dK epilogue ==============
+        const int wq = warp & 3;
+        const int r = wq * 32 + lane;  // TMEM lane: d index (d=128) or query row (d=64)
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        bool ok = true;
+        for (int si = 0; si < nsteps; ++si) {
+            const int q0 = (i0 + si) * C::BMQ;
+            ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->dq_full), (uint32_t)si & 1u,
+                                                    abort_flag, err, kDevTimeoutMma));
+            if (!ok) break;
+            ptx::tc_fence_after();
+            uint32_t a[32], b[32];
+            ptx::tmem_ld32_nowait(tbase + lane_off + C::DQ_COL, a);
+            ptx::tmem_ld32_nowait(tbase + lane_off + C::DQ_COL + 32, b);
+            ptx::tmem_wait_ld(a);
+            ptx::tmem_wait_ld(b);
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(ptx::smem_addr(&bars->dq_free));
+            if (D == 128) {
+                // lane r = head-dim column; 64 query rows -> coalesced across the warp
+                float* base = dq_acc + ((size_t)bh * Npad + q0) * D + r;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    atomicAdd(base + (size_t)j * D, __uint_as_float(a[j]));
+                    atomicAdd(base + (size_t)(32 + j) * D, __uint_as_float(b[j]));
+                }
+            } else {
+                // lane r = query row; 64 head-dim columns
+                float4* row = reinterpret_cast<float4*>(dq_acc + ((size_t)bh * Npad + q0 + r) * D);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    atomicAdd(row + j, make_float4(__uint_as_float(a[4 * j]), __uint_as_float(a[4 * j + 1]),
+                                                   __uint_as_float(a[4 * j + 2]), __uint_as_float(a[4 * j + 3])));
+                    atomicAdd(row + 8 + j, make_float4(__uint_as_float(b[4 * j]), __uint_as_float(b[4 * j + 1]),
+                                                       __uint_as_float(b[4 * j + 2]), __uint_as_float(b[4 * j + 3])));
+                }
+            }
+        }
+        // ---- epilogue: dK * scale -> bf16 -> smem (stage 1 area) -> TMA store ----
+        if (ok) ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->mma_done),
+                                                        (uint32_t)(nsteps - 1) & 1u, abort_flag,
+                                                        err, kDevTimeoutMma));
+        if (ok) {
+            ptx::tc_fence_after();
+            uint8_t* stage = smem + C::OFF_ST + C::STAGE_BYTES;
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+                uint32_t v[32];
+                ptx::tmem_ld32(tbase + lane_off + C::DK_COL + 32 * cc, v);
+                uint8_t* chunk = stage + (cc >> 1) * C::KCHUNK;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    uint4 w;
+                    w.x = ptx::pack_bf16x2(__uint_as_float(v[8 * u + 0]) * scale, __uint_as_float(v[8 * u + 1]) * scale);
+                    w.y = ptx::pack_bf16x2(__uint_as_float(v[8 * u + 2]) * scale, __uint_as_float(v[8 * u + 3]) * scale);
+                    w.z = ptx::pack_bf16x2(__uint_as_float(v[8 * u + 4]) * scale, __uint_as_float(v[8 * u + 5]) * scale);
+                    w.w = ptx::pack_bf16x2(__uint_as_float(v[8 * u + 6]) * scale, __uint_as_float(v[8 * u + 7]) * scale);
+                    *reinterpret_cast<uint4*>(chunk + sw128_offset((uint32_t)r, (uint32_t)((cc & 1) * 4 + u))) = w;
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::named_bar_sync(2, 128);
+            if (r == 0) {
+                for (int ch = 0; ch < D / 64; ++ch)
+                    ptx::tma_store_3d(&tm_dk, ptx::smem_addr(stage + ch * C::KCHUNK), ch * 64, key0, bh);
+                ptx::bulk_commit();
+                ptx::bulk_wait_read_all();
+            }
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tbase, 512);
+    }
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t stream) {
+    using C = BwdCfg<D>;
+    // 1. preprocess
+    {
+        const long long rows = (long long)a.BH * a.Npad;
+        const long long blocks = (rows + 7) / 8;
+        if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+        fa_bwd_pre_kernel<D><<<(unsigned)blocks, 256, 0, stream>>>(
+            static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.lse,
+            a.stats, a.dq_acc, a.N, a.Npad, a.BH);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    // 2. main
+    {
+        auto kern = fa_bwd_kernel<D, CAUSAL>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        const int nkb = (a.N + C::KT - 1) / C::KT;
+        const long long blocks = (long long)nkb * a.BH;
+        if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+        kern<<<(unsigned)blocks, C::THREADS, C::SMEM_BYTES, stream>>>(
+            a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dk, a.tm_dv, a.stats, a.dq_acc, a.N, a.Npad, a.BH,
+            nkb, a.c, a.scale, a.err);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    // 3. dQ convert
+    {
+        const long long total8 = (long long)a.BH * a.N * (D / 8);
+        const long long blocks = (total8 + 255) / 256;
+        if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+        fa_bwd_dq_kernel<D><<<(unsigned)blocks, 256, 0, stream>>>(
+            a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), a.N, a.Npad, a.BH, a.scale);
+        return cudaGetLastError();
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_backward(const BwdLaunch& a, bool causal, cudaStream_t stream) {
+    if (a.d == 64) return causal ? launch_bwd_t<64, true>(a, stream) : launch_bwd_t<64, false>(a, stream);
+    if (a.d == 128) return causal ? launch_bwd_t<128, true>(a, stream) : launch_bwd_t<128, false>(a, stream);
+    return cudaErrorInvalidValue;
+}
+
 }  // namespace fa
