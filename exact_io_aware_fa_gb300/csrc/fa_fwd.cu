@@ -46,14 +46,28 @@ struct FwdCfg {
     static constexpr uint32_t SMEM_BYTES = OFF_BAR + 512 + 1024;  // + alignment slack
     static constexpr int THREADS = 384;
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t TMEM_O = 256;  // first O column
+    // d = 64: S_0, S_1 [0,256), O_0, O_1 [256,384), P_0, P_1 [384,512) -- P has its own
+    //         columns, so S_t(j+1) can be computed while the softmax still works on tile j.
+    // d = 128: S_0, S_1 [0,256), O_0, O_1 [256,512), P_t written over the S_t columns.
+    static constexpr bool P_SEPARATE = (D == 64);
+    __host__ __device__ static constexpr uint32_t s_col(int t) { return (uint32_t)(t * 128); }
+    __host__ __device__ static constexpr uint32_t o_col(int t) { return 256u + (uint32_t)(t * D); }
+    __host__ __device__ static constexpr uint32_t p_col(int t) {
+        return P_SEPARATE ? 384u + (uint32_t)(t * 64) : (uint32_t)(t * 128);
+    }
 };
+
+// The reference max moves as soon as the row max grows (threshold 0): the largest score of a
+// row then gets p = exp2(0) = 1 exactly, so a peaked row's dominant weight carries no bf16
+// rounding. (A stale reference, allowed to lag the max by a few units of log2, skips more
+// O rescales but measurably loosens O in peaked rows.)
+constexpr float kTau = 0.0f;
 
 struct FwdBars {
     uint64_t q_full;
     uint64_t k_full[3], k_empty[3];
     uint64_t v_full[3], v_empty[3];
-    uint64_t s_full[2], p_full[2], o_done[2];
+    uint64_t s_full[2], s_free[2], p_full[2], o_done[2];
     uint64_t mma_final;
     uint32_t tmem_base;
     int abort_flag;
@@ -108,6 +122,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         }
         for (int t = 0; t < 2; ++t) {
             ptx::mbar_init(ptx::smem_addr(&bars->s_full[t]), 1);
+            ptx::mbar_init(ptx::smem_addr(&bars->s_free[t]), C::BM);
             ptx::mbar_init(ptx::smem_addr(&bars->p_full[t]), C::BM);
             ptx::mbar_init(ptx::smem_addr(&bars->o_done[t]), 1);
         }
@@ -182,7 +197,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             constexpr uint32_t idesc_s = ptx::idesc_bf16(128, C::BN, false, false);
             constexpr uint32_t idesc_o = ptx::idesc_bf16(128, D, false, true);
             auto issue_s = [&](int t, int stage) {
-                const uint32_t d_tmem = tbase + (uint32_t)(t * 128);
+                const uint32_t d_tmem = tbase + C::s_col(t);
                 const uint32_t qa = s_q + t * C::TILE_BYTES;
                 const uint32_t ka = s_k + stage * C::TILE_BYTES;
 #pragma unroll
@@ -193,14 +208,55 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 }
             };
             auto issue_pv = [&](int t, int stage, bool acc) {
-                const uint32_t d_tmem = tbase + C::TMEM_O + (uint32_t)(t * D);
-                const uint32_t p_tmem = tbase + (uint32_t)(t * 128);
+                const uint32_t d_tmem = tbase + C::o_col(t);
+                const uint32_t p_tmem = tbase + C::p_col(t);
                 const uint32_t va = s_v + stage * C::TILE_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < C::BN / 16; ++kk)
                     ptx::mma_ts(d_tmem, p_tmem + kk * 8,
                                 ptx::sdesc_sw128(va + kk * 2048, C::CHUNK_BYTES, 1024), idesc_o,
                                 (acc || kk > 0) ? 1u : 0u);
+            };
+            // S_t(j+1) may overwrite the S_t columns once the softmax has read S_t(j) (P in its
+            // own columns) or once O_t += P_t(j) V_j has consumed P_t(j) (P over S).
+            auto s_release = [&](int t) {
+                return C::P_SEPARATE ? ptx::smem_addr(&bars->s_free[t])
+                                     : ptx::smem_addr(&bars->o_done[t]);
+            };
+            auto issue_next_s = [&](int j1) -> bool {  // S for KV tile j1 >= 1
+                const int s1 = j1 % C::NS;
+                if (!wait_phase(ptx::smem_addr(&bars->k_full[s1]), (uint32_t)(j1 / C::NS) & 1u,
+                                abort_flag, err, kDevTimeoutLoad))
+                    return false;
+                ptx::tc_fence_after();
+                for (int t = 0; t < 2; ++t) {
+                    if (j1 >= ntile[t]) continue;
+                    if (!wait_phase(s_release(t), (uint32_t)(j1 - 1) & 1u, abort_flag, err,
+                                    kDevTimeoutSoftmax))
+                        return false;
+                    ptx::tc_fence_after();
+                    issue_s(t, s1);
+                    ptx::mma_commit(ptx::smem_addr(&bars->s_full[t]));
+                }
+                ptx::mma_commit(ptx::smem_addr(&bars->k_empty[s1]));
+                return true;
+            };
+            auto issue_pvs = [&](int j) -> bool {
+                const int s = j % C::NS;
+                if (!wait_phase(ptx::smem_addr(&bars->v_full[s]), (uint32_t)(j / C::NS) & 1u,
+                                abort_flag, err, kDevTimeoutLoad))
+                    return false;
+                for (int t = 0; t < 2; ++t) {
+                    if (j >= ntile[t]) continue;
+                    if (!wait_phase(ptx::smem_addr(&bars->p_full[t]), (uint32_t)j & 1u, abort_flag,
+                                    err, kDevTimeoutSoftmax))
+                        return false;
+                    ptx::tc_fence_after();
+                    issue_pv(t, s, j > 0);
+                    ptx::mma_commit(ptx::smem_addr(&bars->o_done[t]));
+                }
+                ptx::mma_commit(ptx::smem_addr(&bars->v_empty[s]));
+                return true;
             };
             bool ok = wait_phase(b_q_full, 0, abort_flag, err, kDevTimeoutLoad);
             if (ok) ok = wait_phase(ptx::smem_addr(&bars->k_full[0]), 0, abort_flag, err,
@@ -215,41 +271,13 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 ptx::mma_commit(ptx::smem_addr(&bars->k_empty[0]));
             }
             for (int j = 0; ok && j < nkv; ++j) {
-                const int s = j % C::NS;
-                const uint32_t ph = (uint32_t)(j / C::NS) & 1u;
-                ok = wait_phase(ptx::smem_addr(&bars->v_full[s]), ph, abort_flag, err,
-                                kDevTimeoutLoad);
-                if (!ok) break;
-                for (int t = 0; t < 2 && ok; ++t) {
-                    if (j >= ntile[t]) continue;
-                    ok = wait_phase(ptx::smem_addr(&bars->p_full[t]), (uint32_t)j & 1u, abort_flag,
-                                    err, kDevTimeoutSoftmax);
-                    if (!ok) break;
-                    ptx::tc_fence_after();
-                    issue_pv(t, s, j > 0);
-                    ptx::mma_commit(ptx::smem_addr(&bars->o_done[t]));
-                }
-                if (!ok) break;
-                ptx::mma_commit(ptx::smem_addr(&bars->v_empty[s]));
-                if (j + 1 < nkv) {
-                    const int s1 = (j + 1) % C::NS;
-                    const uint32_t ph1 = (uint32_t)((j + 1) / C::NS) & 1u;
-                    ok = wait_phase(ptx::smem_addr(&bars->k_full[s1]), ph1, abort_flag, err,
-                                    kDevTimeoutLoad);
-                    if (!ok) break;
-                    ptx::tc_fence_after();
-                    for (int t = 0; t < 2 && ok; ++t) {
-                        if (j + 1 >= ntile[t]) continue;
-                        // P_t(j) lives in the S_t columns: wait until O_t += P_t V_j has read it.
-                        ok = wait_phase(ptx::smem_addr(&bars->o_done[t]), (uint32_t)j & 1u,
-                                        abort_flag, err, kDevTimeoutMma);
-                        if (!ok) break;
-                        ptx::tc_fence_after();
-                        issue_s(t, s1);
-                        ptx::mma_commit(ptx::smem_addr(&bars->s_full[t]));
-                    }
-                    if (!ok) break;
-                    ptx::mma_commit(ptx::smem_addr(&bars->k_empty[s1]));
+                if (C::P_SEPARATE) {
+                    // Next scores first: they only wait for the softmax to have read S(j).
+                    if (j + 1 < nkv) ok = issue_next_s(j + 1);
+                    if (ok) ok = issue_pvs(j);
+                } else {
+                    ok = issue_pvs(j);
+                    if (ok && j + 1 < nkv) ok = issue_next_s(j + 1);
                 }
             }
             // Every MMA issued (and every commit arrive) must be done before TMEM and the
@@ -266,14 +294,19 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const int row = row0 + r;
         const int n = ntile[t];
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-        const uint32_t t_s = tbase + lane_off + (uint32_t)(t * 128);
-        const uint32_t t_o = tbase + lane_off + C::TMEM_O + (uint32_t)(t * D);
+        const uint32_t t_s = tbase + lane_off + C::s_col(t);
+        const uint32_t t_p = tbase + lane_off + C::p_col(t);
+        const uint32_t t_o = tbase + lane_off + C::o_col(t);
         const uint32_t b_s_full = ptx::smem_addr(&bars->s_full[t]);
+        const uint32_t b_s_free = ptx::smem_addr(&bars->s_free[t]);
         const uint32_t b_p_full = ptx::smem_addr(&bars->p_full[t]);
         const uint32_t b_o_done = ptx::smem_addr(&bars->o_done[t]);
 
-        float m = -INFINITY;  // running max of scale*log2(e)*s
-        float l = 0.f;        // running sum of exp2(c*s - m)
+        // Online softmax: m_ref (scaled log2 domain) moves when the row max exceeds it by more
+        // than kTau; when it moves, both l and the accumulator are rescaled by
+        // alpha = exp2(m_old - m_new). O is rescaled only when some row of the warp moved.
+        float m_ref = -INFINITY;  // reference (scaled log2 domain)
+        float l = 0.f;            // running sum of exp2(c*s - m_ref)
         bool ok = true;
         for (int j = 0; j < n; ++j) {
             ok = __all_sync(0xffffffffu, wait_phase(b_s_full, (uint32_t)j & 1u, abort_flag, err,
@@ -299,6 +332,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     s[96 + k] = __uint_as_float(u3[k]);
                 }
             }
+            if (C::P_SEPARATE) {
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(b_s_free);  // S_t columns may be overwritten now
+            }
             const int key0 = j * C::BN;
             const bool need_mask = (key0 + C::BN > N) || (CAUSAL && key0 + C::BN - 1 > row0);
             if (need_mask) {
@@ -308,49 +345,79 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     if (key >= N || (CAUSAL && key > row)) s[k] = -INFINITY;
                 }
             }
-            float mx = s[0];
+            // Row max: four independent chains of three-input max.
+            float a0 = s[0], a1 = s[1], a2 = s[2], a3 = s[3];
 #pragma unroll
-            for (int k = 1; k < C::BN; ++k) mx = fmaxf(mx, s[k]);
-            const float m_new = fmaxf(m, mx * c);
-            const float m_ref = (m_new == -INFINITY) ? 0.f : m_new;  // safe reference
-            const float alpha = ptx::ex2_approx(m - m_ref);
-            float rs = 0.f;
-#pragma unroll
-            for (int k = 0; k < C::BN; ++k) {
-                s[k] = ptx::ex2_approx(fmaf(s[k], c, -m_ref));
-                rs += s[k];
+            for (int k = 4; k < C::BN - 4; k += 8) {
+                a0 = ptx::fmax3(a0, s[k + 0], s[k + 1]);
+                a1 = ptx::fmax3(a1, s[k + 2], s[k + 3]);
+                a2 = ptx::fmax3(a2, s[k + 4], s[k + 5]);
+                a3 = ptx::fmax3(a3, s[k + 6], s[k + 7]);
             }
-            l = l * alpha + rs;
-            m = m_new;
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) pk[i] = ptx::pack_bf16x2(s[32 * g + 2 * i], s[32 * g + 2 * i + 1]);
-                ptx::tmem_st16(t_s + 16 * g, pk);
+            a0 = ptx::fmax3(a0, s[C::BN - 4], s[C::BN - 3]);
+            a1 = ptx::fmax3(a1, s[C::BN - 2], s[C::BN - 1]);
+            const float mc = ptx::fmax3(a0, a1, fmaxf(a2, a3)) * c;
+            const bool upd = mc > m_ref + kTau;  // false when the tile is fully masked
+            float alpha = 1.f;
+            if (upd) {
+                alpha = ptx::ex2_approx(m_ref - mc);  // 0 on the first visible tile
+                m_ref = mc;
             }
-            ptx::tmem_wait_st();
+            const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;  // safe reference
+            // p = exp2(c*s - m_ref) (packed FMA, then ex2), row sum over eight partials.
+            float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f, r4 = 0.f, r5 = 0.f, r6 = 0.f, r7 = 0.f;
+            uint32_t pk[C::BN / 2];
+#pragma unroll
+            for (int k = 0; k < C::BN; k += 8) {
+                ptx::ffma2(s[k + 0], s[k + 1], s[k + 0], s[k + 1], c, c, neg_m, neg_m);
+                ptx::ffma2(s[k + 2], s[k + 3], s[k + 2], s[k + 3], c, c, neg_m, neg_m);
+                ptx::ffma2(s[k + 4], s[k + 5], s[k + 4], s[k + 5], c, c, neg_m, neg_m);
+                ptx::ffma2(s[k + 6], s[k + 7], s[k + 6], s[k + 7], c, c, neg_m, neg_m);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) s[k + i] = ptx::ex2_approx(s[k + i]);
+                ptx::fadd2(r0, r1, r0, r1, s[k + 0], s[k + 1]);
+                ptx::fadd2(r2, r3, r2, r3, s[k + 2], s[k + 3]);
+                ptx::fadd2(r4, r5, r4, r5, s[k + 4], s[k + 5]);
+                ptx::fadd2(r6, r7, r6, r7, s[k + 6], s[k + 7]);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) pk[k / 2 + i] = ptx::pack_bf16x2(s[k + 2 * i], s[k + 2 * i + 1]);
+            }
+            l = l * alpha + (((r0 + r1) + (r2 + r3)) + ((r4 + r5) + (r6 + r7)));
             if (j > 0) {
-                // O_t += P_t(j-1) V must be complete before O_t is rescaled.
+                // O_t += P_t(j-1) V must be complete before P_t is overwritten (separate P
+                // columns) and before O_t is rescaled.
                 ok = __all_sync(0xffffffffu, wait_phase(b_o_done, (uint32_t)(j - 1) & 1u,
                                                         abort_flag, err, kDevTimeoutMma));
                 if (!ok) break;
                 ptx::tc_fence_after();
-                if (__any_sync(0xffffffffu, alpha != 1.f)) {
+                if (__any_sync(0xffffffffu, upd)) {
 #pragma unroll
                     for (int cc = 0; cc < D / 32; ++cc) {
                         uint32_t o[32];
                         ptx::tmem_ld32(t_o + cc * 32, o);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        for (int i = 0; i < 32; i += 2) {
+                            float x0, x1;
+                            ptx::fmul2(x0, x1, __uint_as_float(o[i]), __uint_as_float(o[i + 1]), alpha, alpha);
+                            o[i] = __float_as_uint(x0);
+                            o[i + 1] = __float_as_uint(x1);
+                        }
                         ptx::tmem_st32(t_o + cc * 32, o);
                     }
-                    ptx::tmem_wait_st();
                 }
             }
+#pragma unroll
+            for (int g = 0; g < C::BN / 32; ++g) {
+                uint32_t chunk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) chunk[i] = pk[16 * g + i];
+                ptx::tmem_st16(t_p + 16 * g, chunk);
+            }
+            ptx::tmem_wait_st();
             ptx::tc_fence_before();
             ptx::mbar_arrive(b_p_full);
         }
+        const float m = m_ref;
         if (ok && n > 0) {
             ok = __all_sync(0xffffffffu, wait_phase(b_o_done, (uint32_t)(n - 1) & 1u, abort_flag,
                                                     err, kDevTimeoutMma));
