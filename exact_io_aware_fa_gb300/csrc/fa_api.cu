@@ -68,18 +68,22 @@ fa_status get_err_ptr(int** out) {
     return FA_OK;
 }
 
-// 3-D tiled map over a contiguous bf16 [BH, N, d] tensor: dims {d, N, BH}, box {64, box_rows, 1},
-// 128-byte swizzle. Rows past N inside a box read as zero and are not written by stores.
-fa_status make_map(CUtensorMap* m, const void* base, int BH, int N, int d, int box_rows) {
+// 3-D tiled map over a contiguous [BH, N, d] tensor of bf16 (or fp32): dims {d, N, BH}, box
+// {128 bytes of columns, box_rows, 1}, 128-byte swizzle. Rows past N inside a box read as zero
+// and are not written by stores or reductions.
+fa_status make_map(CUtensorMap* m, const void* base, int BH, int N, int d, int box_rows,
+                   bool fp32 = false) {
     EncodeTiledFn enc = nullptr;
     fa_status st = get_encode(&enc);
     if (st != FA_OK) return st;
+    const cuuint64_t esz = fp32 ? 4u : 2u;
     cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
-    cuuint64_t strides[2] = {(cuuint64_t)d * 2u, (cuuint64_t)N * (cuuint64_t)d * 2u};
-    cuuint32_t box[3] = {64u, (cuuint32_t)box_rows, 1u};
+    cuuint64_t strides[2] = {(cuuint64_t)d * esz, (cuuint64_t)N * (cuuint64_t)d * esz};
+    cuuint32_t box[3] = {(cuuint32_t)(128u / esz), (cuuint32_t)box_rows, 1u};
     cuuint32_t estr[3] = {1u, 1u, 1u};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
-                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    CUresult r = enc(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                     const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         t_last_cuda_error = (int)r;
@@ -198,6 +202,10 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
     a.dq = dq;
     a.stats = static_cast<float*>(ws);
     a.dq_acc = static_cast<float*>(ws) + 2 * (size_t)BH * (size_t)Npad;
+    if ((st = make_map(&a.tm_dqacc, a.dq_acc, BH, Npad, d, q_rows, true)) != FA_OK) {
+        if (owned) cudaFreeAsync(ws, s);
+        return st;
+    }
     a.N = N;
     a.Npad = Npad;
     a.BH = BH;

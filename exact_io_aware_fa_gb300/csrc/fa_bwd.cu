@@ -8,16 +8,19 @@
 //   dQ = scale dS K,  dK = scale dS^T Q  (the scale factors follow from S = scale Q K^T).
 //   Work is partitioned over key tiles (column-oriented): each CTA owns one 128-key tile
 //   K_j, V_j and its dK_j, dV_j; contributions to dQ from different key tiles are added in
-//   fp32 with atomic reductions.
+//   fp32 with (bulk) atomic reductions.
 //
 // Three kernels:
 //   fa_bwd_pre_kernel   D_i = sum_e dO_ie O_ie, LSE * log2(e) into a padded row-statistics
 //                       buffer (+inf / 0 on padded rows), dQ accumulator zeroed.
 //   fa_bwd_kernel<D>    per key tile: loop over query steps (from the diagonal when causal):
-//                       S^T = K Q_i^T and dP^T = V dO_i^T (tcgen05, TMEM), P^T and dS^T by the
-//                       compute warpgroup (one thread per key row), dV += P^T dO_i and
-//                       dK += dS^T Q_i (A operand from TMEM), dQ_i partial (A/B from smem),
-//                       drained from TMEM and reduced into the fp32 dQ accumulator.
+//                       S^T = K Q_i^T and dP^T = V dO_i^T (tcgen05, TMEM); P^T (to TMEM) and
+//                       dS^T (to smem) by the compute warpgroup, one thread per key row;
+//                       dV += P^T dO_i (A from TMEM), dK += dS^T Q_i (A from smem), the dQ_i
+//                       partial (A/B from smem) drained from TMEM by a second warpgroup and
+//                       added into the fp32 dQ accumulator with a TMA bulk reduce-add.
+//                       The next step's S^T/dP^T are issued as soon as the compute warps
+//                       have read the current ones, so they overlap dV/dK/dQ of this step.
 //   fa_bwd_dq_kernel    dQ = bf16(scale * dQacc).
 //
 // d = 128: query steps of 64 rows, the dQ partial computed transposed (dQ^T = K^T dS^T,
@@ -43,51 +46,46 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 constexpr float kLog2e = 1.4426950408889634074f;
 
 // ----------------------------------------------------------------------------------------
-// Preprocess: one warp per row.
+// Preprocess: D/8 threads per row, 16-byte loads; 256 threads cover 2048/D rows.
 // ----------------------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(256)
 fa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
                   const float* __restrict__ lse, float* __restrict__ stats,
                   float* __restrict__ dq_acc, int N, int Npad, int BH) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const long long row_global = (long long)blockIdx.x * 8 + warp;  // over BH * Npad
-    if (row_global >= (long long)BH * Npad) return;
-    const int bh = (int)(row_global / Npad);
-    const int n = (int)(row_global % Npad);
-    constexpr int PER = D / 32;  // bf16 per lane
+    constexpr int TPR = D / 8;            // threads per row
+    constexpr int RPB = 256 / TPR;        // rows per block
+    const int sub = threadIdx.x % TPR;
+    const long long row_global = (long long)blockIdx.x * RPB + threadIdx.x / TPR;  // over BH*Npad
+    const bool valid_row = row_global < (long long)BH * Npad;
+    const int bh = valid_row ? (int)(row_global / Npad) : 0;
+    const int n = valid_row ? (int)(row_global % Npad) : 0;
     float dot = 0.f;
-    if (n < N) {
-        const size_t base = ((size_t)bh * N + n) * D + lane * PER;
-        if (PER == 4) {
-            const uint2 a = *reinterpret_cast<const uint2*>(o + base);
-            const uint2 b = *reinterpret_cast<const uint2*>(dout + base);
-            const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
-            const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
-            for (int i = 0; i < 2; ++i) {
-                const float2 fa = __bfloat1622float2(pa[i]);
-                const float2 fb = __bfloat1622float2(pb[i]);
-                dot = fmaf(fa.x, fb.x, dot);
-                dot = fmaf(fa.y, fb.y, dot);
-            }
-        } else {
-            const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(o + base);
-            const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(dout + base);
-            const float2 fa = __bfloat1622float2(a);
-            const float2 fb = __bfloat1622float2(b);
+    if (valid_row && n < N) {
+        const size_t base = ((size_t)bh * N + n) * D + sub * 8;
+        const uint4 a = *reinterpret_cast<const uint4*>(o + base);
+        const uint4 b = *reinterpret_cast<const uint4*>(dout + base);
+        const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
+        const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 fa = __bfloat1622float2(pa[i]);
+            const float2 fb = __bfloat1622float2(pb[i]);
             dot = fmaf(fa.x, fb.x, dot);
             dot = fmaf(fa.y, fb.y, dot);
         }
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-    if (lane == 0) {
+    for (int off = TPR / 2; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+    if (!valid_row) return;
+    if (sub == 0) {
         const size_t si = (size_t)bh * Npad + n;
         stats[si] = (n < N) ? lse[(size_t)bh * N + n] * kLog2e : __int_as_float(0x7f800000);
         stats[(size_t)BH * Npad + si] = (n < N) ? dot : 0.f;
     }
-    float4* acc = reinterpret_cast<float4*>(dq_acc + ((size_t)bh * Npad + n) * D);
-    if (lane < D / 4) acc[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4* acc = reinterpret_cast<float4*>(dq_acc + ((size_t)bh * Npad + n) * D + sub * 8);
+    acc[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // ----------------------------------------------------------------------------------------
@@ -129,26 +127,33 @@ struct BwdCfg {
     static constexpr uint32_t STAT_BYTES = (uint32_t)BMQ * 4u;
     // stage: [Q][dO][LSE2][Dvec], padded to 1024
     static constexpr uint32_t STAGE_BYTES = ((2 * QTILE + 2 * STAT_BYTES) + 1023u) / 1024u * 1024u;
-    static constexpr uint32_t DS_BYTES = (uint32_t)BMQ * 128u * 2u;  // dS tile (128 keys x BMQ)
+    // dS tile: 128 key rows, BMQ queries contiguous per row, in 64-query (128-byte) regions
+    static constexpr uint32_t DS_BYTES = (uint32_t)BMQ * 128u * 2u;
+    static constexpr uint32_t DSREG = 128u * 128u;           // one 64-query region
+    static constexpr uint32_t DQS_BYTES = (uint32_t)BMQ * D * 4u;  // fp32 dQ staging
+    static constexpr uint32_t DQBOX = (uint32_t)BMQ * 128u;  // one 32-column fp32 box
     static constexpr uint32_t OFF_K = 0;
     static constexpr uint32_t OFF_V = OFF_K + KTILE;
     static constexpr uint32_t OFF_ST = OFF_V + KTILE;
     static constexpr uint32_t OFF_DS = OFF_ST + NQS * STAGE_BYTES;
-    static constexpr uint32_t OFF_BAR = OFF_DS + 2 * DS_BYTES;
+    static constexpr uint32_t OFF_DQS = OFF_DS + 2 * DS_BYTES;
+    static constexpr uint32_t OFF_BAR = OFF_DQS + DQS_BYTES;
     static constexpr uint32_t SMEM_BYTES = OFF_BAR + 512 + 1024;
     static constexpr int THREADS = 384;
-    // TMEM columns
+    // TMEM columns. d=128: dV[0,128) dK[128,256) S^T[256,320) dP^T[320,384) dQ^T[384,448)
+    // P^T[448,480). d=64: dV[0,64) dK[64,128) S^T[128,256) dP^T[256,384) dQ[384,448) P^T[448,512).
     static constexpr uint32_t DV_COL = 0;
     static constexpr uint32_t DK_COL = (uint32_t)D;
     static constexpr uint32_t S_COL = 2u * D;
     static constexpr uint32_t DP_COL = S_COL + BMQ;
     static constexpr uint32_t DQ_COL = 384;
+    static constexpr uint32_t PT_COL = 448;
 };
 
 struct BwdBars {
     uint64_t kv_full;
     uint64_t q_full[2], q_empty[2];
-    uint64_t s_full, p_ready, mma_done;
+    uint64_t s_full, s_free, p_ready, mma_done;
     uint64_t ds_free[2];
     uint64_t dq_full, dq_free;
     uint64_t final_bar;
@@ -161,9 +166,9 @@ __global__ void __launch_bounds__(384, 1)
 fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
               const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
-              const float* __restrict__ stats, float* __restrict__ dq_acc, const int N,
-              const int Npad, const int BH, const int nkb, const float c, const float scale,
-              int* err) {
+              const __grid_constant__ CUtensorMap tm_dqacc, const float* __restrict__ stats,
+              const int N, const int Npad, const int BH, const int nkb, const float c,
+              const float scale, int* err) {
     using C = BwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
@@ -186,6 +191,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             ptx::mbar_init(ptx::smem_addr(&bars->q_empty[s]), 1);
         }
         ptx::mbar_init(ptx::smem_addr(&bars->s_full), 1);
+        ptx::mbar_init(ptx::smem_addr(&bars->s_free), 128);
         ptx::mbar_init(ptx::smem_addr(&bars->p_ready), 128);
         ptx::mbar_init(ptx::smem_addr(&bars->mma_done), 1);
         ptx::mbar_init(ptx::smem_addr(&bars->ds_free[0]), 1);
@@ -201,6 +207,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         ptx::tma_prefetch_desc(&tm_do);
         ptx::tma_prefetch_desc(&tm_dk);
         ptx::tma_prefetch_desc(&tm_dv);
+        ptx::tma_prefetch_desc(&tm_dqacc);
     }
     if (warp == 2) {
         ptx::tmem_alloc(ptx::smem_addr(&bars->tmem_base), 512);
@@ -260,22 +267,9 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             // dQ: d=128 -> dQ^T = K^T dS^T (M=d, N=BMQ); d=64 -> dQ = dS K (M=BMQ, N=d)
             constexpr uint32_t idesc_q = (D == 128) ? ptx::idesc_bf16(128, C::BMQ, true, true)
                                                     : ptx::idesc_bf16(128, D, true, true);
-            bool ok = wait_phase(ptx::smem_addr(&bars->kv_full), 0, abort_flag, err, kDevTimeoutLoad);
-            for (int si = 0; ok && si < nsteps; ++si) {
-                const int st = si % C::NQS;
-                const uint32_t ph = (uint32_t)(si / C::NQS) & 1u;
-                const uint32_t qa = s_st + st * C::STAGE_BYTES;
+            auto issue_s_dp = [&](int si) {
+                const uint32_t qa = s_st + (si % C::NQS) * C::STAGE_BYTES;
                 const uint32_t doa = qa + C::QTILE;
-                ok = wait_phase(ptx::smem_addr(&bars->q_full[st]), ph, abort_flag, err, kDevTimeoutLoad);
-                if (!ok) break;
-                if (si > 0) {
-                    // dV/dK of the previous step read P^T/dS^T from the S/dP columns.
-                    ok = wait_phase(ptx::smem_addr(&bars->mma_done), (uint32_t)(si - 1) & 1u,
-                                    abort_flag, err, kDevTimeoutMma);
-                    if (!ok) break;
-                }
-                ptx::tc_fence_after();
-                // S^T = K Q^T and dP^T = V dO^T (K-major operands, K dimension = d).
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t koff = (kk >> 2) * C::KCHUNK + (kk & 3) * 32;
@@ -291,20 +285,44 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                                 ptx::sdesc_sw128(doa + qoff, 16, 1024), idesc_s, kk > 0);
                 }
                 ptx::mma_commit(ptx::smem_addr(&bars->s_full));
+            };
+            bool ok = wait_phase(ptx::smem_addr(&bars->kv_full), 0, abort_flag, err, kDevTimeoutLoad);
+            if (ok) ok = wait_phase(ptx::smem_addr(&bars->q_full[0]), 0, abort_flag, err, kDevTimeoutLoad);
+            if (ok) {
+                ptx::tc_fence_after();
+                issue_s_dp(0);
+            }
+            for (int si = 0; ok && si < nsteps; ++si) {
+                const int st = si % C::NQS;
+                const uint32_t qa = s_st + st * C::STAGE_BYTES;
+                const uint32_t doa = qa + C::QTILE;
+                const uint32_t dsa = s_ds + (uint32_t)(si & 1) * C::DS_BYTES;
+                if (si + 1 < nsteps) {
+                    // Next S^T/dP^T as soon as the compute warps have read this step's.
+                    const int st1 = (si + 1) % C::NQS;
+                    ok = wait_phase(ptx::smem_addr(&bars->q_full[st1]), (uint32_t)((si + 1) / C::NQS) & 1u,
+                                    abort_flag, err, kDevTimeoutLoad);
+                    if (ok) ok = wait_phase(ptx::smem_addr(&bars->s_free), (uint32_t)si & 1u, abort_flag,
+                                            err, kDevTimeoutSoftmax);
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+                    issue_s_dp(si + 1);
+                }
                 ok = wait_phase(ptx::smem_addr(&bars->p_ready), (uint32_t)si & 1u, abort_flag, err,
                                 kDevTimeoutSoftmax);
                 if (!ok) break;
                 ptx::tc_fence_after();
-                // dV += P^T dO and dK += dS^T Q (A from TMEM, B MN-major, K dimension = BMQ).
+                // dV += P^T dO (A = P^T in TMEM) and dK += dS^T Q (A = dS^T, K-major in smem).
 #pragma unroll
                 for (int kk = 0; kk < C::BMQ / 16; ++kk) {
-                    ptx::mma_ts(tbase + C::DV_COL, tbase + C::S_COL + kk * 8,
+                    ptx::mma_ts(tbase + C::DV_COL, tbase + C::PT_COL + kk * 8,
                                 ptx::sdesc_sw128(doa + kk * 2048, C::QCHUNK, 1024), idesc_kv,
                                 (si > 0 || kk > 0) ? 1u : 0u);
                 }
 #pragma unroll
                 for (int kk = 0; kk < C::BMQ / 16; ++kk) {
-                    ptx::mma_ts(tbase + C::DK_COL, tbase + C::DP_COL + kk * 8,
+                    ptx::mma_ss(tbase + C::DK_COL,
+                                ptx::sdesc_sw128(dsa + (kk >> 2) * C::DSREG + (kk & 3) * 32, 16, 1024),
                                 ptx::sdesc_sw128(qa + kk * 2048, C::QCHUNK, 1024), idesc_kv,
                                 (si > 0 || kk > 0) ? 1u : 0u);
                 }
@@ -316,19 +334,16 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     if (!ok) break;
                     ptx::tc_fence_after();
                 }
-                const uint32_t dsa = s_ds + (uint32_t)(si & 1) * C::DS_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < C::KT / 16; ++kk) {
                     if (D == 128) {
                         // dQ^T = K^T dS^T: A = K as MN-major [d x keys], B = dS as MN-major [q x keys]
                         ptx::mma_ss(tbase + C::DQ_COL, ptx::sdesc_sw128(s_k + kk * 2048, C::KCHUNK, 1024),
-                                    ptx::sdesc_sw128(dsa + kk * 2048, 128u * 128u, 1024), idesc_q,
-                                    kk > 0);
+                                    ptx::sdesc_sw128(dsa + kk * 2048, C::DSREG, 1024), idesc_q, kk > 0);
                     } else {
                         // dQ = dS K: A = dS as MN-major [q x keys], B = K as MN-major [d x keys]
-                        ptx::mma_ss(tbase + C::DQ_COL, ptx::sdesc_sw128(dsa + kk * 2048, 128u * 128u, 1024),
-                                    ptx::sdesc_sw128(s_k + kk * 2048, C::KCHUNK, 1024), idesc_q,
-                                    kk > 0);
+                        ptx::mma_ss(tbase + C::DQ_COL, ptx::sdesc_sw128(dsa + kk * 2048, C::DSREG, 1024),
+                                    ptx::sdesc_sw128(s_k + kk * 2048, C::KCHUNK, 1024), idesc_q, kk > 0);
                     }
                 }
                 ptx::mma_commit(ptx::smem_addr(&bars->dq_full));
@@ -345,6 +360,8 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const uint32_t t_s = tbase + lane_off + C::S_COL;
         const uint32_t t_dp = tbase + lane_off + C::DP_COL;
+        const uint32_t t_pt = tbase + lane_off + C::PT_COL;
+        constexpr int NCH = C::BMQ / 32;
         bool ok = true;
         for (int si = 0; si < nsteps; ++si) {
             const int st = si % C::NQS;
@@ -356,32 +373,41 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                                                     (uint32_t)(si / C::NQS) & 1u, abort_flag, err,
                                                     kDevTimeoutLoad));
             if (!ok) break;
-            if (si >= 2) {
-                ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->ds_free[si & 1]),
-                                                        (uint32_t)((si >> 1) - 1) & 1u, abort_flag,
-                                                        err, kDevTimeoutMma));
-                if (!ok) break;
-            }
             ptx::tc_fence_after();
             const float* lse2 = reinterpret_cast<const float*>(smem + C::OFF_ST + st * C::STAGE_BYTES + 2 * C::QTILE);
             const float* dvec = lse2 + C::BMQ;
             uint8_t* dsbuf = smem + C::OFF_DS + (si & 1) * C::DS_BYTES;
             const bool need_mask = CAUSAL && (q0 < key0 + C::KT - 1);
 #pragma unroll 1
-            for (int cc = 0; cc < C::BMQ / 32; ++cc) {
+            for (int cc = 0; cc < NCH; ++cc) {
                 uint32_t sv[32], dpv[32];
                 ptx::tmem_ld32_nowait(t_s + 32 * cc, sv);
                 ptx::tmem_ld32_nowait(t_dp + 32 * cc, dpv);
                 ptx::tmem_wait_ld(sv);
                 ptx::tmem_wait_ld(dpv);
+                if (cc == NCH - 1) {
+                    // every S^T/dP^T column of this step is in registers: release them
+                    ptx::tc_fence_before();
+                    ptx::mbar_arrive(ptx::smem_addr(&bars->s_free));
+                }
                 float p[32], ds[32];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
+                for (int j = 0; j < 32; j += 2) {
                     const int qi = 32 * cc + j;
-                    float pj = ptx::ex2_approx(fmaf(__uint_as_float(sv[j]), c, -lse2[qi]));
-                    if (need_mask && key > q0 + qi) pj = 0.f;
-                    p[j] = pj;
-                    ds[j] = pj * (__uint_as_float(dpv[j]) - dvec[qi]);
+                    float x0, x1;
+                    ptx::ffma2(x0, x1, __uint_as_float(sv[j]), __uint_as_float(sv[j + 1]), c, c,
+                               -lse2[qi], -lse2[qi + 1]);
+                    float p0 = ptx::ex2_approx(x0), p1 = ptx::ex2_approx(x1);
+                    if (need_mask) {
+                        if (key > q0 + qi) p0 = 0.f;
+                        if (key > q0 + qi + 1) p1 = 0.f;
+                    }
+                    p[j] = p0;
+                    p[j + 1] = p1;
+                    float y0, y1;
+                    ptx::fadd2(y0, y1, __uint_as_float(dpv[j]), __uint_as_float(dpv[j + 1]), -dvec[qi],
+                               -dvec[qi + 1]);
+                    ptx::fmul2(ds[j], ds[j + 1], p0, p1, y0, y1);
                 }
                 uint32_t pk[16], dk[16];
 #pragma unroll
@@ -389,16 +415,33 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     pk[j] = ptx::pack_bf16x2(p[2 * j], p[2 * j + 1]);
                     dk[j] = ptx::pack_bf16x2(ds[2 * j], ds[2 * j + 1]);
                 }
-                ptx::tmem_st16(t_s + 16 * cc, pk);
-                ptx::tmem_st16(t_dp + 16 * cc, dk);
+                if (cc == 0) {
+                    if (si > 0) {
+                        // dV(si-1) must have read P^T before it is overwritten.
+                        ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->mma_done),
+                                                                (uint32_t)(si - 1) & 1u, abort_flag,
+                                                                err, kDevTimeoutMma));
+                        if (!ok) break;
+                    }
+                    if (si >= 2) {
+                        // dK(si-2) and dQ(si-2) must have read this dS buffer.
+                        ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->ds_free[si & 1]),
+                                                                (uint32_t)((si >> 1) - 1) & 1u,
+                                                                abort_flag, err, kDevTimeoutMma));
+                        if (!ok) break;
+                    }
+                    ptx::tc_fence_after();
+                }
+                ptx::tmem_st16(t_pt + 16 * cc, pk);
                 // dS row k (queries contiguous) into the 128B-swizzled dS tile.
-                uint8_t* region = dsbuf + (cc >> 1) * (128u * 128u);
+                uint8_t* region = dsbuf + (cc >> 1) * C::DSREG;
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     uint4 w = make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
                     *reinterpret_cast<uint4*>(region + sw128_offset((uint32_t)k, (uint32_t)((cc & 1) * 4 + u))) = w;
                 }
             }
+            if (!ok) break;
             ptx::tmem_wait_st();
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
@@ -440,6 +483,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const int wq = warp & 3;
         const int r = wq * 32 + lane;  // TMEM lane: d index (d=128) or query row (d=64)
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        uint8_t* dqs = smem + C::OFF_DQS;
         bool ok = true;
         for (int si = 0; si < nsteps; ++si) {
             const int q0 = (i0 + si) * C::BMQ;
@@ -454,26 +498,41 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             ptx::tmem_wait_ld(b);
             ptx::tc_fence_before();
             ptx::mbar_arrive(ptx::smem_addr(&bars->dq_free));
+            // The previous step's reduce must have finished reading the staging tile.
+            if (si > 0) {
+                if (r == 0) ptx::bulk_wait_read_all();
+                ptx::named_bar_sync(2, 128);
+            }
             if (D == 128) {
-                // lane r = head-dim column; 64 query rows -> coalesced across the warp
-                float* base = dq_acc + ((size_t)bh * Npad + q0) * D + r;
+                // lane r = head-dim column e; a/b hold query rows 0-31 / 32-63.
+                // fp32 box (e / 32): [BMQ rows x 128 B], element e at byte 4 (e % 32).
+                uint8_t* box = dqs + (r >> 5) * C::DQBOX;
+                const uint32_t u = (uint32_t)((r & 31) >> 2);
+                const uint32_t wb = (uint32_t)(r & 3) * 4u;
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
-                    atomicAdd(base + (size_t)j * D, __uint_as_float(a[j]));
-                    atomicAdd(base + (size_t)(32 + j) * D, __uint_as_float(b[j]));
+                    *reinterpret_cast<uint32_t*>(box + sw128_offset((uint32_t)j, u) + wb) = a[j];
+                    *reinterpret_cast<uint32_t*>(box + sw128_offset((uint32_t)(32 + j), u) + wb) = b[j];
                 }
             } else {
-                // lane r = query row; 64 head-dim columns
-                float4* row = reinterpret_cast<float4*>(dq_acc + ((size_t)bh * Npad + q0 + r) * D);
+                // lane r = query row; a/b hold head-dim columns 0-31 / 32-63 (one fp32 box each).
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    atomicAdd(row + j, make_float4(__uint_as_float(a[4 * j]), __uint_as_float(a[4 * j + 1]),
-                                                   __uint_as_float(a[4 * j + 2]), __uint_as_float(a[4 * j + 3])));
-                    atomicAdd(row + 8 + j, make_float4(__uint_as_float(b[4 * j]), __uint_as_float(b[4 * j + 1]),
-                                                       __uint_as_float(b[4 * j + 2]), __uint_as_float(b[4 * j + 3])));
+                for (int u = 0; u < 8; ++u) {
+                    *reinterpret_cast<uint4*>(dqs + sw128_offset((uint32_t)r, (uint32_t)u)) =
+                        make_uint4(a[4 * u], a[4 * u + 1], a[4 * u + 2], a[4 * u + 3]);
+                    *reinterpret_cast<uint4*>(dqs + C::DQBOX + sw128_offset((uint32_t)r, (uint32_t)u)) =
+                        make_uint4(b[4 * u], b[4 * u + 1], b[4 * u + 2], b[4 * u + 3]);
                 }
             }
+            ptx::fence_proxy_async_smem();
+            ptx::named_bar_sync(2, 128);
+            if (r == 0) {
+                for (int bx = 0; bx < D / 32; ++bx)
+                    ptx::tma_reduce_add_3d(&tm_dqacc, ptx::smem_addr(dqs + bx * C::DQBOX), bx * 32, q0, bh);
+                ptx::bulk_commit();
+            }
         }
+        if (r == 0) ptx::bulk_wait_all();
         // ---- epilogue: dK * scale -> bf16 -> smem (stage 1 area) -> TMA store ----
         if (ok) ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->mma_done),
                                                         (uint32_t)(nsteps - 1) & 1u, abort_flag,
@@ -521,7 +580,8 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t stream) {
     // 1. preprocess
     {
         const long long rows = (long long)a.BH * a.Npad;
-        const long long blocks = (rows + 7) / 8;
+        const long long rpb = 256 / (D / 8);
+        const long long blocks = (rows + rpb - 1) / rpb;
         if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
         fa_bwd_pre_kernel<D><<<(unsigned)blocks, 256, 0, stream>>>(
             static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.lse,
@@ -539,8 +599,8 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t stream) {
         const long long blocks = (long long)nkb * a.BH;
         if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
         kern<<<(unsigned)blocks, C::THREADS, C::SMEM_BYTES, stream>>>(
-            a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dk, a.tm_dv, a.stats, a.dq_acc, a.N, a.Npad, a.BH,
-            nkb, a.c, a.scale, a.err);
+            a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dk, a.tm_dv, a.tm_dqacc, a.stats, a.N, a.Npad,
+            a.BH, nkb, a.c, a.scale, a.err);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

@@ -22,6 +22,7 @@ cudaError_t launch_forward(const FwdLaunch& a, int d, bool causal, cudaStream_t 
 struct BwdLaunch {
     CUtensorMap tm_q, tm_k, tm_v, tm_do;  // loads, box {64, rows, 1}
     CUtensorMap tm_dk, tm_dv;             // stores, box {64, 128, 1}
+    CUtensorMap tm_dqacc;                 // fp32 [B*H, Npad, d] accumulator, box {32, rows, 1}
     const void* o;                        // bf16 [B*H, N, d]
     const void* dout;                     // bf16 [B*H, N, d]
     const float* lse;                     // fp32 [B*H, N]
