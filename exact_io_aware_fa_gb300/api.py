@@ -23,8 +23,11 @@ FA_ERR_CUDA = 4
 FA_ERR_TIMEOUT = 5
 
 # Every symbol include/fa.h declares.
-EXPORTS = ("fa_forward", "fa_backward_workspace_bytes", "fa_backward", "fa_status_string",
-           "fa_last_cuda_error", "fa_device_error")
+EXPORTS = ("fa_forward", "fa_backward_workspace_bytes", "fa_backward", "fa_backward_noalloc",
+           "fa_status_string", "fa_last_cuda_error", "fa_device_error")
+
+# Size of the library's own backward workspace (FA_NOALLOC_SCRATCH_BYTES in include/fa.h).
+NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 
 class FaLibraryMissing(RuntimeError):
@@ -62,6 +65,8 @@ def library(path: str | None = None):
         lib.fa_backward_workspace_bytes.restype = Z
         lib.fa_backward.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, P, P]
         lib.fa_backward.restype = I
+        lib.fa_backward_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, P]
+        lib.fa_backward_noalloc.restype = I
         lib.fa_status_string.argtypes = [I]
         lib.fa_status_string.restype = ctypes.c_char_p
         lib.fa_last_cuda_error.argtypes = []
@@ -93,6 +98,14 @@ def backward_raw(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, causal, scale, w
                  stream) -> int:
     return library().fa_backward(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, causal, scale,
                                  workspace, stream)
+
+
+def backward_noalloc_raw(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, causal, scale,
+                         stream) -> int:
+    """fa_backward_noalloc: the backward with the library's own fixed device workspace, for
+    callers that may not allocate device memory at call time (see include/fa.h)."""
+    return library().fa_backward_noalloc(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, causal,
+                                         scale, stream)
 
 
 def backward_workspace_bytes(B: int, H: int, N: int, d: int) -> int:

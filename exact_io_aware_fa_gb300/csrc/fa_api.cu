@@ -112,6 +112,30 @@ fa_status check_common(int B, int H, int N, int d, int causal, float scale, bool
 
 constexpr float kLog2e = 1.4426950408889634074f;
 
+// Workspace of fa_backward_noalloc: one array per device that loads the library, kept for
+// the life of the process. Host code must not use its name as an address (it is a host-side
+// stand-in); the device address comes from cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device, looked up once per device.
+fa_status get_noalloc_scratch(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e);
+        if (p == nullptr) return cuda_fail(cudaErrorInvalidSymbol);
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return FA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -219,6 +243,21 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
     }
     if (e != cudaSuccess) return cuda_fail(e);
     return FA_OK;
+}
+
+fa_status fa_backward_noalloc(const void* q, const void* k, const void* v, const void* o,
+                              const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                              int B, int H, int N, int d, int causal, float scale,
+                              struct CUstream_st* stream) {
+    bool empty = false;
+    fa_status st = check_common(B, H, N, d, causal, scale, &empty);
+    if (st != FA_OK || empty) return st;
+    if (fa_backward_workspace_bytes(B, H, N, d) > (size_t)FA_NOALLOC_SCRATCH_BYTES)
+        return FA_ERR_UNSUPPORTED;
+    void* scratch = nullptr;
+    if ((st = get_noalloc_scratch(&scratch)) != FA_OK) return st;
+    return fa_backward(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, causal, scale, scratch,
+                       stream);
 }
 
 fa_status fa_device_error(struct CUstream_st* stream, int* code) {

@@ -94,6 +94,35 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
                       int H, int N, int d, int causal, float scale, void* workspace,
                       struct CUstream_st* stream);
 
+/*
+ * Allocation-free backward (no counterpart in the pages: an integration convenience).
+ *
+ * Same computation, arguments and results as fa_backward, for callers that may not allocate
+ * device memory at call time: runtimes that plan every device buffer once at start-up and
+ * forbid allocation afterwards, hosts embedding the library without access to an allocator,
+ * or loops where an allocation's latency or fragmentation is not acceptable. Instead of a
+ * caller buffer or cudaMallocAsync, the workspace is one file-scope device array of
+ * FA_NOALLOC_SCRATCH_BYTES bytes inside libfa.so, which every GPU that loads the library keeps
+ * until the process exits. This call allocates nothing (no cudaMalloc, cudaFree or allocating
+ * library routine).
+ *   - Sizes whose workspace (fa_backward_workspace_bytes) exceeds FA_NOALLOC_SCRATCH_BYTES are
+ *     rejected with FA_ERR_UNSUPPORTED before anything is launched (for example B*H = 64,
+ *     N = 2048, d = 64 needs 34.6 MB and fits; B*H = 64, N = 4096, d = 128 needs 136 MB and
+ *     does not). Other argument errors are those of fa_backward.
+ *   - The first call on a device looks up the array's device address (with that device
+ *     current) and caches it; make that first call before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents; the kernels
+ *     initialise every part of it they read, so no clearing is needed. Calls whose work
+ *     overlaps on the GPU (different streams, or different host threads, without ordering
+ *     between them) race on the array: order them.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+fa_status fa_backward_noalloc(const void* q, const void* k, const void* v, const void* o,
+                              const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                              int B, int H, int N, int d, int causal, float scale,
+                              struct CUstream_st* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* fa_status_string(fa_status s);
 
