@@ -216,7 +216,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
-    const uint32_t tbase = bars->tmem_base;
+    const uint32_t tbase = __shfl_sync(0xffffffffu, bars->tmem_base, 0);
     volatile int* abort_flag = &bars->abort_flag;
     const uint32_t s_k = ptx::smem_addr(smem + C::OFF_K);
     const uint32_t s_v = ptx::smem_addr(smem + C::OFF_V);
@@ -261,95 +261,117 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         }
     } else if (warp == 1) {
         // ================================ MMA issuer ==================================
-        if (lane == 0) {
+        {  // whole warp; one elected lane issues
             constexpr uint32_t idesc_s = ptx::idesc_bf16(128, C::BMQ, false, false);  // S^T, dP^T
             constexpr uint32_t idesc_kv = ptx::idesc_bf16(128, D, false, true);       // dV, dK
             // dQ: d=128 -> dQ^T = K^T dS^T (M=d, N=BMQ); d=64 -> dQ = dS K (M=BMQ, N=d)
             constexpr uint32_t idesc_q = (D == 128) ? ptx::idesc_bf16(128, C::BMQ, true, true)
                                                     : ptx::idesc_bf16(128, D, true, true);
+            // Descriptors built once, stepped by constant offsets per MMA (see the forward).
+            const uint64_t k_kmaj = ptx::sdesc_sw128(s_k, 16, 1024);
+            const uint64_t v_kmaj = ptx::sdesc_sw128(s_v, 16, 1024);
+            const uint64_t k_mn = ptx::sdesc_sw128(s_k, C::KCHUNK, 1024);
+            const uint64_t st_kmaj = ptx::sdesc_sw128(s_st, 16, 1024);
+            const uint64_t st_mn = ptx::sdesc_sw128(s_st, C::QCHUNK, 1024);
+            const uint64_t ds_kmaj = ptx::sdesc_sw128(s_ds, 16, 1024);
+            const uint64_t ds_mn = ptx::sdesc_sw128(s_ds, C::DSREG, 1024);
             auto issue_s_dp = [&](int si) {
-                const uint32_t qa = s_st + (si % C::NQS) * C::STAGE_BYTES;
-                const uint32_t doa = qa + C::QTILE;
+                const uint32_t st_off = (uint32_t)(si % C::NQS) * C::STAGE_BYTES;
+                const uint64_t qd = ptx::sdesc_add(st_kmaj, st_off);
+                const uint64_t dod = ptx::sdesc_add(st_kmaj, st_off + C::QTILE);
+                if (ptx::elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t koff = (kk >> 2) * C::KCHUNK + (kk & 3) * 32;
                     const uint32_t qoff = (kk >> 2) * C::QCHUNK + (kk & 3) * 32;
-                    ptx::mma_ss(tbase + C::S_COL, ptx::sdesc_sw128(s_k + koff, 16, 1024),
-                                ptx::sdesc_sw128(qa + qoff, 16, 1024), idesc_s, kk > 0);
+                    ptx::mma_ss(tbase + C::S_COL, ptx::sdesc_add(k_kmaj, koff), ptx::sdesc_add(qd, qoff),
+                                idesc_s, kk > 0);
                 }
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t koff = (kk >> 2) * C::KCHUNK + (kk & 3) * 32;
                     const uint32_t qoff = (kk >> 2) * C::QCHUNK + (kk & 3) * 32;
-                    ptx::mma_ss(tbase + C::DP_COL, ptx::sdesc_sw128(s_v + koff, 16, 1024),
-                                ptx::sdesc_sw128(doa + qoff, 16, 1024), idesc_s, kk > 0);
+                    ptx::mma_ss(tbase + C::DP_COL, ptx::sdesc_add(v_kmaj, koff), ptx::sdesc_add(dod, qoff),
+                                idesc_s, kk > 0);
                 }
                 ptx::mma_commit(ptx::smem_addr(&bars->s_full));
+                }
+                __syncwarp();
             };
-            bool ok = wait_phase(ptx::smem_addr(&bars->kv_full), 0, abort_flag, err, kDevTimeoutLoad);
-            if (ok) ok = wait_phase(ptx::smem_addr(&bars->q_full[0]), 0, abort_flag, err, kDevTimeoutLoad);
+            auto commit = [&](uint64_t* bar) {
+                if (ptx::elect_one()) ptx::mma_commit(ptx::smem_addr(bar));
+                __syncwarp();
+            };
+            bool ok = warp_wait(ptx::smem_addr(&bars->kv_full), 0, abort_flag, err, kDevTimeoutLoad);
+            if (ok) ok = warp_wait(ptx::smem_addr(&bars->q_full[0]), 0, abort_flag, err, kDevTimeoutLoad);
             if (ok) {
                 ptx::tc_fence_after();
                 issue_s_dp(0);
             }
             for (int si = 0; ok && si < nsteps; ++si) {
                 const int st = si % C::NQS;
-                const uint32_t qa = s_st + st * C::STAGE_BYTES;
-                const uint32_t doa = qa + C::QTILE;
-                const uint32_t dsa = s_ds + (uint32_t)(si & 1) * C::DS_BYTES;
                 if (si + 1 < nsteps) {
                     // Next S^T/dP^T as soon as the compute warps have read this step's.
                     const int st1 = (si + 1) % C::NQS;
-                    ok = wait_phase(ptx::smem_addr(&bars->q_full[st1]), (uint32_t)((si + 1) / C::NQS) & 1u,
+                    ok = warp_wait(ptx::smem_addr(&bars->q_full[st1]), (uint32_t)((si + 1) / C::NQS) & 1u,
                                     abort_flag, err, kDevTimeoutLoad);
-                    if (ok) ok = wait_phase(ptx::smem_addr(&bars->s_free), (uint32_t)si & 1u, abort_flag,
+                    if (ok) ok = warp_wait(ptx::smem_addr(&bars->s_free), (uint32_t)si & 1u, abort_flag,
                                             err, kDevTimeoutSoftmax);
                     if (!ok) break;
                     ptx::tc_fence_after();
                     issue_s_dp(si + 1);
                 }
-                ok = wait_phase(ptx::smem_addr(&bars->p_ready), (uint32_t)si & 1u, abort_flag, err,
+                ok = warp_wait(ptx::smem_addr(&bars->p_ready), (uint32_t)si & 1u, abort_flag, err,
                                 kDevTimeoutSoftmax);
                 if (!ok) break;
                 ptx::tc_fence_after();
                 // dV += P^T dO (A = P^T in TMEM) and dK += dS^T Q (A = dS^T, K-major in smem).
+                const uint32_t st_off = (uint32_t)st * C::STAGE_BYTES;
+                const uint32_t ds_off = (uint32_t)(si & 1) * C::DS_BYTES;
+                const uint64_t do_mn = ptx::sdesc_add(st_mn, st_off + C::QTILE);
+                const uint64_t q_mn = ptx::sdesc_add(st_mn, st_off);
+                const uint64_t dsk = ptx::sdesc_add(ds_kmaj, ds_off);
+                if (ptx::elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < C::BMQ / 16; ++kk) {
                     ptx::mma_ts(tbase + C::DV_COL, tbase + C::PT_COL + kk * 8,
-                                ptx::sdesc_sw128(doa + kk * 2048, C::QCHUNK, 1024), idesc_kv,
-                                (si > 0 || kk > 0) ? 1u : 0u);
+                                ptx::sdesc_add(do_mn, kk * 2048), idesc_kv, (si > 0 || kk > 0) ? 1u : 0u);
                 }
 #pragma unroll
                 for (int kk = 0; kk < C::BMQ / 16; ++kk) {
-                    ptx::mma_ss(tbase + C::DK_COL,
-                                ptx::sdesc_sw128(dsa + (kk >> 2) * C::DSREG + (kk & 3) * 32, 16, 1024),
-                                ptx::sdesc_sw128(qa + kk * 2048, C::QCHUNK, 1024), idesc_kv,
-                                (si > 0 || kk > 0) ? 1u : 0u);
+                    ptx::mma_ss(tbase + C::DK_COL, ptx::sdesc_add(dsk, (kk >> 2) * C::DSREG + (kk & 3) * 32),
+                                ptx::sdesc_add(q_mn, kk * 2048), idesc_kv, (si > 0 || kk > 0) ? 1u : 0u);
                 }
                 ptx::mma_commit(ptx::smem_addr(&bars->mma_done));
                 ptx::mma_commit(ptx::smem_addr(&bars->q_empty[st]));
+                }
+                __syncwarp();
                 if (si > 0) {
-                    ok = wait_phase(ptx::smem_addr(&bars->dq_free), (uint32_t)(si - 1) & 1u,
+                    ok = warp_wait(ptx::smem_addr(&bars->dq_free), (uint32_t)(si - 1) & 1u,
                                     abort_flag, err, kDevTimeoutSoftmax);
                     if (!ok) break;
                     ptx::tc_fence_after();
                 }
+                const uint64_t dsm = ptx::sdesc_add(ds_mn, ds_off);
+                if (ptx::elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < C::KT / 16; ++kk) {
                     if (D == 128) {
                         // dQ^T = K^T dS^T: A = K as MN-major [d x keys], B = dS as MN-major [q x keys]
-                        ptx::mma_ss(tbase + C::DQ_COL, ptx::sdesc_sw128(s_k + kk * 2048, C::KCHUNK, 1024),
-                                    ptx::sdesc_sw128(dsa + kk * 2048, C::DSREG, 1024), idesc_q, kk > 0);
+                        ptx::mma_ss(tbase + C::DQ_COL, ptx::sdesc_add(k_mn, kk * 2048),
+                                    ptx::sdesc_add(dsm, kk * 2048), idesc_q, kk > 0);
                     } else {
                         // dQ = dS K: A = dS as MN-major [q x keys], B = K as MN-major [d x keys]
-                        ptx::mma_ss(tbase + C::DQ_COL, ptx::sdesc_sw128(dsa + kk * 2048, C::DSREG, 1024),
-                                    ptx::sdesc_sw128(s_k + kk * 2048, C::KCHUNK, 1024), idesc_q, kk > 0);
+                        ptx::mma_ss(tbase + C::DQ_COL, ptx::sdesc_add(dsm, kk * 2048),
+                                    ptx::sdesc_add(k_mn, kk * 2048), idesc_q, kk > 0);
                     }
                 }
                 ptx::mma_commit(ptx::smem_addr(&bars->dq_full));
                 ptx::mma_commit(ptx::smem_addr(&bars->ds_free[si & 1]));
+                }
+                __syncwarp();
             }
-            ptx::mma_commit(ptx::smem_addr(&bars->final_bar));
+            commit(&bars->final_bar);
             drain_wait(ptx::smem_addr(&bars->final_bar), 0);
         }
     } else if (warp >= 4 && warp < 8) {

@@ -38,6 +38,12 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
     }
 }
 
+// wait_phase for a whole warp: every lane polls, and the outcome is made warp-uniform.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          int* err, int code) {
+    return __all_sync(0xffffffffu, wait_phase(bar, parity, abort_flag, err, code));
+}
+
 // Byte offset of the 16-byte unit `u` (0..7) of row `r` inside a 128-byte-swizzled tile whose
 // rows are 128 bytes apart (the layout TMA writes with CU_TENSOR_MAP_SWIZZLE_128B and the
 // tcgen05 descriptors read with layout type 2). The tile base must be 1024-byte aligned.

@@ -141,7 +141,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
-    const uint32_t tbase = bars->tmem_base;
+    const uint32_t tbase = __shfl_sync(0xffffffffu, bars->tmem_base, 0);
     volatile int* abort_flag = &bars->abort_flag;
 
     const uint32_t s_q = ptx::smem_addr(smem + C::OFF_Q);
@@ -193,29 +193,46 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         }
     } else if (warp == 1) {
         // ================================ MMA issuer ==================================
-        if (lane == 0 && nkv > 0) {
+        if (nkv > 0) {  // whole warp; one elected lane issues
             constexpr uint32_t idesc_s = ptx::idesc_bf16(128, C::BN, false, false);
             constexpr uint32_t idesc_o = ptx::idesc_bf16(128, D, false, true);
-            auto issue_s = [&](int t, int stage) {
+            // Descriptors are built once and stepped by constant offsets per MMA: the issuing
+            // thread shares its SMSP with two softmax warps, so every instruction it saves
+            // shortens the gap between MMAs.
+            const uint64_t dq0 = ptx::sdesc_sw128(s_q, 16, 1024);
+            const uint64_t dk0 = ptx::sdesc_sw128(s_k, 16, 1024);
+            const uint64_t dv0 = ptx::sdesc_sw128(s_v, C::CHUNK_BYTES, 1024);
+            auto issue_s = [&](int t, int stage) {  // S_t = Q_t K^T, then arrive on s_full[t]
                 const uint32_t d_tmem = tbase + C::s_col(t);
-                const uint32_t qa = s_q + t * C::TILE_BYTES;
-                const uint32_t ka = s_k + stage * C::TILE_BYTES;
+                const uint64_t qd = ptx::sdesc_add(dq0, (uint32_t)t * C::TILE_BYTES);
+                const uint64_t kd = ptx::sdesc_add(dk0, (uint32_t)stage * C::TILE_BYTES);
+                if (ptx::elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
-                    ptx::mma_ss(d_tmem, ptx::sdesc_sw128(qa + off, 16, 1024),
-                                ptx::sdesc_sw128(ka + off, 16, 1024), idesc_s, kk > 0);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
+                        ptx::mma_ss(d_tmem, ptx::sdesc_add(qd, off), ptx::sdesc_add(kd, off), idesc_s,
+                                    kk > 0);
+                    }
+                    ptx::mma_commit(ptx::smem_addr(&bars->s_full[t]));
                 }
+                __syncwarp();
             };
-            auto issue_pv = [&](int t, int stage, bool acc) {
+            auto issue_pv = [&](int t, int stage, bool acc) {  // O_t += P_t V, arrive on o_done[t]
                 const uint32_t d_tmem = tbase + C::o_col(t);
                 const uint32_t p_tmem = tbase + C::p_col(t);
-                const uint32_t va = s_v + stage * C::TILE_BYTES;
+                const uint64_t vd = ptx::sdesc_add(dv0, (uint32_t)stage * C::TILE_BYTES);
+                if (ptx::elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < C::BN / 16; ++kk)
-                    ptx::mma_ts(d_tmem, p_tmem + kk * 8,
-                                ptx::sdesc_sw128(va + kk * 2048, C::CHUNK_BYTES, 1024), idesc_o,
-                                (acc || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < C::BN / 16; ++kk)
+                        ptx::mma_ts(d_tmem, p_tmem + kk * 8, ptx::sdesc_add(vd, kk * 2048), idesc_o,
+                                    (acc || kk > 0) ? 1u : 0u);
+                    ptx::mma_commit(ptx::smem_addr(&bars->o_done[t]));
+                }
+                __syncwarp();
+            };
+            auto commit = [&](uint64_t* bar) {
+                if (ptx::elect_one()) ptx::mma_commit(ptx::smem_addr(bar));
+                __syncwarp();
             };
             // S_t(j+1) may overwrite the S_t columns once the softmax has read S_t(j) (P in its
             // own columns) or once O_t += P_t(j) V_j has consumed P_t(j) (P over S).
@@ -225,50 +242,47 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             };
             auto issue_next_s = [&](int j1) -> bool {  // S for KV tile j1 >= 1
                 const int s1 = j1 % C::NS;
-                if (!wait_phase(ptx::smem_addr(&bars->k_full[s1]), (uint32_t)(j1 / C::NS) & 1u,
+                if (!warp_wait(ptx::smem_addr(&bars->k_full[s1]), (uint32_t)(j1 / C::NS) & 1u,
                                 abort_flag, err, kDevTimeoutLoad))
                     return false;
                 ptx::tc_fence_after();
                 for (int t = 0; t < 2; ++t) {
                     if (j1 >= ntile[t]) continue;
-                    if (!wait_phase(s_release(t), (uint32_t)(j1 - 1) & 1u, abort_flag, err,
+                    if (!warp_wait(s_release(t), (uint32_t)(j1 - 1) & 1u, abort_flag, err,
                                     kDevTimeoutSoftmax))
                         return false;
                     ptx::tc_fence_after();
                     issue_s(t, s1);
-                    ptx::mma_commit(ptx::smem_addr(&bars->s_full[t]));
                 }
-                ptx::mma_commit(ptx::smem_addr(&bars->k_empty[s1]));
+                commit(&bars->k_empty[s1]);
                 return true;
             };
             auto issue_pvs = [&](int j) -> bool {
                 const int s = j % C::NS;
-                if (!wait_phase(ptx::smem_addr(&bars->v_full[s]), (uint32_t)(j / C::NS) & 1u,
+                if (!warp_wait(ptx::smem_addr(&bars->v_full[s]), (uint32_t)(j / C::NS) & 1u,
                                 abort_flag, err, kDevTimeoutLoad))
                     return false;
                 for (int t = 0; t < 2; ++t) {
                     if (j >= ntile[t]) continue;
-                    if (!wait_phase(ptx::smem_addr(&bars->p_full[t]), (uint32_t)j & 1u, abort_flag,
+                    if (!warp_wait(ptx::smem_addr(&bars->p_full[t]), (uint32_t)j & 1u, abort_flag,
                                     err, kDevTimeoutSoftmax))
                         return false;
                     ptx::tc_fence_after();
                     issue_pv(t, s, j > 0);
-                    ptx::mma_commit(ptx::smem_addr(&bars->o_done[t]));
                 }
-                ptx::mma_commit(ptx::smem_addr(&bars->v_empty[s]));
+                commit(&bars->v_empty[s]);
                 return true;
             };
-            bool ok = wait_phase(b_q_full, 0, abort_flag, err, kDevTimeoutLoad);
-            if (ok) ok = wait_phase(ptx::smem_addr(&bars->k_full[0]), 0, abort_flag, err,
+            bool ok = warp_wait(b_q_full, 0, abort_flag, err, kDevTimeoutLoad);
+            if (ok) ok = warp_wait(ptx::smem_addr(&bars->k_full[0]), 0, abort_flag, err,
                                     kDevTimeoutLoad);
             if (ok) {
                 ptx::tc_fence_after();
                 for (int t = 0; t < 2; ++t) {
                     if (ntile[t] == 0) continue;
                     issue_s(t, 0);
-                    ptx::mma_commit(ptx::smem_addr(&bars->s_full[t]));
                 }
-                ptx::mma_commit(ptx::smem_addr(&bars->k_empty[0]));
+                commit(&bars->k_empty[0]);
             }
             for (int j = 0; ok && j < nkv; ++j) {
                 if (C::P_SEPARATE) {
@@ -282,7 +296,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             }
             // Every MMA issued (and every commit arrive) must be done before TMEM and the
             // barriers are released.
-            ptx::mma_commit(ptx::smem_addr(&bars->mma_final));
+            commit(&bars->mma_final);
             drain_wait(ptx::smem_addr(&bars->mma_final), 0);
         }
     } else if (warp >= 4) {

@@ -150,6 +150,19 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     return p;
 }
 
+// One lane of a fully active warp (the lowest) gets true. Issuing tcgen05 work from an
+// elected lane inside warp-uniform code keeps descriptors and TMEM addresses in uniform
+// registers, which tcgen05.mma reads directly.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "elect.sync _|P, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, P;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 // ---- named barriers ------------------------------------------------------------------------
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
@@ -238,6 +251,13 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
     d |= (uint64_t)1 << 46;
     d |= (uint64_t)2 << 61;
     return d;
+}
+
+// Advance a descriptor's start address by `bytes` (a multiple of 16): the start field holds
+// addr >> 4 in bits 0-13 and shared addresses stay below 256 KB, so the add never carries out
+// of the field. Lets the MMA issuer build each descriptor once and step it with constants.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t d, uint32_t bytes) {
+    return d + (uint64_t)(bytes >> 4);
 }
 
 // ---- tcgen05: TMEM <-> registers ------------------------------------------------------
