@@ -31,6 +31,15 @@ FWD_KERNEL_SRC = os.path.join(ROOT, "exact_io_aware_fa_gb300", "csrc", "fa_fwd.c
 BWD_KERNEL_SRC = os.path.join(ROOT, "exact_io_aware_fa_gb300", "csrc", "fa_bwd.cu")
 TRAFFIC_JSON = os.path.join(ROOT, "profiles", "traffic.json")
 L2_FLUSH_BYTES = 512 << 20
+METRIC = ("attention fwd+bwd TFLOPS (bf16 in, fp32 accumulate), 1 step = fa_forward + fa_backward"
+          " on B4 H16 N2048 d64")
+
+
+def workload_config(world=1):
+    w = WORKLOAD
+    return {"workload": w["name"], "global_batch": w["B"] * world, "seq_len": w["N"],
+            "heads": w["H"], "head_dim": w["d"], "causal": w["causal"],
+            "parallelism": f"heads-replica x{world}" if world > 1 else "single"}
 
 
 def fwd_flops(B, H, N, d, causal):
@@ -84,19 +93,13 @@ def dist_init(n_gpus):
 
 
 def barrier(world):
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
+    from exact_io_aware_fa_gb300 import dist as fadist
+    fadist.barrier()
 
 
 def max_over_ranks(x, world):
-    if world == 1:
-        return x
-    import torch
-    import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+    from exact_io_aware_fa_gb300 import dist as fadist
+    return fadist.max_over_ranks(x, device="cuda" if world > 1 else None)
 
 
 # ---- clocks sampling ------------------------------------------------------------------------
@@ -184,14 +187,13 @@ def run_reference(args, rank, world):
         total_f += fl
     value = total_f / total_t / 1e12
     line = {
-        "impl": "reference", "metric": "attention fwd+bwd TFLOPS (fp64 CPU oracle, sampled heads)",
+        "impl": "reference", "metric": METRIC,
         "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": w["name"], "global_batch": w["B"], "seq_len": w["N"],
-                   "heads": w["H"], "head_dim": w["d"], "causal": w["causal"],
-                   "sample": f"{heads} of {w['B'] * w['H']} heads per step", "l2": "n/a (CPU)"},
+        "config": dict(workload_config(1), l2="n/a (CPU)",
+                       sample=f"{heads} of {w['B'] * w['H']} heads per step (fp64 oracle)"),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": f"{heads} heads of B4 H16 N2048 d64, fwd+bwd, per step"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -217,7 +219,9 @@ def run_ours(args, rank, world, local):
     B, H, N, d, causal = w["B"], w["H"], w["N"], w["d"], w["causal"]
     scale = 1.0 / math.sqrt(d)
     # Weak scaling: every rank runs the full workload on its own heads (its own seed).
-    bits = synthetic.attention_inputs(B, H, N, d, seed=w["seed"] + 1000 * rank, with_dout=True)
+    from exact_io_aware_fa_gb300 import dist as fadist
+    bits = synthetic.attention_inputs(B, H, N, d, seed=fadist.rank_seed(w["seed"], rank),
+                                      with_dout=True)
 
     def dev_t(b):
         return torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).to(dev)
@@ -275,7 +279,7 @@ def run_ours(args, rank, world, local):
     total_ms = max_over_ranks(total_ms, world)
     ff = fwd_flops(B, H, N, d, causal)
     bf = bwd_flops(B, H, N, d, causal)
-    value = world * args.steps * (ff + bf) / (total_ms * 1e-3) / 1e12
+    value = fadist.weak_scaling_value(ff + bf, args.steps, world, total_ms * 1e-3)
     peaks = load_peaks()
     fwd_avg = sum(fwd_ms) / len(fwd_ms)
     bwd_avg = sum(bwd_ms) / len(bwd_ms)
@@ -324,7 +328,8 @@ def run_ours(args, rank, world, local):
         eb.record(stream)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(ea.elapsed_time(eb), world)
-        e2e = {"value": world * args.steps * (ff + bf) / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": fadist.weak_scaling_value(ff + bf, args.steps, world, e2e_ms * 1e-3),
+               "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_ms / args.steps}
 
@@ -338,14 +343,12 @@ def run_ours(args, rank, world, local):
     if rank != 0:
         return
     line = {
-        "metric": "attention fwd+bwd TFLOPS (bf16 in, fp32 accumulate), 1 step = fa_forward + fa_backward",
+        "metric": METRIC,
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w["name"], "global_batch": w["B"] * world, "seq_len": N,
-                   "heads": H, "head_dim": d, "causal": causal,
-                   "parallelism": f"heads-replica x{world}" if world > 1 else "single",
-                   "l2": "flushed between timed steps (512 MiB write outside the events)"},
+        "config": dict(workload_config(world),
+                       l2="flushed between timed steps (512 MiB write outside the events)"),
         "fwd": {"ms": fwd_avg, "tflops": fwd_tf, "frac_of_peak": fwd_tf / peaks["bf16_tflops"]},
         "bwd": {"ms": bwd_avg, "tflops": bwd_tf, "frac_of_peak": bwd_tf / peaks["bf16_tflops"]},
         "roofline": {"kernel": dominant, "bound": "tensor", "achieved": dom_tf,

@@ -139,7 +139,7 @@ struct BwdCfg {
     static constexpr uint32_t OFF_DQS = OFF_DS + 2 * DS_BYTES;
     static constexpr uint32_t OFF_BAR = OFF_DQS + DQS_BYTES;
     static constexpr uint32_t SMEM_BYTES = OFF_BAR + 512 + 1024;
-    static constexpr int THREADS = 384;
+    static constexpr int THREADS = 512;
     // TMEM columns. d=128: dV[0,128) dK[128,256) S^T[256,320) dP^T[320,384) dQ^T[384,448)
     // P^T[448,480). d=64: dV[0,64) dK[64,128) S^T[128,256) dP^T[256,384) dQ[384,448) P^T[448,512).
     static constexpr uint32_t DV_COL = 0;
@@ -162,7 +162,7 @@ struct BwdBars {
 };
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(512, 1)
 fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
               const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
@@ -191,8 +191,8 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             ptx::mbar_init(ptx::smem_addr(&bars->q_empty[s]), 1);
         }
         ptx::mbar_init(ptx::smem_addr(&bars->s_full), 1);
-        ptx::mbar_init(ptx::smem_addr(&bars->s_free), 128);
-        ptx::mbar_init(ptx::smem_addr(&bars->p_ready), 128);
+        ptx::mbar_init(ptx::smem_addr(&bars->s_free), 256);
+        ptx::mbar_init(ptx::smem_addr(&bars->p_ready), 256);
         ptx::mbar_init(ptx::smem_addr(&bars->mma_done), 1);
         ptx::mbar_init(ptx::smem_addr(&bars->ds_free[0]), 1);
         ptx::mbar_init(ptx::smem_addr(&bars->ds_free[1]), 1);
@@ -374,8 +374,11 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             commit(&bars->final_bar);
             drain_wait(ptx::smem_addr(&bars->final_bar), 0);
         }
-    } else if (warp >= 4 && warp < 8) {
-        // ============== compute warpgroup: P^T and dS^T, one thread per key row ==============
+    } else if (warp >= 4 && warp < 12) {
+        // ============ compute warpgroups: P^T and dS^T, one thread per key row ============
+        // Two warpgroups split each step's query columns (half h takes 32-column chunks
+        // [h*NCH/2, (h+1)*NCH/2)), so every SMSP runs two compute warps.
+        const int h = (warp - 4) >> 2;
         const int wq = warp & 3;
         const int k = wq * 32 + lane;  // key row within the tile
         const int key = key0 + k;
@@ -384,6 +387,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const uint32_t t_dp = tbase + lane_off + C::DP_COL;
         const uint32_t t_pt = tbase + lane_off + C::PT_COL;
         constexpr int NCH = C::BMQ / 32;
+        constexpr int NCH_H = NCH / 2;
         bool ok = true;
         for (int si = 0; si < nsteps; ++si) {
             const int st = si % C::NQS;
@@ -400,44 +404,47 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             const float* dvec = lse2 + C::BMQ;
             uint8_t* dsbuf = smem + C::OFF_DS + (si & 1) * C::DS_BYTES;
             const bool need_mask = CAUSAL && (q0 < key0 + C::KT - 1);
-#pragma unroll 1
-            for (int cc = 0; cc < NCH; ++cc) {
+#pragma unroll
+            for (int ci = 0; ci < NCH_H; ++ci) {
+                const int cc = h * NCH_H + ci;
                 uint32_t sv[32], dpv[32];
                 ptx::tmem_ld32_nowait(t_s + 32 * cc, sv);
                 ptx::tmem_ld32_nowait(t_dp + 32 * cc, dpv);
                 ptx::tmem_wait_ld(sv);
                 ptx::tmem_wait_ld(dpv);
-                if (cc == NCH - 1) {
-                    // every S^T/dP^T column of this step is in registers: release them
+                if (ci == NCH_H - 1) {
+                    // this half's S^T/dP^T columns are in registers: release them
                     ptx::tc_fence_before();
                     ptx::mbar_arrive(ptx::smem_addr(&bars->s_free));
                 }
-                float p[32], ds[32];
+                uint32_t pk[16], dk[16];
 #pragma unroll
-                for (int j = 0; j < 32; j += 2) {
+                for (int j = 0; j < 32; j += 4) {
                     const int qi = 32 * cc + j;
-                    float x0, x1;
-                    ptx::ffma2(x0, x1, __uint_as_float(sv[j]), __uint_as_float(sv[j + 1]), c, c,
-                               -lse2[qi], -lse2[qi + 1]);
+                    const float4 L = *reinterpret_cast<const float4*>(lse2 + qi);  // broadcast
+                    const float4 Dq = *reinterpret_cast<const float4*>(dvec + qi);
+                    float x0, x1, x2, x3;
+                    ptx::ffma2(x0, x1, __uint_as_float(sv[j]), __uint_as_float(sv[j + 1]), c, c, -L.x, -L.y);
+                    ptx::ffma2(x2, x3, __uint_as_float(sv[j + 2]), __uint_as_float(sv[j + 3]), c, c, -L.z, -L.w);
                     float p0 = ptx::ex2_approx(x0), p1 = ptx::ex2_approx(x1);
+                    float p2 = ptx::ex2_approx(x2), p3 = ptx::ex2_approx(x3);
                     if (need_mask) {
                         if (key > q0 + qi) p0 = 0.f;
                         if (key > q0 + qi + 1) p1 = 0.f;
+                        if (key > q0 + qi + 2) p2 = 0.f;
+                        if (key > q0 + qi + 3) p3 = 0.f;
                     }
-                    p[j] = p0;
-                    p[j + 1] = p1;
-                    float y0, y1;
-                    ptx::fadd2(y0, y1, __uint_as_float(dpv[j]), __uint_as_float(dpv[j + 1]), -dvec[qi],
-                               -dvec[qi + 1]);
-                    ptx::fmul2(ds[j], ds[j + 1], p0, p1, y0, y1);
+                    float y0, y1, y2, y3, d0, d1, d2, d3;
+                    ptx::fadd2(y0, y1, __uint_as_float(dpv[j]), __uint_as_float(dpv[j + 1]), -Dq.x, -Dq.y);
+                    ptx::fadd2(y2, y3, __uint_as_float(dpv[j + 2]), __uint_as_float(dpv[j + 3]), -Dq.z, -Dq.w);
+                    ptx::fmul2(d0, d1, p0, p1, y0, y1);
+                    ptx::fmul2(d2, d3, p2, p3, y2, y3);
+                    pk[j / 2] = ptx::pack_bf16x2(p0, p1);
+                    pk[j / 2 + 1] = ptx::pack_bf16x2(p2, p3);
+                    dk[j / 2] = ptx::pack_bf16x2(d0, d1);
+                    dk[j / 2 + 1] = ptx::pack_bf16x2(d2, d3);
                 }
-                uint32_t pk[16], dk[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    pk[j] = ptx::pack_bf16x2(p[2 * j], p[2 * j + 1]);
-                    dk[j] = ptx::pack_bf16x2(ds[2 * j], ds[2 * j + 1]);
-                }
-                if (cc == 0) {
+                if (ci == 0) {
                     if (si > 0) {
                         // dV(si-1) must have read P^T before it is overwritten.
                         ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->mma_done),
@@ -469,11 +476,11 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             ptx::tc_fence_before();
             ptx::mbar_arrive(ptx::smem_addr(&bars->p_ready));
         }
-        // ---- epilogue: dV -> bf16 -> smem (stage 0 area) -> TMA store ----
-        if (ok) ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->mma_done),
+        // ---- epilogue (first compute warpgroup): dV -> bf16 -> smem (stage 0 area) -> TMA store ----
+        if (ok && h == 0) ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->mma_done),
                                                         (uint32_t)(nsteps - 1) & 1u, abort_flag,
                                                         err, kDevTimeoutMma));
-        if (ok) {
+        if (ok && h == 0) {
             ptx::tc_fence_after();
             uint8_t* stage = smem + C::OFF_ST;
 #pragma unroll
@@ -500,7 +507,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 ptx::bulk_wait_read_all();
             }
         }
-    } else if (warp >= 8) {
+    } else if (warp >= 12) {
         // ============== dQ drain warpgroup, then the dK epilogue ==============
         const int wq = warp & 3;
         const int r = wq * 32 + lane;  // TMEM lane: d index (d=128) or query row (d=64)
