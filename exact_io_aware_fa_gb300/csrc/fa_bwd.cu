@@ -198,7 +198,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         ptx::mbar_init(ptx::smem_addr(&bars->ds_free[1]), 1);
         ptx::mbar_init(ptx::smem_addr(&bars->dq_full), 1);
         ptx::mbar_init(ptx::smem_addr(&bars->dq_free), 128);
-        ptx::mbar_init(ptx::smem_addr(&bars->final_bar), 1);
+        ptx::mbar_init(ptx::smem_addr(&bars->final_bar), 2);
         bars->abort_flag = 0;
         ptx::fence_barrier_init();
         ptx::tma_prefetch_desc(&tm_q);
@@ -259,8 +259,8 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             for (int si = max(0, issued - C::NQS); si < issued; ++si)
                 drain_wait(ptx::smem_addr(&bars->q_full[si % C::NQS]), (uint32_t)(si / C::NQS) & 1u);
         }
-    } else if (warp == 1) {
-        // ================================ MMA issuer ==================================
+    } else if (warp == 1 || warp == 3) {
+        // ================================ MMA issuers =================================
         {  // whole warp; one elected lane issues
             constexpr uint32_t idesc_s = ptx::idesc_bf16(128, C::BMQ, false, false);  // S^T, dP^T
             constexpr uint32_t idesc_kv = ptx::idesc_bf16(128, D, false, true);       // dV, dK
@@ -302,15 +302,16 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 if (ptx::elect_one()) ptx::mma_commit(ptx::smem_addr(bar));
                 __syncwarp();
             };
+            // Two issuing warps (see the forward): warp 1 issues S^T/dP^T, warp 3 issues
+            // dV/dK/dQ, so one warp's MMAs run while the other waits for operands.
             bool ok = warp_wait(ptx::smem_addr(&bars->kv_full), 0, abort_flag, err, kDevTimeoutLoad);
-            if (ok) ok = warp_wait(ptx::smem_addr(&bars->q_full[0]), 0, abort_flag, err, kDevTimeoutLoad);
-            if (ok) {
-                ptx::tc_fence_after();
-                issue_s_dp(0);
-            }
-            for (int si = 0; ok && si < nsteps; ++si) {
-                const int st = si % C::NQS;
-                if (si + 1 < nsteps) {
+            if (warp == 1) {
+                if (ok) ok = warp_wait(ptx::smem_addr(&bars->q_full[0]), 0, abort_flag, err, kDevTimeoutLoad);
+                if (ok) {
+                    ptx::tc_fence_after();
+                    issue_s_dp(0);
+                }
+                for (int si = 0; ok && si + 1 < nsteps; ++si) {
                     // Next S^T/dP^T as soon as the compute warps have read this step's.
                     const int st1 = (si + 1) % C::NQS;
                     ok = warp_wait(ptx::smem_addr(&bars->q_full[st1]), (uint32_t)((si + 1) / C::NQS) & 1u,
@@ -321,6 +322,9 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     ptx::tc_fence_after();
                     issue_s_dp(si + 1);
                 }
+            }
+            for (int si = 0; warp == 3 && ok && si < nsteps; ++si) {
+                const int st = si % C::NQS;
                 ok = warp_wait(ptx::smem_addr(&bars->p_ready), (uint32_t)si & 1u, abort_flag, err,
                                 kDevTimeoutSoftmax);
                 if (!ok) break;

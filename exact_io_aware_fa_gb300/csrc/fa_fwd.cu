@@ -14,7 +14,8 @@
 //
 // GB300 mapping (one CTA = 256 query rows of one (batch, head) = two 128-row Q tiles):
 //   warp 0      TMA producer: Q tiles once, then K_j / V_j into separate mbarrier rings
-//   warp 1      MMA issuer: S_t = Q_t K_j^T and O_t += P_t V_j with tcgen05.mma (fp32 in TMEM)
+//   warp 1      MMA issuer for S_t = Q_t K_j^T (tcgen05.mma, fp32 in TMEM)
+//   warp 3      MMA issuer for O_t += P_t V_j
 //   warp 2      TMEM allocation / release
 //   warps 4-7   softmax for Q tile 0, warps 8-11 softmax for Q tile 1: one thread per row,
 //               the whole row of S read from TMEM into registers (no cross-thread reduction),
@@ -126,7 +127,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             ptx::mbar_init(ptx::smem_addr(&bars->p_full[t]), C::BM);
             ptx::mbar_init(ptx::smem_addr(&bars->o_done[t]), 1);
         }
-        ptx::mbar_init(ptx::smem_addr(&bars->mma_final), 1);
+        ptx::mbar_init(ptx::smem_addr(&bars->mma_final), 2);
         bars->abort_flag = 0;
         ptx::fence_barrier_init();
         ptx::tma_prefetch_desc(&tm_q);
@@ -191,8 +192,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             for (int j = max(0, jv - C::NS); j < jv; ++j)
                 drain_wait(ptx::smem_addr(&bars->v_full[j % C::NS]), (uint32_t)(j / C::NS) & 1u);
         }
-    } else if (warp == 1) {
-        // ================================ MMA issuer ==================================
+    } else if (warp == 1 || warp == 3) {
+        // ================================ MMA issuers =================================
         if (nkv > 0) {  // whole warp; one elected lane issues
             constexpr uint32_t idesc_s = ptx::idesc_bf16(128, C::BN, false, false);
             constexpr uint32_t idesc_o = ptx::idesc_bf16(128, D, false, true);
@@ -273,29 +274,29 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 commit(&bars->v_empty[s]);
                 return true;
             };
-            bool ok = warp_wait(b_q_full, 0, abort_flag, err, kDevTimeoutLoad);
-            if (ok) ok = warp_wait(ptx::smem_addr(&bars->k_full[0]), 0, abort_flag, err,
-                                    kDevTimeoutLoad);
-            if (ok) {
-                ptx::tc_fence_after();
-                for (int t = 0; t < 2; ++t) {
-                    if (ntile[t] == 0) continue;
-                    issue_s(t, 0);
+            // Two issuing warps: warp 1 issues the S MMAs, warp 3 the PV MMAs. A thread that
+            // issues MMAs stalls until the tensor pipe has (almost) drained them, so with one
+            // issuer every barrier wait left the pipe empty; with two, one warp's MMAs run
+            // while the other waits for its next operands.
+            bool ok = true;
+            if (warp == 1) {
+                ok = warp_wait(b_q_full, 0, abort_flag, err, kDevTimeoutLoad);
+                if (ok) ok = warp_wait(ptx::smem_addr(&bars->k_full[0]), 0, abort_flag, err,
+                                        kDevTimeoutLoad);
+                if (ok) {
+                    ptx::tc_fence_after();
+                    for (int t = 0; t < 2; ++t) {
+                        if (ntile[t] == 0) continue;
+                        issue_s(t, 0);
+                    }
+                    commit(&bars->k_empty[0]);
                 }
-                commit(&bars->k_empty[0]);
+                for (int j = 1; ok && j < nkv; ++j) ok = issue_next_s(j);
+            } else {
+                for (int j = 0; ok && j < nkv; ++j) ok = issue_pvs(j);
             }
-            for (int j = 0; ok && j < nkv; ++j) {
-                if (C::P_SEPARATE) {
-                    // Next scores first: they only wait for the softmax to have read S(j).
-                    if (j + 1 < nkv) ok = issue_next_s(j + 1);
-                    if (ok) ok = issue_pvs(j);
-                } else {
-                    ok = issue_pvs(j);
-                    if (ok && j + 1 < nkv) ok = issue_next_s(j + 1);
-                }
-            }
-            // Every MMA issued (and every commit arrive) must be done before TMEM and the
-            // barriers are released.
+            // Every MMA this warp issued (and every commit arrive) must be done before TMEM
+            // and the barriers are released (mma_final expects one arrive per issuing warp).
             commit(&bars->mma_final);
             drain_wait(ptx::smem_addr(&bars->mma_final), 0);
         }
