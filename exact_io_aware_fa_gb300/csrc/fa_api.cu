@@ -22,6 +22,7 @@ __device__ int g_fa_error_word;
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 int* g_err_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -65,6 +66,23 @@ fa_status get_err_ptr(int** out) {
         g_err_ptr[dev] = static_cast<int*>(p);
     }
     *out = g_err_ptr[dev];
+    return FA_OK;
+}
+
+// Streaming-multiprocessor count of the current device (looked up once per device).
+fa_status get_num_sms(int* out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_num_sms[dev] == 0) {
+        int n = 0;
+        e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e);
+        g_num_sms[dev] = n > 0 ? n : 1;
+    }
+    *out = g_num_sms[dev];
     return FA_OK;
 }
 
@@ -170,6 +188,7 @@ fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float
     if ((st = make_map(&a.tm_v, v, BH, N, d, 128)) != FA_OK) return st;
     if ((st = make_map(&a.tm_o, o, BH, N, d, 128)) != FA_OK) return st;
     if ((st = get_err_ptr(&a.err)) != FA_OK) return st;
+    if ((st = get_num_sms(&a.num_sms)) != FA_OK) return st;
     a.N = N;
     a.BH = BH;
     a.c = scale * kLog2e;

@@ -12,7 +12,9 @@
 //   at the end O = a / l and LSE = m + ln l. Tiles wholly above the causal diagonal are
 //   skipped; only the diagonal tile and the ragged last tile are masked elementwise.
 //
-// GB300 mapping (one CTA = 256 query rows of one (batch, head) = two 128-row Q tiles):
+// GB300 mapping: a persistent grid of one CTA per SM; a CTA walks work units (one unit = 256
+// query rows of one (batch, head) = two 128-row Q tiles) so that the next unit's loads and
+// first score MMAs overlap the current unit's epilogue. Roles:
 //   warp 0      TMA producer: Q tiles once, then K_j / V_j into separate mbarrier rings
 //   warp 1      MMA issuer for S_t = Q_t K_j^T (tcgen05.mma, fp32 in TMEM)
 //   warp 3      MMA issuer for O_t += P_t V_j
@@ -23,6 +25,8 @@
 //               over the S columns, O rescaled in TMEM when the row max moves, and the
 //               epilogue (O / l -> bf16 -> swizzled smem -> TMA store; LSE -> global).
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 and O_1 after column 256.
+#include <algorithm>
+
 #include "fa_common.cuh"
 #include "fa_launch.h"
 
@@ -40,8 +44,11 @@ struct FwdCfg {
     static constexpr int NS = (D == 64) ? 3 : 2;  // K and V ring depth
     static constexpr uint32_t TILE_BYTES = 128u * D * 2u;  // one 128-row bf16 tile
     static constexpr uint32_t CHUNK_BYTES = 128u * 128u;   // one 128-row x 64-col chunk
+    // Q buffers: two at d=64 (the next unit's Q loads while this unit finishes), one at d=128
+    // (the next Q waits for the epilogue, which stages O in the Q buffer, to release it).
+    static constexpr int NQB = (D == 64) ? 2 : 1;
     static constexpr uint32_t OFF_Q = 0;
-    static constexpr uint32_t OFF_K = OFF_Q + 2 * TILE_BYTES;
+    static constexpr uint32_t OFF_K = OFF_Q + NQB * 2 * TILE_BYTES;
     static constexpr uint32_t OFF_V = OFF_K + NS * TILE_BYTES;
     static constexpr uint32_t OFF_BAR = OFF_V + NS * TILE_BYTES;
     static constexpr uint32_t SMEM_BYTES = OFF_BAR + 512 + 1024;  // + alignment slack
@@ -65,7 +72,8 @@ struct FwdCfg {
 constexpr float kTau = 0.0f;
 
 struct FwdBars {
-    uint64_t q_full;
+    uint64_t q_full[2], q_free[2];
+    uint64_t o_free[2];
     uint64_t k_full[3], k_empty[3];
     uint64_t v_full[3], v_empty[3];
     uint64_t s_full[2], s_free[2], p_full[2], o_done[2];
@@ -86,11 +94,49 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     }
 }
 
+// One work unit: (bh, 256-row block qb).
+struct FwdUnit {
+    int bh, qb, n0, n1, nkv;
+};
+
+// The k-th unit of CTA `cta` (of G), or -1 past the end. Units are numbered head by head.
+// Non-causal: plain round robin. Causal: a head's blocks are ordered heaviest, lightest,
+// second heaviest, second lightest, ... and each CTA takes consecutive pairs, so every pair
+// (and so every CTA's share of a round) costs about the same while concurrently running CTAs
+// still work on a few neighbouring heads (their K/V stays in L2).
+template <bool CAUSAL>
+__device__ __forceinline__ int fwd_unit_index(int cta, int k, int G, int U) {
+    const long long u = CAUSAL ? 2LL * (cta + (long long)(k >> 1) * G) + (k & 1)
+                               : cta + (long long)k * G;
+    return u < U ? (int)u : -1;
+}
+
+template <int D, bool CAUSAL>
+__device__ __forceinline__ FwdUnit fwd_unit(int u, int nqb, int N) {
+    using C = FwdCfg<D>;
+    FwdUnit w;
+    w.bh = u / nqb;
+    const int i = u % nqb;
+    if (CAUSAL) {
+        const int q = (i & 1) ? nqb - 1 - (i >> 1) : (i >> 1);  // rank by cost, 0 = heaviest
+        w.qb = nqb - 1 - q;
+    } else {
+        w.qb = i;
+    }
+    const int nk_total = (N + C::BN - 1) / C::BN;
+    const int r1 = w.qb * C::ROWS + C::BM;
+    w.n0 = CAUSAL ? min(nk_total, w.qb * 2 + 1) : nk_total;
+    w.n1 = (r1 >= N) ? 0 : (CAUSAL ? min(nk_total, w.qb * 2 + 2) : nk_total);
+    w.nkv = max(w.n0, w.n1);
+    return w;
+}
+
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(384, 1)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-              const int N, const int nqb, const float c, float* __restrict__ lse_out, int* err) {
+              const int N, const int nqb, const int num_units, const float c,
+              float* __restrict__ lse_out, int* err) {
     using C = FwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
@@ -98,23 +144,13 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
+    const int G = gridDim.x;
 
-    // ---- work unit: (bh, 256-row block), heaviest causal blocks of a head first ----------
-    const int bh = blockIdx.x / nqb;
-    int qb = blockIdx.x % nqb;
-    if (CAUSAL) qb = nqb - 1 - qb;
-    const int nk_total = (N + C::BN - 1) / C::BN;
-    int ntile[2];
-#pragma unroll
-    for (int t = 0; t < 2; ++t) {
-        const int r0 = qb * C::ROWS + t * C::BM;
-        ntile[t] = (r0 >= N) ? 0 : (CAUSAL ? min(nk_total, qb * 2 + t + 1) : nk_total);
-    }
-    const int nkv = max(ntile[0], ntile[1]);
-
-    const uint32_t b_q_full = ptx::smem_addr(&bars->q_full);
     if (tid == 0) {
-        ptx::mbar_init(b_q_full, 1);
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(ptx::smem_addr(&bars->q_full[b]), 1);
+            ptx::mbar_init(ptx::smem_addr(&bars->q_free[b]), 2);  // one arrive per Q tile
+        }
         for (int s = 0; s < C::NS; ++s) {
             ptx::mbar_init(ptx::smem_addr(&bars->k_full[s]), 1);
             ptx::mbar_init(ptx::smem_addr(&bars->k_empty[s]), 1);
@@ -126,6 +162,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             ptx::mbar_init(ptx::smem_addr(&bars->s_free[t]), C::BM);
             ptx::mbar_init(ptx::smem_addr(&bars->p_full[t]), C::BM);
             ptx::mbar_init(ptx::smem_addr(&bars->o_done[t]), 1);
+            ptx::mbar_init(ptx::smem_addr(&bars->o_free[t]), C::BM);
         }
         ptx::mbar_init(ptx::smem_addr(&bars->mma_final), 2);
         bars->abort_flag = 0;
@@ -151,163 +188,172 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 
     if (warp == 0) {
         // ================================ TMA producer ================================
-        if (lane == 0 && nkv > 0) {
+        if (lane == 0) {
             const uint64_t pol_kv = ptx::l2_policy_evict_last();
             const uint64_t pol_q = ptx::l2_policy_evict_first();
-            const int ntl = (ntile[0] > 0) + (ntile[1] > 0);
-            ptx::mbar_arrive_expect_tx(b_q_full, ntl * C::TILE_BYTES);
-            for (int t = 0; t < 2; ++t) {
-                if (ntile[t] == 0) continue;
-                for (int ch = 0; ch < C::DCH; ++ch)
-                    ptx::tma_load_3d_hint(s_q + t * C::TILE_BYTES + ch * C::CHUNK_BYTES, &tm_q,
-                                          b_q_full, ch * 64, qb * C::ROWS + t * C::BM, bh, pol_q);
-            }
-            int jk = 0, jv = 0;
-            for (int j = 0; j < nkv; ++j) {
-                const int s = j % C::NS;
-                const uint32_t ph = (uint32_t)(j / C::NS) & 1u;
-                const uint32_t bkf = ptx::smem_addr(&bars->k_full[s]);
-                const uint32_t bvf = ptx::smem_addr(&bars->v_full[s]);
-                if (!wait_phase(ptx::smem_addr(&bars->k_empty[s]), ph ^ 1u, abort_flag, err,
-                                kDevTimeoutConsumer))
-                    break;
-                ptx::mbar_arrive_expect_tx(bkf, C::TILE_BYTES);
-                for (int ch = 0; ch < C::DCH; ++ch)
-                    ptx::tma_load_3d_hint(s_k + s * C::TILE_BYTES + ch * C::CHUNK_BYTES, &tm_k, bkf,
-                                          ch * 64, j * C::BN, bh, pol_kv);
-                ++jk;
-                if (!wait_phase(ptx::smem_addr(&bars->v_empty[s]), ph ^ 1u, abort_flag, err,
-                                kDevTimeoutConsumer))
-                    break;
-                ptx::mbar_arrive_expect_tx(bvf, C::TILE_BYTES);
-                for (int ch = 0; ch < C::DCH; ++ch)
-                    ptx::tma_load_3d_hint(s_v + s * C::TILE_BYTES + ch * C::CHUNK_BYTES, &tm_v, bvf,
-                                          ch * 64, j * C::BN, bh, pol_kv);
-                ++jv;
+            int kv = 0;   // K/V tiles loaded so far (ring position)
+            int ul = 0;   // units started by this CTA
+            int last_q_use[2] = {-1, -1};
+            bool ok = true;
+            for (int u; ok && (u = fwd_unit_index<CAUSAL>(blockIdx.x, ul, G, num_units)) >= 0; ++ul) {
+                const FwdUnit w = fwd_unit<D, CAUSAL>(u, nqb, N);
+                const int b = ul % C::NQB;
+                const int use = ul / C::NQB;  // earlier uses of Q buffer b
+                if (use > 0) {
+                    // the epilogues of unit (ul - NQB) staged O in this buffer and stored it
+                    ok = wait_phase(ptx::smem_addr(&bars->q_free[b]), (uint32_t)(use - 1) & 1u,
+                                    abort_flag, err, kDevTimeoutSoftmax);
+                    if (!ok) break;
+                }
+                const uint32_t bq = ptx::smem_addr(&bars->q_full[b]);
+                const int ntl = 1 + (w.n1 > 0);
+                ptx::mbar_arrive_expect_tx(bq, ntl * C::TILE_BYTES);
+                for (int t = 0; t < ntl; ++t)
+                    for (int ch = 0; ch < C::DCH; ++ch)
+                        ptx::tma_load_3d_hint(s_q + (b * 2 + t) * C::TILE_BYTES + ch * C::CHUNK_BYTES,
+                                              &tm_q, bq, ch * 64, w.qb * C::ROWS + t * C::BM, w.bh,
+                                              pol_q);
+                last_q_use[b] = use;
+                for (int j = 0; j < w.nkv; ++j, ++kv) {
+                    const int s = kv % C::NS;
+                    const uint32_t ph = (uint32_t)(kv / C::NS) & 1u;
+                    const uint32_t bkf = ptx::smem_addr(&bars->k_full[s]);
+                    const uint32_t bvf = ptx::smem_addr(&bars->v_full[s]);
+                    ok = wait_phase(ptx::smem_addr(&bars->k_empty[s]), ph ^ 1u, abort_flag, err,
+                                    kDevTimeoutConsumer);
+                    if (!ok) break;
+                    ptx::mbar_arrive_expect_tx(bkf, C::TILE_BYTES);
+                    for (int ch = 0; ch < C::DCH; ++ch)
+                        ptx::tma_load_3d_hint(s_k + s * C::TILE_BYTES + ch * C::CHUNK_BYTES, &tm_k,
+                                              bkf, ch * 64, j * C::BN, w.bh, pol_kv);
+                    ok = wait_phase(ptx::smem_addr(&bars->v_empty[s]), ph ^ 1u, abort_flag, err,
+                                    kDevTimeoutConsumer);
+                    if (!ok) {
+                        drain_wait(bkf, ph);
+                        break;
+                    }
+                    ptx::mbar_arrive_expect_tx(bvf, C::TILE_BYTES);
+                    for (int ch = 0; ch < C::DCH; ++ch)
+                        ptx::tma_load_3d_hint(s_v + s * C::TILE_BYTES + ch * C::CHUNK_BYTES, &tm_v,
+                                              bvf, ch * 64, j * C::BN, w.bh, pol_kv);
+                }
             }
             // Drain: every copy issued must have landed before the CTA can exit.
-            drain_wait(b_q_full, 0);
-            for (int j = max(0, jk - C::NS); j < jk; ++j)
-                drain_wait(ptx::smem_addr(&bars->k_full[j % C::NS]), (uint32_t)(j / C::NS) & 1u);
-            for (int j = max(0, jv - C::NS); j < jv; ++j)
-                drain_wait(ptx::smem_addr(&bars->v_full[j % C::NS]), (uint32_t)(j / C::NS) & 1u);
+            for (int b = 0; b < 2; ++b)
+                if (last_q_use[b] >= 0)
+                    drain_wait(ptx::smem_addr(&bars->q_full[b]), (uint32_t)last_q_use[b] & 1u);
+            for (int x = max(0, kv - C::NS); x < kv; ++x) {
+                drain_wait(ptx::smem_addr(&bars->k_full[x % C::NS]), (uint32_t)(x / C::NS) & 1u);
+                drain_wait(ptx::smem_addr(&bars->v_full[x % C::NS]), (uint32_t)(x / C::NS) & 1u);
+            }
         }
     } else if (warp == 1 || warp == 3) {
         // ================================ MMA issuers =================================
-        if (nkv > 0) {  // whole warp; one elected lane issues
-            constexpr uint32_t idesc_s = ptx::idesc_bf16(128, C::BN, false, false);
-            constexpr uint32_t idesc_o = ptx::idesc_bf16(128, D, false, true);
-            // Descriptors are built once and stepped by constant offsets per MMA: the issuing
-            // thread shares its SMSP with two softmax warps, so every instruction it saves
-            // shortens the gap between MMAs.
-            const uint64_t dq0 = ptx::sdesc_sw128(s_q, 16, 1024);
-            const uint64_t dk0 = ptx::sdesc_sw128(s_k, 16, 1024);
-            const uint64_t dv0 = ptx::sdesc_sw128(s_v, C::CHUNK_BYTES, 1024);
-            auto issue_s = [&](int t, int stage) {  // S_t = Q_t K^T, then arrive on s_full[t]
-                const uint32_t d_tmem = tbase + C::s_col(t);
-                const uint64_t qd = ptx::sdesc_add(dq0, (uint32_t)t * C::TILE_BYTES);
-                const uint64_t kd = ptx::sdesc_add(dk0, (uint32_t)stage * C::TILE_BYTES);
-                if (ptx::elect_one()) {
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
-                        ptx::mma_ss(d_tmem, ptx::sdesc_add(qd, off), ptx::sdesc_add(kd, off), idesc_s,
-                                    kk > 0);
-                    }
-                    ptx::mma_commit(ptx::smem_addr(&bars->s_full[t]));
-                }
-                __syncwarp();
-            };
-            auto issue_pv = [&](int t, int stage, bool acc) {  // O_t += P_t V, arrive on o_done[t]
-                const uint32_t d_tmem = tbase + C::o_col(t);
-                const uint32_t p_tmem = tbase + C::p_col(t);
-                const uint64_t vd = ptx::sdesc_add(dv0, (uint32_t)stage * C::TILE_BYTES);
-                if (ptx::elect_one()) {
-#pragma unroll
-                    for (int kk = 0; kk < C::BN / 16; ++kk)
-                        ptx::mma_ts(d_tmem, p_tmem + kk * 8, ptx::sdesc_add(vd, kk * 2048), idesc_o,
-                                    (acc || kk > 0) ? 1u : 0u);
-                    ptx::mma_commit(ptx::smem_addr(&bars->o_done[t]));
-                }
-                __syncwarp();
-            };
-            auto commit = [&](uint64_t* bar) {
-                if (ptx::elect_one()) ptx::mma_commit(ptx::smem_addr(bar));
-                __syncwarp();
-            };
-            // S_t(j+1) may overwrite the S_t columns once the softmax has read S_t(j) (P in its
-            // own columns) or once O_t += P_t(j) V_j has consumed P_t(j) (P over S).
-            auto s_release = [&](int t) {
-                return C::P_SEPARATE ? ptx::smem_addr(&bars->s_free[t])
-                                     : ptx::smem_addr(&bars->o_done[t]);
-            };
-            auto issue_next_s = [&](int j1) -> bool {  // S for KV tile j1 >= 1
-                const int s1 = j1 % C::NS;
-                if (!warp_wait(ptx::smem_addr(&bars->k_full[s1]), (uint32_t)(j1 / C::NS) & 1u,
-                                abort_flag, err, kDevTimeoutLoad))
-                    return false;
-                ptx::tc_fence_after();
-                for (int t = 0; t < 2; ++t) {
-                    if (j1 >= ntile[t]) continue;
-                    if (!warp_wait(s_release(t), (uint32_t)(j1 - 1) & 1u, abort_flag, err,
-                                    kDevTimeoutSoftmax))
-                        return false;
-                    ptx::tc_fence_after();
-                    issue_s(t, s1);
-                }
-                commit(&bars->k_empty[s1]);
-                return true;
-            };
-            auto issue_pvs = [&](int j) -> bool {
-                const int s = j % C::NS;
-                if (!warp_wait(ptx::smem_addr(&bars->v_full[s]), (uint32_t)(j / C::NS) & 1u,
-                                abort_flag, err, kDevTimeoutLoad))
-                    return false;
-                for (int t = 0; t < 2; ++t) {
-                    if (j >= ntile[t]) continue;
-                    if (!warp_wait(ptx::smem_addr(&bars->p_full[t]), (uint32_t)j & 1u, abort_flag,
-                                    err, kDevTimeoutSoftmax))
-                        return false;
-                    ptx::tc_fence_after();
-                    issue_pv(t, s, j > 0);
-                }
-                commit(&bars->v_empty[s]);
-                return true;
-            };
-            // Two issuing warps: warp 1 issues the S MMAs, warp 3 the PV MMAs. A thread that
-            // issues MMAs stalls until the tensor pipe has (almost) drained them, so with one
-            // issuer every barrier wait left the pipe empty; with two, one warp's MMAs run
-            // while the other waits for its next operands.
-            bool ok = true;
+        // Two issuing warps: warp 1 issues the S MMAs, warp 3 the PV MMAs. A thread that
+        // issues MMAs stalls until the tensor pipe has (almost) drained them, so with one
+        // issuer every barrier wait left the pipe empty; with two, one warp's MMAs run while
+        // the other waits for its next operands. The whole warp runs the loop and one elected
+        // lane issues, which keeps descriptors and TMEM addresses in uniform registers.
+        constexpr uint32_t idesc_s = ptx::idesc_bf16(128, C::BN, false, false);
+        constexpr uint32_t idesc_o = ptx::idesc_bf16(128, D, false, true);
+        const uint64_t dq0 = ptx::sdesc_sw128(s_q, 16, 1024);
+        const uint64_t dk0 = ptx::sdesc_sw128(s_k, 16, 1024);
+        const uint64_t dv0 = ptx::sdesc_sw128(s_v, C::CHUNK_BYTES, 1024);
+        auto commit = [&](uint64_t* bar) {
+            if (ptx::elect_one()) ptx::mma_commit(ptx::smem_addr(bar));
+            __syncwarp();
+        };
+        int it[2] = {0, 0};  // score tiles (S) or products (PV) issued so far, per Q tile
+        int uo[2] = {0, 0};  // units in which each Q tile ran (PV issuer: o_free phases)
+        int kv = 0;
+        int ul = 0;
+        bool ok = true;
+        for (int u; ok && (u = fwd_unit_index<CAUSAL>(blockIdx.x, ul, G, num_units)) >= 0; ++ul) {
+            const FwdUnit w = fwd_unit<D, CAUSAL>(u, nqb, N);
+            const int nt[2] = {w.n0, w.n1};
+            const int b = ul % C::NQB;
             if (warp == 1) {
-                ok = warp_wait(b_q_full, 0, abort_flag, err, kDevTimeoutLoad);
-                if (ok) ok = warp_wait(ptx::smem_addr(&bars->k_full[0]), 0, abort_flag, err,
-                                        kDevTimeoutLoad);
-                if (ok) {
-                    ptx::tc_fence_after();
-                    for (int t = 0; t < 2; ++t) {
-                        if (ntile[t] == 0) continue;
-                        issue_s(t, 0);
+                ok = warp_wait(ptx::smem_addr(&bars->q_full[b]), (uint32_t)(ul / C::NQB) & 1u,
+                               abort_flag, err, kDevTimeoutLoad);
+                for (int j = 0; ok && j < w.nkv; ++j, ++kv) {
+                    const int s = kv % C::NS;
+                    ok = warp_wait(ptx::smem_addr(&bars->k_full[s]), (uint32_t)(kv / C::NS) & 1u,
+                                   abort_flag, err, kDevTimeoutLoad);
+                    for (int t = 0; ok && t < 2; ++t) {
+                        if (j >= nt[t]) continue;
+                        if (it[t] > 0) {
+                            // S_t may be overwritten once the softmax has read S_t (P in its own
+                            // columns) or once O_t += P_t V has consumed P_t (P over S).
+                            const uint32_t rel = C::P_SEPARATE ? ptx::smem_addr(&bars->s_free[t])
+                                                               : ptx::smem_addr(&bars->o_done[t]);
+                            ok = warp_wait(rel, (uint32_t)(it[t] - 1) & 1u, abort_flag, err,
+                                           kDevTimeoutSoftmax);
+                            if (!ok) break;
+                        }
+                        ptx::tc_fence_after();
+                        const uint32_t d_tmem = tbase + C::s_col(t);
+                        const uint64_t qd = ptx::sdesc_add(dq0, (uint32_t)(b * 2 + t) * C::TILE_BYTES);
+                        const uint64_t kd = ptx::sdesc_add(dk0, (uint32_t)s * C::TILE_BYTES);
+                        if (ptx::elect_one()) {
+#pragma unroll
+                            for (int kk = 0; kk < D / 16; ++kk) {
+                                const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
+                                ptx::mma_ss(d_tmem, ptx::sdesc_add(qd, off), ptx::sdesc_add(kd, off),
+                                            idesc_s, kk > 0);
+                            }
+                            ptx::mma_commit(ptx::smem_addr(&bars->s_full[t]));
+                        }
+                        __syncwarp();
+                        ++it[t];
                     }
-                    commit(&bars->k_empty[0]);
+                    if (ok) commit(&bars->k_empty[s]);
                 }
-                for (int j = 1; ok && j < nkv; ++j) ok = issue_next_s(j);
             } else {
-                for (int j = 0; ok && j < nkv; ++j) ok = issue_pvs(j);
+                for (int j = 0; ok && j < w.nkv; ++j, ++kv) {
+                    const int s = kv % C::NS;
+                    ok = warp_wait(ptx::smem_addr(&bars->v_full[s]), (uint32_t)(kv / C::NS) & 1u,
+                                   abort_flag, err, kDevTimeoutLoad);
+                    for (int t = 0; ok && t < 2; ++t) {
+                        if (j >= nt[t]) continue;
+                        if (j == 0 && uo[t] > 0) {
+                            // O_t is about to be overwritten: the previous unit's epilogue must
+                            // have read it (o_free completes once per unit in which tile t ran).
+                            ok = warp_wait(ptx::smem_addr(&bars->o_free[t]),
+                                           (uint32_t)(uo[t] - 1) & 1u, abort_flag, err,
+                                           kDevTimeoutSoftmax);
+                            if (!ok) break;
+                        }
+                        ok = warp_wait(ptx::smem_addr(&bars->p_full[t]), (uint32_t)it[t] & 1u,
+                                       abort_flag, err, kDevTimeoutSoftmax);
+                        if (!ok) break;
+                        ptx::tc_fence_after();
+                        const uint32_t d_tmem = tbase + C::o_col(t);
+                        const uint32_t p_tmem = tbase + C::p_col(t);
+                        const uint64_t vd = ptx::sdesc_add(dv0, (uint32_t)s * C::TILE_BYTES);
+                        if (ptx::elect_one()) {
+#pragma unroll
+                            for (int kk = 0; kk < C::BN / 16; ++kk)
+                                ptx::mma_ts(d_tmem, p_tmem + kk * 8, ptx::sdesc_add(vd, kk * 2048),
+                                            idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                            ptx::mma_commit(ptx::smem_addr(&bars->o_done[t]));
+                        }
+                        __syncwarp();
+                        ++it[t];
+                    }
+                    if (ok) commit(&bars->v_empty[s]);
+                }
+                for (int t = 0; t < 2; ++t) uo[t] += (nt[t] > 0);
             }
-            // Every MMA this warp issued (and every commit arrive) must be done before TMEM
-            // and the barriers are released (mma_final expects one arrive per issuing warp).
-            commit(&bars->mma_final);
-            drain_wait(ptx::smem_addr(&bars->mma_final), 0);
         }
+        // Every MMA this warp issued (and every commit arrive) must be done before TMEM and
+        // the barriers are released (mma_final expects one arrive per issuing warp).
+        commit(&bars->mma_final);
+        drain_wait(ptx::smem_addr(&bars->mma_final), 0);
     } else if (warp >= 4) {
         // ============================ softmax + epilogue ==============================
         const int t = (warp - 4) >> 2;  // Q tile of this warpgroup
         const int wq = warp & 3;        // TMEM lane quarter
         const int r = wq * 32 + lane;   // row within the tile
-        const int row0 = qb * C::ROWS + t * C::BM;
-        const int row = row0 + r;
-        const int n = ntile[t];
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const uint32_t t_s = tbase + lane_off + C::s_col(t);
         const uint32_t t_p = tbase + lane_off + C::p_col(t);
@@ -316,157 +362,186 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const uint32_t b_s_free = ptx::smem_addr(&bars->s_free[t]);
         const uint32_t b_p_full = ptx::smem_addr(&bars->p_full[t]);
         const uint32_t b_o_done = ptx::smem_addr(&bars->o_done[t]);
-
-        // Online softmax: m_ref (scaled log2 domain) moves when the row max exceeds it by more
-        // than kTau; when it moves, both l and the accumulator are rescaled by
-        // alpha = exp2(m_old - m_new). O is rescaled only when some row of the warp moved.
-        float m_ref = -INFINITY;  // reference (scaled log2 domain)
-        float l = 0.f;            // running sum of exp2(c*s - m_ref)
+        int it = 0;  // score tiles of this Q tile processed so far (all units)
+        int ul = 0;
         bool ok = true;
-        for (int j = 0; j < n; ++j) {
-            ok = __all_sync(0xffffffffu, wait_phase(b_s_full, (uint32_t)j & 1u, abort_flag, err,
-                                                    kDevTimeoutMma));
-            if (!ok) break;
-            ptx::tc_fence_after();
-            float s[C::BN];
-            {
-                uint32_t u0[32], u1[32], u2[32], u3[32];
-                ptx::tmem_ld32_nowait(t_s + 0, u0);
-                ptx::tmem_ld32_nowait(t_s + 32, u1);
-                ptx::tmem_ld32_nowait(t_s + 64, u2);
-                ptx::tmem_ld32_nowait(t_s + 96, u3);
-                ptx::tmem_wait_ld(u0);
-                ptx::tmem_wait_ld(u1);
-                ptx::tmem_wait_ld(u2);
-                ptx::tmem_wait_ld(u3);
-#pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    s[k] = __uint_as_float(u0[k]);
-                    s[32 + k] = __uint_as_float(u1[k]);
-                    s[64 + k] = __uint_as_float(u2[k]);
-                    s[96 + k] = __uint_as_float(u3[k]);
-                }
+        for (int u; ok && (u = fwd_unit_index<CAUSAL>(blockIdx.x, ul, G, num_units)) >= 0; ++ul) {
+            const FwdUnit w = fwd_unit<D, CAUSAL>(u, nqb, N);
+            const int n = (t == 0) ? w.n0 : w.n1;
+            const int b = ul % C::NQB;
+            const int row0 = w.qb * C::ROWS + t * C::BM;
+            const int row = row0 + r;
+            if (n == 0) {
+                // This Q tile is past N in this unit: release its share of the Q buffer. It
+                // first waits for this unit's Q load, so that its arrival counts towards this
+                // use of the buffer and cannot complete an earlier use's phase ahead of the
+                // other tile's epilogue (an mbarrier counts arrivals, not arrivers).
+                ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->q_full[b]),
+                                                        (uint32_t)(ul / C::NQB) & 1u, abort_flag,
+                                                        err, kDevTimeoutLoad));
+                if (!ok) break;
+                if (r == 0) ptx::mbar_arrive(ptx::smem_addr(&bars->q_free[b]));
+                continue;
             }
-            if (C::P_SEPARATE) {
-                ptx::tc_fence_before();
-                ptx::mbar_arrive(b_s_free);  // S_t columns may be overwritten now
-            }
-            const int key0 = j * C::BN;
-            const bool need_mask = (key0 + C::BN > N) || (CAUSAL && key0 + C::BN - 1 > row0);
-            if (need_mask) {
-#pragma unroll
-                for (int k = 0; k < C::BN; ++k) {
-                    const int key = key0 + k;
-                    if (key >= N || (CAUSAL && key > row)) s[k] = -INFINITY;
-                }
-            }
-            // Row max: four independent chains of three-input max.
-            float a0 = s[0], a1 = s[1], a2 = s[2], a3 = s[3];
-#pragma unroll
-            for (int k = 4; k < C::BN - 4; k += 8) {
-                a0 = ptx::fmax3(a0, s[k + 0], s[k + 1]);
-                a1 = ptx::fmax3(a1, s[k + 2], s[k + 3]);
-                a2 = ptx::fmax3(a2, s[k + 4], s[k + 5]);
-                a3 = ptx::fmax3(a3, s[k + 6], s[k + 7]);
-            }
-            a0 = ptx::fmax3(a0, s[C::BN - 4], s[C::BN - 3]);
-            a1 = ptx::fmax3(a1, s[C::BN - 2], s[C::BN - 1]);
-            const float mc = ptx::fmax3(a0, a1, fmaxf(a2, a3)) * c;
-            const bool upd = mc > m_ref + kTau;  // false when the tile is fully masked
-            float alpha = 1.f;
-            if (upd) {
-                alpha = ptx::ex2_approx(m_ref - mc);  // 0 on the first visible tile
-                m_ref = mc;
-            }
-            const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;  // safe reference
-            // p = exp2(c*s - m_ref) (packed FMA, then ex2), row sum over eight partials.
-            float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f, r4 = 0.f, r5 = 0.f, r6 = 0.f, r7 = 0.f;
-            uint32_t pk[C::BN / 2];
-#pragma unroll
-            for (int k = 0; k < C::BN; k += 8) {
-                ptx::ffma2(s[k + 0], s[k + 1], s[k + 0], s[k + 1], c, c, neg_m, neg_m);
-                ptx::ffma2(s[k + 2], s[k + 3], s[k + 2], s[k + 3], c, c, neg_m, neg_m);
-                ptx::ffma2(s[k + 4], s[k + 5], s[k + 4], s[k + 5], c, c, neg_m, neg_m);
-                ptx::ffma2(s[k + 6], s[k + 7], s[k + 6], s[k + 7], c, c, neg_m, neg_m);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) s[k + i] = ptx::ex2_approx(s[k + i]);
-                ptx::fadd2(r0, r1, r0, r1, s[k + 0], s[k + 1]);
-                ptx::fadd2(r2, r3, r2, r3, s[k + 2], s[k + 3]);
-                ptx::fadd2(r4, r5, r4, r5, s[k + 4], s[k + 5]);
-                ptx::fadd2(r6, r7, r6, r7, s[k + 6], s[k + 7]);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) pk[k / 2 + i] = ptx::pack_bf16x2(s[k + 2 * i], s[k + 2 * i + 1]);
-            }
-            l = l * alpha + (((r0 + r1) + (r2 + r3)) + ((r4 + r5) + (r6 + r7)));
-            if (j > 0) {
-                // O_t += P_t(j-1) V must be complete before P_t is overwritten (separate P
-                // columns) and before O_t is rescaled.
-                ok = __all_sync(0xffffffffu, wait_phase(b_o_done, (uint32_t)(j - 1) & 1u,
-                                                        abort_flag, err, kDevTimeoutMma));
+            // Online softmax: m_ref (scaled log2 domain) moves when the row max exceeds it by
+            // more than kTau; when it moves, both l and the accumulator are rescaled by
+            // alpha = exp2(m_old - m_new). O is rescaled only when some row of the warp moved.
+            float m_ref = -INFINITY;  // reference (scaled log2 domain)
+            float l = 0.f;            // running sum of exp2(c*s - m_ref)
+            for (int j = 0; j < n; ++j, ++it) {
+                ok = __all_sync(0xffffffffu, wait_phase(b_s_full, (uint32_t)it & 1u, abort_flag, err,
+                                                        kDevTimeoutMma));
                 if (!ok) break;
                 ptx::tc_fence_after();
-                if (__any_sync(0xffffffffu, upd)) {
+                float s[C::BN];
+                {
+                    uint32_t u0[32], u1[32], u2[32], u3[32];
+                    ptx::tmem_ld32_nowait(t_s + 0, u0);
+                    ptx::tmem_ld32_nowait(t_s + 32, u1);
+                    ptx::tmem_ld32_nowait(t_s + 64, u2);
+                    ptx::tmem_ld32_nowait(t_s + 96, u3);
+                    ptx::tmem_wait_ld(u0);
+                    ptx::tmem_wait_ld(u1);
+                    ptx::tmem_wait_ld(u2);
+                    ptx::tmem_wait_ld(u3);
 #pragma unroll
-                    for (int cc = 0; cc < D / 32; ++cc) {
-                        uint32_t o[32];
-                        ptx::tmem_ld32(t_o + cc * 32, o);
-#pragma unroll
-                        for (int i = 0; i < 32; i += 2) {
-                            float x0, x1;
-                            ptx::fmul2(x0, x1, __uint_as_float(o[i]), __uint_as_float(o[i + 1]), alpha, alpha);
-                            o[i] = __float_as_uint(x0);
-                            o[i + 1] = __float_as_uint(x1);
-                        }
-                        ptx::tmem_st32(t_o + cc * 32, o);
+                    for (int k = 0; k < 32; ++k) {
+                        s[k] = __uint_as_float(u0[k]);
+                        s[32 + k] = __uint_as_float(u1[k]);
+                        s[64 + k] = __uint_as_float(u2[k]);
+                        s[96 + k] = __uint_as_float(u3[k]);
                     }
                 }
-            }
+                if (C::P_SEPARATE) {
+                    ptx::tc_fence_before();
+                    ptx::mbar_arrive(b_s_free);  // S_t columns may be overwritten now
+                }
+                const int key0 = j * C::BN;
+                const bool need_mask = (key0 + C::BN > N) || (CAUSAL && key0 + C::BN - 1 > row0);
+                if (need_mask) {
 #pragma unroll
-            for (int g = 0; g < C::BN / 32; ++g) {
-                uint32_t chunk[16];
+                    for (int k = 0; k < C::BN; ++k) {
+                        const int key = key0 + k;
+                        if (key >= N || (CAUSAL && key > row)) s[k] = -INFINITY;
+                    }
+                }
+                // Row max: four independent chains of three-input max.
+                float a0 = s[0], a1 = s[1], a2 = s[2], a3 = s[3];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) chunk[i] = pk[16 * g + i];
-                ptx::tmem_st16(t_p + 16 * g, chunk);
+                for (int k = 4; k < C::BN - 4; k += 8) {
+                    a0 = ptx::fmax3(a0, s[k + 0], s[k + 1]);
+                    a1 = ptx::fmax3(a1, s[k + 2], s[k + 3]);
+                    a2 = ptx::fmax3(a2, s[k + 4], s[k + 5]);
+                    a3 = ptx::fmax3(a3, s[k + 6], s[k + 7]);
+                }
+                a0 = ptx::fmax3(a0, s[C::BN - 4], s[C::BN - 3]);
+                a1 = ptx::fmax3(a1, s[C::BN - 2], s[C::BN - 1]);
+                const float mc = ptx::fmax3(a0, a1, fmaxf(a2, a3)) * c;
+                const bool upd = mc > m_ref + kTau;  // false when the tile is fully masked
+                float alpha = 1.f;
+                if (upd) {
+                    alpha = ptx::ex2_approx(m_ref - mc);  // 0 on the first visible tile
+                    m_ref = mc;
+                }
+                const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;  // safe reference
+                // p = exp2(c*s - m_ref) (packed FMA, then ex2), row sum over eight partials.
+                float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f, r4 = 0.f, r5 = 0.f, r6 = 0.f, r7 = 0.f;
+                uint32_t pk[C::BN / 2];
+#pragma unroll
+                for (int k = 0; k < C::BN; k += 8) {
+                    ptx::ffma2(s[k + 0], s[k + 1], s[k + 0], s[k + 1], c, c, neg_m, neg_m);
+                    ptx::ffma2(s[k + 2], s[k + 3], s[k + 2], s[k + 3], c, c, neg_m, neg_m);
+                    ptx::ffma2(s[k + 4], s[k + 5], s[k + 4], s[k + 5], c, c, neg_m, neg_m);
+                    ptx::ffma2(s[k + 6], s[k + 7], s[k + 6], s[k + 7], c, c, neg_m, neg_m);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) s[k + i] = ptx::ex2_approx(s[k + i]);
+                    ptx::fadd2(r0, r1, r0, r1, s[k + 0], s[k + 1]);
+                    ptx::fadd2(r2, r3, r2, r3, s[k + 2], s[k + 3]);
+                    ptx::fadd2(r4, r5, r4, r5, s[k + 4], s[k + 5]);
+                    ptx::fadd2(r6, r7, r6, r7, s[k + 6], s[k + 7]);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) pk[k / 2 + i] = ptx::pack_bf16x2(s[k + 2 * i], s[k + 2 * i + 1]);
+                }
+                l = l * alpha + (((r0 + r1) + (r2 + r3)) + ((r4 + r5) + (r6 + r7)));
+                if (j > 0) {
+                    // O_t += P_t(j-1) V must be complete before P_t is overwritten (separate P
+                    // columns) and before O_t is rescaled.
+                    ok = __all_sync(0xffffffffu, wait_phase(b_o_done, (uint32_t)(it - 1) & 1u,
+                                                            abort_flag, err, kDevTimeoutMma));
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+                    if (__any_sync(0xffffffffu, upd)) {
+#pragma unroll
+                        for (int cc = 0; cc < D / 32; ++cc) {
+                            uint32_t o[32];
+                            ptx::tmem_ld32(t_o + cc * 32, o);
+#pragma unroll
+                            for (int i = 0; i < 32; i += 2) {
+                                float x0, x1;
+                                ptx::fmul2(x0, x1, __uint_as_float(o[i]), __uint_as_float(o[i + 1]), alpha, alpha);
+                                o[i] = __float_as_uint(x0);
+                                o[i + 1] = __float_as_uint(x1);
+                            }
+                            ptx::tmem_st32(t_o + cc * 32, o);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int g = 0; g < C::BN / 32; ++g) {
+                    uint32_t chunk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) chunk[i] = pk[16 * g + i];
+                    ptx::tmem_st16(t_p + 16 * g, chunk);
+                }
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(b_p_full);
             }
-            ptx::tmem_wait_st();
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(b_p_full);
-        }
-        const float m = m_ref;
-        if (ok && n > 0) {
-            ok = __all_sync(0xffffffffu, wait_phase(b_o_done, (uint32_t)(n - 1) & 1u, abort_flag,
+            if (!ok) break;
+            // ---- epilogue: O = a / l as bf16 into this tile's part of the Q buffer, TMA store ----
+            ok = __all_sync(0xffffffffu, wait_phase(b_o_done, (uint32_t)(it - 1) & 1u, abort_flag,
                                                     err, kDevTimeoutMma));
-        }
-        if (ok && n > 0) {
+            if (!ok) break;
             ptx::tc_fence_after();
-            // ---- epilogue: O = a / l as bf16 into the (now idle) Q tile buffer, TMA store ----
             const float inv_l = 1.f / l;
-            uint8_t* stage = smem + C::OFF_Q + t * C::TILE_BYTES;
+            uint32_t o_all[D];
 #pragma unroll
             for (int cc = 0; cc < D / 32; ++cc) {
                 uint32_t o[32];
                 ptx::tmem_ld32(t_o + cc * 32, o);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o_all[cc * 32 + i] = o[i];
+            }
+            // O_t is in registers: the next unit's first O_t += P V may overwrite it.
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(ptx::smem_addr(&bars->o_free[t]));
+            uint8_t* stage = smem + C::OFF_Q + (b * 2 + t) * C::TILE_BYTES;
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
                 uint8_t* chunk = stage + (cc >> 1) * C::CHUNK_BYTES;
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    uint4 w;
-                    w.x = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 0]) * inv_l, __uint_as_float(o[8 * u + 1]) * inv_l);
-                    w.y = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 2]) * inv_l, __uint_as_float(o[8 * u + 3]) * inv_l);
-                    w.z = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 4]) * inv_l, __uint_as_float(o[8 * u + 5]) * inv_l);
-                    w.w = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 6]) * inv_l, __uint_as_float(o[8 * u + 7]) * inv_l);
-                    *reinterpret_cast<uint4*>(chunk + sw128_offset((uint32_t)r, (uint32_t)((cc & 1) * 4 + u))) = w;
+                for (int uu = 0; uu < 4; ++uu) {
+                    const uint32_t* o = o_all + cc * 32 + 8 * uu;
+                    uint4 wv;
+                    wv.x = ptx::pack_bf16x2(__uint_as_float(o[0]) * inv_l, __uint_as_float(o[1]) * inv_l);
+                    wv.y = ptx::pack_bf16x2(__uint_as_float(o[2]) * inv_l, __uint_as_float(o[3]) * inv_l);
+                    wv.z = ptx::pack_bf16x2(__uint_as_float(o[4]) * inv_l, __uint_as_float(o[5]) * inv_l);
+                    wv.w = ptx::pack_bf16x2(__uint_as_float(o[6]) * inv_l, __uint_as_float(o[7]) * inv_l);
+                    *reinterpret_cast<uint4*>(chunk + sw128_offset((uint32_t)r, (uint32_t)((cc & 1) * 4 + uu))) = wv;
                 }
             }
             ptx::fence_proxy_async_smem();
             ptx::named_bar_sync(1 + t, C::BM);
+            if (row < N) lse_out[(size_t)w.bh * N + row] = (m_ref + __log2f(l)) * kLn2;
             if (r == 0) {
                 for (int ch = 0; ch < C::DCH; ++ch)
                     ptx::tma_store_3d(&tm_o, ptx::smem_addr(stage + ch * C::CHUNK_BYTES), ch * 64,
-                                      row0, bh);
+                                      row0, w.bh);
                 ptx::bulk_commit();
+                ptx::bulk_wait_read_all();
+                // the staging area (this tile's half of Q buffer b) may be reloaded now
+                ptx::mbar_arrive(ptx::smem_addr(&bars->q_free[b]));
             }
-            if (row < N) lse_out[(size_t)bh * N + row] = (m + __log2f(l)) * kLn2;
-            if (r == 0) ptx::bulk_wait_read_all();
         }
     }
 
@@ -486,10 +561,13 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
                                          (int)C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int nqb = (a.N + C::ROWS - 1) / C::ROWS;
-    const long long blocks = (long long)nqb * a.BH;
-    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    kern<<<(unsigned)blocks, C::THREADS, C::SMEM_BYTES, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o,
-                                                                  a.N, nqb, a.c, a.lse, a.err);
+    const long long units = (long long)nqb * a.BH;
+    if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    // Persistent grid: one CTA per SM (the shared-memory footprint admits no more), each
+    // walking units blockIdx.x, blockIdx.x + gridDim.x, ...
+    const int grid = (int)std::min<long long>(units, (long long)a.num_sms);
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.N, nqb,
+                                                      (int)units, a.c, a.lse, a.err);
     return cudaGetLastError();
 }
 

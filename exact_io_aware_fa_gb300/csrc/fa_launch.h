@@ -14,6 +14,7 @@ struct FwdLaunch {
     float c;                             // scale * log2(e)
     float* lse;                          // [B*H, N] fp32
     int* err;                            // device error word
+    int num_sms;                         // SMs of the device (persistent grid size)
 };
 
 // Forward: O and LSE. d in {64, 128}.
