@@ -59,10 +59,17 @@ def _lib(mutant: int = 0):
         lib.fa_oracle_backward_f64.argtypes = [P, P, P, P, P, P, P, L, L, L, L, I, D, I]
         lib.fa_oracle_backward_rows_bf16.argtypes = [P, P, P, P, P, P, P, L, L, L, L, I, D,
                                                      P, L, P, L, I]
+        lib.fa_oracle_forward_ex_f64.argtypes = [P, P, P, P, P, L, L, L, L, L, L, I, L, D, I]
+        lib.fa_oracle_forward_ex_bf16.argtypes = [P, P, P, P, P, L, L, L, L, L, L, I, L, D, I]
+        lib.fa_oracle_backward_ex_f64.argtypes = [P, P, P, P, P, P, P, L, L, L, L, L, L, I, L, D, I]
+        lib.fa_oracle_backward_ex_bf16.argtypes = [P, P, P, P, P, P, P, L, L, L, L, L, L, I, L, D,
+                                                   I]
         lib.fa_oracle_mutant_id.argtypes = []
         for fn in ("fa_oracle_forward_bf16", "fa_oracle_forward_rows_bf16",
                    "fa_oracle_forward_f64", "fa_oracle_probs_f64", "fa_oracle_backward_bf16",
                    "fa_oracle_backward_f64", "fa_oracle_backward_rows_bf16",
+                   "fa_oracle_forward_ex_f64", "fa_oracle_forward_ex_bf16",
+                   "fa_oracle_backward_ex_f64", "fa_oracle_backward_ex_bf16",
                    "fa_oracle_mutant_id"):
             getattr(lib, fn).restype = ctypes.c_int
         _LIBS[mutant] = lib
@@ -173,6 +180,61 @@ class Oracle:
                                                      rq.shape[0], _ptr(rk), rk.shape[0],
                                                      self.threads), "backward_rows")
         return dq, dk, dv
+
+
+class NoVisibleKey(ValueError):
+    """A query row sees no key (the attention of that row is undefined)."""
+
+
+def _check_ex(rc: int, what: str) -> None:
+    if rc == -3:
+        raise NoVisibleKey(f"oracle {what}: a query row has no visible key")
+    _check(rc, what)
+
+
+def _ex_shapes(q, k):
+    if q.ndim != 4 or k.ndim != 4 or q.shape[0] != k.shape[0] or q.shape[3] != k.shape[3]:
+        raise ValueError("expected q [B,Hq,Tq,d] and k/v [B,Hkv,Tk,d]")
+    B, Hq, Tq, d = q.shape
+    _, Hkv, Tk, _ = k.shape
+    return B, Hq, Hkv, Tq, Tk, d
+
+
+def _ex_methods():
+    def forward_ex(self, q, k, v, causal: bool, scale: float, window: int = -1):
+        """Grouped KV heads, query rows at positions (Tk - Tq) + i, optional left window."""
+        B, Hq, Hkv, Tq, Tk, d = _ex_shapes(q, k)
+        f64 = q.dtype != np.uint16
+        conv = (lambda x: np.ascontiguousarray(x, dtype=np.float64)) if f64 else \
+               (lambda x: np.ascontiguousarray(x, dtype=np.uint16))
+        q, k, v = conv(q), conv(k), conv(v)
+        o = np.empty((B, Hq, Tq, d), dtype=np.float64)
+        lse = np.empty((B, Hq, Tq), dtype=np.float64)
+        fn = self.lib.fa_oracle_forward_ex_f64 if f64 else self.lib.fa_oracle_forward_ex_bf16
+        _check_ex(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Tq, Tk, d,
+                     int(causal), int(window), float(scale), self.threads), "forward_ex")
+        return o, lse
+
+    def backward_ex(self, q, k, v, dout, causal: bool, scale: float, window: int = -1):
+        B, Hq, Hkv, Tq, Tk, d = _ex_shapes(q, k)
+        f64 = q.dtype != np.uint16
+        conv = (lambda x: np.ascontiguousarray(x, dtype=np.float64)) if f64 else \
+               (lambda x: np.ascontiguousarray(x, dtype=np.uint16))
+        q, k, v, dout = conv(q), conv(k), conv(v), conv(dout)
+        dq = np.empty((B, Hq, Tq, d), dtype=np.float64)
+        dk = np.empty((B, Hkv, Tk, d), dtype=np.float64)
+        dv = np.empty((B, Hkv, Tk, d), dtype=np.float64)
+        fn = self.lib.fa_oracle_backward_ex_f64 if f64 else self.lib.fa_oracle_backward_ex_bf16
+        _check_ex(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), B, Hq,
+                     Hkv, Tq, Tk, d, int(causal), int(window), float(scale), self.threads),
+                  "backward_ex")
+        return dq, dk, dv
+
+    Oracle.forward_ex = forward_ex
+    Oracle.backward_ex = backward_ex
+
+
+_ex_methods()
 
 
 def oracle(threads: int | None = None) -> Oracle:

@@ -199,6 +199,8 @@ struct job {
     double *o, *lse, *dq, *dk, *dv;
     const long *rows_q, *rows_k;
     long nrows_q, nrows_k;
+    /* extension: grouped KV heads, query offset, sliding window */
+    long Hq, Hkv, Tq, Tk, window;
     size_t scratch_doubles;
     long next;
     pthread_mutex_t mu;
@@ -507,6 +509,213 @@ int fa_oracle_backward_rows_bf16(const uint16_t* q, const uint16_t* k, const uin
     jb.scratch_doubles = 5 * (size_t)N + 4 * (size_t)N * (size_t)d;
     if (jb.BH == 0 || N == 0) return 0;
     return run_job(&jb, nthreads);
+}
+
+/* ---- extension: grouped KV heads, query offset, sliding window ------------------------
+ *
+ * "15. FlashAttention" (inference.shantanugoel.com), section "The algorithm in plain
+ * PyTorch": query head h reads KV head h / (Hq / Hkv) (grouped-query attention); query row i
+ * sits at position (Tk - Tq) + i, so the last query lines up with the last key; key j is
+ * visible iff j <= position (causal). Section "Stretch exercises", item 3 (sliding window):
+ * tiles wholly before position - window are skipped, i.e. with a window key j is visible only
+ * if j >= position - window. A row with no visible key is an error (the page raises).
+ * Same definitions as above otherwise: materialised score row, safe softmax, O = P V,
+ * LSE = m + ln l; dK, dV of a KV head add up the contributions of all its query heads.
+ */
+
+static int visible_ex(long pos, long j, int causal, long window) {
+    if (causal && j > pos) return 0;
+    if (window >= 0 && j < pos - window) return 0;
+    return 1;
+}
+
+/* prob[j] for j < Tk; returns 0 if the row has no visible key. */
+static int prob_row_ex(const double* qrow, const double* k, long Tk, long d, long pos, int causal,
+                       long window, double scale, double* prob, double* m_out, double* l_out) {
+    double m = -INFINITY;
+    long nvis = 0;
+    for (long j = 0; j < Tk; ++j) {
+        if (visible_ex(pos, j, causal, window)) {
+            prob[j] = scale * dot(qrow, k + j * d, d);
+            if (prob[j] > m) m = prob[j];
+            ++nvis;
+        }
+    }
+    if (nvis == 0) return 0;
+    double l = 0.0;
+    for (long j = 0; j < Tk; ++j)
+        if (visible_ex(pos, j, causal, window)) l += exp(prob[j] - m);
+    for (long j = 0; j < Tk; ++j)
+        prob[j] = visible_ex(pos, j, causal, window) ? exp(prob[j] - m) / l : 0.0;
+    *m_out = m;
+    *l_out = l;
+    return 1;
+}
+
+static const double* slice_input(const job* jb, const void* base, long idx, long rows, double* buf) {
+    long n = rows * jb->d;
+    if (jb->in_bf16) {
+        widen((const uint16_t*)base + idx * n, buf, n);
+        return buf;
+    }
+    return (const double*)base + idx * n;
+}
+
+/* One (batch, KV head) slice: every query head of its group. */
+static void fwd_ex_slice(const job* jb, long bkv, double* scratch) {
+    long d = jb->d, Tq = jb->Tq, Tk = jb->Tk, group = jb->Hq / jb->Hkv;
+    long b = bkv / jb->Hkv, hk = bkv % jb->Hkv;
+    double* prob = scratch;
+    double* bufk = prob + Tk;
+    double* bufv = bufk + Tk * d;
+    double* bufq = bufv + Tk * d;
+    const double* k = slice_input(jb, jb->k, bkv, Tk, bufk);
+    const double* v = slice_input(jb, jb->v, bkv, Tk, bufv);
+    for (long g = 0; g < group; ++g) {
+        long bhq = b * jb->Hq + hk * group + g;
+        const double* q = slice_input(jb, jb->q, bhq, Tq, bufq);
+        for (long i = 0; i < Tq; ++i) {
+            double m, l;
+            long pos = (Tk - Tq) + i;
+            if (!prob_row_ex(q + i * d, k, Tk, d, pos, jb->causal, jb->window, jb->scale, prob, &m, &l)) {
+                ((job*)jb)->failed = 1;
+                return;
+            }
+            double* orow = jb->o + (bhq * Tq + i) * d;
+            for (long e = 0; e < d; ++e) {
+                double acc = 0.0;
+                for (long j = 0; j < Tk; ++j) acc += prob[j] * v[j * d + e];
+                orow[e] = acc;
+            }
+            jb->lse[bhq * Tq + i] = m + log(l);
+        }
+    }
+}
+
+static void bwd_ex_slice(const job* jb, long bkv, double* scratch) {
+    long d = jb->d, Tq = jb->Tq, Tk = jb->Tk, group = jb->Hq / jb->Hkv;
+    long b = bkv / jb->Hkv, hk = bkv % jb->Hkv;
+    double* P = scratch;            /* Tq x Tk */
+    double* dS = P + Tq * Tk;       /* Tq x Tk (dP, then dS in place) */
+    double* Dv = dS + Tq * Tk;
+    double* bufk = Dv + Tq;
+    double* bufv = bufk + Tk * d;
+    double* bufq = bufv + Tk * d;
+    double* bufo = bufq + Tq * d;
+    const double* k = slice_input(jb, jb->k, bkv, Tk, bufk);
+    const double* v = slice_input(jb, jb->v, bkv, Tk, bufv);
+    double* dk = jb->dk + bkv * Tk * d;
+    double* dv = jb->dv + bkv * Tk * d;
+    for (long x = 0; x < Tk * d; ++x) dk[x] = dv[x] = 0.0;
+    for (long g = 0; g < group; ++g) {
+        long bhq = b * jb->Hq + hk * group + g;
+        const double* q = slice_input(jb, jb->q, bhq, Tq, bufq);
+        const double* dout = slice_input(jb, jb->dout, bhq, Tq, bufo);
+        for (long i = 0; i < Tq; ++i) {
+            double m, l;
+            if (!prob_row_ex(q + i * d, k, Tk, d, (Tk - Tq) + i, jb->causal, jb->window, jb->scale,
+                             P + i * Tk, &m, &l)) {
+                ((job*)jb)->failed = 1;
+                return;
+            }
+        }
+        for (long i = 0; i < Tq; ++i)
+            for (long j = 0; j < Tk; ++j) dS[i * Tk + j] = dot(dout + i * d, v + j * d, d);
+        for (long i = 0; i < Tq; ++i) {
+            double s = 0.0;
+            for (long j = 0; j < Tk; ++j) s += P[i * Tk + j] * dS[i * Tk + j];
+            Dv[i] = s;
+        }
+        for (long i = 0; i < Tq; ++i)
+            for (long j = 0; j < Tk; ++j) dS[i * Tk + j] = P[i * Tk + j] * (dS[i * Tk + j] - Dv[i]);
+        for (long j = 0; j < Tk; ++j)
+            for (long e = 0; e < d; ++e) {
+                double a = 0.0, c = 0.0;
+                for (long i = 0; i < Tq; ++i) {
+                    a += P[i * Tk + j] * dout[i * d + e];
+                    c += dS[i * Tk + j] * q[i * d + e];
+                }
+                dv[j * d + e] += a;
+                dk[j * d + e] += jb->scale * c;
+            }
+        double* dq = jb->dq + bhq * Tq * d;
+        for (long i = 0; i < Tq; ++i)
+            for (long e = 0; e < d; ++e) {
+                double a = 0.0;
+                for (long j = 0; j < Tk; ++j) a += dS[i * Tk + j] * k[j * d + e];
+                dq[i * d + e] = jb->scale * a;
+            }
+    }
+}
+
+static int ex_common(int in_bf16, int backward, const void* q, const void* k, const void* v,
+                     const void* dout, double* o, double* lse, double* dq, double* dk, double* dv,
+                     long B, long Hq, long Hkv, long Tq, long Tk, long d, int causal, long window,
+                     double scale, int nthreads) {
+    if (B < 0 || Hq < 0 || Hkv < 1 || Tq < 0 || Tk < 0 || d < 1) return -2;
+    if (Hq % Hkv != 0) return -2;
+    if (window >= 0 && !causal) return -2;
+    job jb;
+    memset(&jb, 0, sizeof jb);
+    jb.fn = backward ? bwd_ex_slice : fwd_ex_slice;
+    jb.BH = B * Hkv;
+    jb.N = Tk;
+    jb.d = d;
+    jb.causal = causal;
+    jb.scale = scale;
+    jb.in_bf16 = in_bf16;
+    jb.q = q;
+    jb.k = k;
+    jb.v = v;
+    jb.dout = dout;
+    jb.o = o;
+    jb.lse = lse;
+    jb.dq = dq;
+    jb.dk = dk;
+    jb.dv = dv;
+    jb.Hq = Hq;
+    jb.Hkv = Hkv;
+    jb.Tq = Tq;
+    jb.Tk = Tk;
+    jb.window = window;
+    jb.scratch_doubles = backward ? 2 * (size_t)Tq * (size_t)Tk + (size_t)Tq + 2 * (size_t)Tk * (size_t)d + 2 * (size_t)Tq * (size_t)d
+                                  : (size_t)Tk + 2 * (size_t)Tk * (size_t)d + (size_t)Tq * (size_t)d;
+    if (jb.BH == 0 || Tq == 0 || Hq == 0) return 0;
+    if (Tk == 0) return -3;
+    int rc = run_job(&jb, nthreads);
+    return rc == 0 ? 0 : -3;
+}
+
+/* O [B,Hq,Tq,d], LSE [B,Hq,Tq] from q [B,Hq,Tq,d], k/v [B,Hkv,Tk,d] (float64 inputs).
+ * window < 0: none; window >= 0 needs causal. Returns -3 if a row has no visible key. */
+int fa_oracle_forward_ex_f64(const double* q, const double* k, const double* v, double* o,
+                             double* lse, long B, long Hq, long Hkv, long Tq, long Tk, long d,
+                             int causal, long window, double scale, int nthreads) {
+    return ex_common(0, 0, q, k, v, NULL, o, lse, NULL, NULL, NULL, B, Hq, Hkv, Tq, Tk, d, causal,
+                     window, scale, nthreads);
+}
+
+int fa_oracle_forward_ex_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v, double* o,
+                              double* lse, long B, long Hq, long Hkv, long Tq, long Tk, long d,
+                              int causal, long window, double scale, int nthreads) {
+    return ex_common(1, 0, q, k, v, NULL, o, lse, NULL, NULL, NULL, B, Hq, Hkv, Tq, Tk, d, causal,
+                     window, scale, nthreads);
+}
+
+/* dQ [B,Hq,Tq,d], dK/dV [B,Hkv,Tk,d] of L = sum(O (.) dO). */
+int fa_oracle_backward_ex_f64(const double* q, const double* k, const double* v, const double* dout,
+                              double* dq, double* dk, double* dv, long B, long Hq, long Hkv, long Tq,
+                              long Tk, long d, int causal, long window, double scale, int nthreads) {
+    return ex_common(0, 1, q, k, v, dout, NULL, NULL, dq, dk, dv, B, Hq, Hkv, Tq, Tk, d, causal,
+                     window, scale, nthreads);
+}
+
+int fa_oracle_backward_ex_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                               const uint16_t* dout, double* dq, double* dk, double* dv, long B,
+                               long Hq, long Hkv, long Tq, long Tk, long d, int causal, long window,
+                               double scale, int nthreads) {
+    return ex_common(1, 1, q, k, v, dout, NULL, NULL, dq, dk, dv, B, Hq, Hkv, Tq, Tk, d, causal,
+                     window, scale, nthreads);
 }
 
 int fa_oracle_mutant_id(void) { return ORACLE_MUTANT; }

@@ -363,6 +363,140 @@ def check_entry_points_agree(orc):
         assert np.max(np.abs(sv - g[2][:, :, rows[::-1]])) <= 1e-12
 
 
+# ---------------------------------------------------------------------------------------
+# Extension: grouped KV heads, query offset (bottom-right alignment), sliding window
+
+def check_ex_reduces_to_mha(orc):
+    """Hq = Hkv, Tq = Tk, no window: the extended entry points equal the plain ones."""
+    r = _rng(30)
+    for causal in (False, True):
+        q, k, v, dout = (r.standard_normal((2, 3, 10, 4)) for _ in range(4))
+        o, lse = orc.forward_f64(q, k, v, causal=causal, scale=0.6)
+        oe, lsee = orc.forward_ex(q, k, v, causal, 0.6)
+        assert np.max(np.abs(oe - o)) <= 1e-14 and np.max(np.abs(lsee - lse)) <= 1e-14
+        g = orc.backward_f64(q, k, v, dout, causal=causal, scale=0.6)
+        ge = orc.backward_ex(q, k, v, dout, causal, 0.6)
+        for a, b in zip(ge, g):
+            assert np.max(np.abs(a - b)) <= 1e-13
+
+
+def check_ex_gqa_equals_repeated_kv(orc):
+    """Query head h reads KV head h // group: same as multi-head attention with every KV head
+    repeated `group` times; its dK/dV are the sums over the group."""
+    r = _rng(31)
+    B, Hkv, group, T, d = 2, 2, 3, 9, 4
+    q = r.standard_normal((B, Hkv * group, T, d))
+    k = r.standard_normal((B, Hkv, T, d))
+    v = r.standard_normal((B, Hkv, T, d))
+    dout = r.standard_normal((B, Hkv * group, T, d))
+    kr, vr = np.repeat(k, group, axis=1), np.repeat(v, group, axis=1)
+    for causal in (False, True):
+        o, lse = orc.forward_f64(q, kr, vr, causal=causal, scale=0.7)
+        oe, lsee = orc.forward_ex(q, k, v, causal, 0.7)
+        assert np.max(np.abs(oe - o)) <= 1e-13 and np.max(np.abs(lsee - lse)) <= 1e-13
+        dq, dk, dv = orc.backward_f64(q, kr, vr, dout, causal=causal, scale=0.7)
+        dqe, dke, dve = orc.backward_ex(q, k, v, dout, causal, 0.7)
+        assert np.max(np.abs(dqe - dq)) <= 1e-12
+        assert np.max(np.abs(dke - dk.reshape(B, Hkv, group, T, d).sum(2))) <= 1e-12
+        assert np.max(np.abs(dve - dv.reshape(B, Hkv, group, T, d).sum(2))) <= 1e-12
+
+
+def check_ex_query_offset_bottom_right(orc):
+    """Tq < Tk, causal: query row i sits at key position Tk - Tq + i, so the rows equal the
+    last Tq rows of a full causal attention whose last queries are these."""
+    r = _rng(32)
+    Tq, Tk, d = 5, 12, 3
+    q = r.standard_normal((1, 2, Tq, d))
+    k = r.standard_normal((1, 2, Tk, d))
+    v = r.standard_normal((1, 2, Tk, d))
+    qf = r.standard_normal((1, 2, Tk, d))
+    qf[:, :, Tk - Tq:] = q
+    of, lf = orc.forward_f64(qf, k, v, causal=True, scale=0.9)
+    oe, le = orc.forward_ex(q, k, v, True, 0.9)
+    assert np.max(np.abs(oe - of[:, :, Tk - Tq:])) <= 1e-14
+    assert np.max(np.abs(le - lf[:, :, Tk - Tq:])) <= 1e-14
+    # Non-causal rows do not depend on the offset: every key is visible.
+    o2, l2 = orc.forward_ex(q, k, v, False, 0.9)
+    s = 0.9 * np.einsum("bhie,bhje->bhij", q, k)
+    from scipy.special import logsumexp, softmax
+    assert np.max(np.abs(l2 - logsumexp(s, -1))) <= 1e-12
+    assert np.max(np.abs(o2 - softmax(s, -1) @ v)) <= 1e-12
+    # A query before the first key (Tq > Tk, causal) has nothing to attend to.
+    try:
+        orc.forward_ex(r.standard_normal((1, 1, 6, d)), k[:, :1, :4], v[:, :1, :4], True, 0.9)
+    except ValueError:
+        pass
+    else:
+        raise AssertionError("a row with no visible key was accepted")
+
+
+def check_ex_sliding_window(orc):
+    """Window w: key j visible iff pos - w <= j <= pos ("15. FlashAttention", stretch item 3:
+    tiles wholly before q_pos - window are skipped)."""
+    from scipy.special import logsumexp, softmax
+    r = _rng(33)
+    Tq, Tk, d = 7, 10, 3
+    q = r.standard_normal((1, 2, Tq, d))
+    k = r.standard_normal((1, 2, Tk, d))
+    v = r.standard_normal((1, 2, Tk, d))
+    # window 0: each row sees only the key at its own position
+    o, lse = orc.forward_ex(q, k, v, True, 0.8, window=0)
+    pos = np.arange(Tq) + (Tk - Tq)
+    assert np.max(np.abs(o - v[:, :, pos])) <= 1e-15
+    s_own = 0.8 * np.einsum("bhie,bhie->bhi", q, k[:, :, pos])
+    assert np.max(np.abs(lse - s_own)) <= 1e-14
+    # window >= Tk: plain causal
+    o1, l1 = orc.forward_ex(q, k, v, True, 0.8, window=Tk)
+    o2, l2 = orc.forward_ex(q, k, v, True, 0.8)
+    assert np.max(np.abs(o1 - o2)) <= 1e-15 and np.max(np.abs(l1 - l2)) <= 1e-15
+    # window 3 against scipy on the explicit mask
+    w = 3
+    s = 0.8 * np.einsum("bhie,bhje->bhij", q, k)
+    j = np.arange(Tk)[None, :]
+    vis = (j <= pos[:, None]) & (j >= pos[:, None] - w)
+    s = np.where(vis, s, -np.inf)
+    o3, l3 = orc.forward_ex(q, k, v, True, 0.8, window=w)
+    assert np.max(np.abs(l3 - logsumexp(s, -1))) <= 1e-12
+    assert np.max(np.abs(o3 - softmax(s, -1) @ v)) <= 1e-12
+    # a window without the causal mask is not defined here
+    try:
+        orc.forward_ex(q, k, v, False, 0.8, window=2)
+    except (ValueError, RuntimeError):
+        pass
+    else:
+        raise AssertionError("window without causal accepted")
+
+
+def check_ex_backward_finite_differences(orc):
+    """Gradients of the extended forward (GQA + offset + window) by central differences."""
+    r = _rng(34)
+    h = 1e-5
+    B, Hkv, group, Tq, Tk, d = 1, 1, 2, 4, 7, 2
+    q = r.standard_normal((B, Hkv * group, Tq, d))
+    k = r.standard_normal((B, Hkv, Tk, d))
+    v = r.standard_normal((B, Hkv, Tk, d))
+    dout = r.standard_normal((B, Hkv * group, Tq, d))
+    for window in (-1, 2):
+        dq, dk, dv = orc.backward_ex(q, k, v, dout, True, 1.3, window=window)
+
+        def loss(qq, kk, vv):
+            o, _ = orc.forward_ex(qq, kk, vv, True, 1.3, window=window)
+            return float(np.sum(o * dout))
+
+        for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+            num = np.zeros_like(x)
+            for idx in np.ndindex(x.shape):
+                xp, xm = x.copy(), x.copy()
+                xp[idx] += h
+                xm[idx] -= h
+                a = {"q": q, "k": k, "v": v}
+                b = dict(a)
+                a[name], b[name] = xp, xm
+                num[idx] = (loss(a["q"], a["k"], a["v"]) - loss(b["q"], b["k"], b["v"])) / (2 * h)
+            err = np.max(np.abs(num - g)) / max(1.0, np.max(np.abs(g)))
+            assert err <= 1e-6, (name, window, err)
+
+
 ALL_CHECKS = [
     check_worked_example_oracle,
     check_worked_example_two_tiles,
@@ -380,4 +514,9 @@ ALL_CHECKS = [
     check_backward_identities,
     check_backward_linear_in_dout,
     check_entry_points_agree,
+    check_ex_reduces_to_mha,
+    check_ex_gqa_equals_repeated_kv,
+    check_ex_query_offset_bottom_right,
+    check_ex_sliding_window,
+    check_ex_backward_finite_differences,
 ]
