@@ -23,8 +23,9 @@ FA_ERR_CUDA = 4
 FA_ERR_TIMEOUT = 5
 
 # Every symbol include/fa.h declares.
-EXPORTS = ("fa_forward", "fa_backward_workspace_bytes", "fa_backward", "fa_backward_noalloc",
-           "fa_status_string", "fa_last_cuda_error", "fa_device_error")
+EXPORTS = ("fa_forward", "fa_forward_ex", "fa_backward_workspace_bytes", "fa_backward",
+           "fa_backward_ex", "fa_backward_noalloc", "fa_status_string", "fa_last_cuda_error",
+           "fa_device_error")
 
 # Size of the library's own backward workspace (FA_NOALLOC_SCRATCH_BYTES in include/fa.h).
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
@@ -61,10 +62,14 @@ def library(path: str | None = None):
         P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         lib.fa_forward.argtypes = [P, P, P, P, P, I, I, I, I, I, F, P]
         lib.fa_forward.restype = I
+        lib.fa_forward_ex.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, F, P]
+        lib.fa_forward_ex.restype = I
         lib.fa_backward_workspace_bytes.argtypes = [I, I, I, I]
         lib.fa_backward_workspace_bytes.restype = Z
         lib.fa_backward.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, P, P]
         lib.fa_backward.restype = I
+        lib.fa_backward_ex.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, P, P]
+        lib.fa_backward_ex.restype = I
         lib.fa_backward_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, P]
         lib.fa_backward_noalloc.restype = I
         lib.fa_status_string.argtypes = [I]
@@ -92,6 +97,19 @@ def _check(status: int, what: str) -> None:
 def forward_raw(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int, d: int,
                 causal: int, scale: float, stream: int) -> int:
     return library().fa_forward(q, k, v, o, lse, B, H, N, d, causal, scale, stream)
+
+
+def forward_ex_raw(q: int, k: int, v: int, o: int, lse: int, B: int, Hq: int, Hkv: int, Tq: int,
+                   Tk: int, d: int, causal: int, window: int, scale: float, stream: int) -> int:
+    """fa_forward_ex: grouped KV heads, query offset Tk - Tq, optional sliding window."""
+    return library().fa_forward_ex(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, causal, window, scale,
+                                   stream)
+
+
+def backward_ex_raw(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Tq, Tk, d, causal, window,
+                    scale, workspace, stream) -> int:
+    return library().fa_backward_ex(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Tq, Tk, d,
+                                    causal, window, scale, workspace, stream)
 
 
 def backward_raw(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, causal, scale, workspace,
@@ -138,43 +156,58 @@ def _check_tensor(name, t, shape=None):
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
 
 
-def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
-            stream=None):
-    """O, LSE = attention(q, k, v). Tensors are bf16 [B, H, N, d] on one CUDA device."""
+def _shapes(q, k, v):
     import torch
     for name, t in (("q", q), ("k", k), ("v", v)):
-        _check_tensor(name, t, q.shape if name != "q" else None)
+        _check_tensor(name, t)
         if t.dtype != torch.bfloat16:
             raise ValueError(f"{name} must be bfloat16")
-    if q.dim() != 4:
-        raise ValueError("q must be [B, H, N, d]")
-    B, H, N, d = q.shape
+        if t.dim() != 4:
+            raise ValueError(f"{name} must be 4-D")
+    B, Hq, Tq, d = q.shape
+    _, Hkv, Tk, _ = k.shape
+    if tuple(k.shape) != (B, Hkv, Tk, d) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError(f"k, v must both be [B, Hkv, Tk, d] = {(B, Hkv, Tk, d)}")
+    return B, Hq, Hkv, Tq, Tk, d
+
+
+def forward(q, k, v, causal: bool = False, scale: float | None = None, window: int = -1,
+            out=None, lse=None, stream=None):
+    """O, LSE = attention(q, k, v).
+
+    q is bf16 [B, Hq, Tq, d]; k and v are bf16 [B, Hkv, Tk, d] with Hq % Hkv == 0. Query row i
+    sits at key position Tk - Tq + i; ``window`` >= 0 (causal only) keeps keys no more than
+    ``window`` positions before it. Multi-head attention is Hkv = Hq, Tq = Tk.
+    """
+    import torch
+    B, Hq, Hkv, Tq, Tk, d = _shapes(q, k, v)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
-        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+        lse = torch.empty((B, Hq, Tq), dtype=torch.float32, device=q.device)
     _check_tensor("out", out, q.shape)
-    _check_tensor("lse", lse, (B, H, N))
+    _check_tensor("lse", lse, (B, Hq, Tq))
     s = stream if stream is not None else torch.cuda.current_stream(q.device).cuda_stream
     with torch.cuda.device(q.device):
-        st = forward_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                         B, H, N, d, int(bool(causal)), float(scale), s)
-    _check(st, "fa_forward")
+        st = forward_ex_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                            lse.data_ptr(), B, Hq, Hkv, Tq, Tk, d, int(bool(causal)), int(window),
+                            float(scale), s)
+    _check(st, "fa_forward_ex")
     return out, lse
 
 
-def backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None, dq=None,
-             dk=None, dv=None, workspace=None, stream=None):
-    """dQ, dK, dV of sum(O * dO) given the forward's O and LSE."""
+def backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None,
+             window: int = -1, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """dQ, dK, dV of sum(O * dO) given the forward's O and LSE (shapes as ``forward``)."""
     import torch
-    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+    B, Hq, Hkv, Tq, Tk, d = _shapes(q, k, v)
+    for name, t in (("o", o), ("dout", dout)):
         _check_tensor(name, t, q.shape)
         if t.dtype != torch.bfloat16:
             raise ValueError(f"{name} must be bfloat16")
-    B, H, N, d = q.shape
-    _check_tensor("lse", lse, (B, H, N))
+    _check_tensor("lse", lse, (B, Hq, Tq))
     if lse.dtype != torch.float32:
         raise ValueError("lse must be float32")
     if scale is None:
@@ -182,18 +215,20 @@ def backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = 
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
-        _check_tensor(name, t, q.shape)
+    _check_tensor("dq", dq, q.shape)
+    _check_tensor("dk", dk, k.shape)
+    _check_tensor("dv", dv, v.shape)
     ws_ptr = 0
     if workspace is not None:
-        need = backward_workspace_bytes(B, H, N, d)
+        need = backward_workspace_bytes(B, Hq, Tq, d)
         if workspace.numel() * workspace.element_size() < need:
             raise ValueError(f"workspace needs {need} bytes")
         ws_ptr = workspace.data_ptr()
     s = stream if stream is not None else torch.cuda.current_stream(q.device).cuda_stream
     with torch.cuda.device(q.device):
-        st = backward_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                          dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d,
-                          int(bool(causal)), float(scale), ws_ptr, s)
-    _check(st, "fa_backward")
+        st = backward_ex_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                             lse.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                             dv.data_ptr(), B, Hq, Hkv, Tq, Tk, d, int(bool(causal)), int(window),
+                             float(scale), ws_ptr, s)
+    _check(st, "fa_backward_ex")
     return dq, dk, dv

@@ -112,20 +112,52 @@ fa_status make_map(CUtensorMap* m, const void* base, int BH, int N, int d, int b
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Checks shared by forward and backward. Sets *empty when there is no work.
-fa_status check_common(int B, int H, int N, int d, int causal, float scale, bool* empty) {
-    if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID_ARG;
+// Problem shape after the host checks.
+struct Shape {
+    int B, Hq, Hkv, Tq, Tk, d, causal, window;
+    int BHq, BHkv;
+};
+
+// Checks shared by every entry point. Sets *empty when there is nothing to compute (no query
+// rows; the backward still owes zero dK/dV when there are keys).
+fa_status check_shape(int B, int Hq, int Hkv, int Tq, int Tk, int d, int causal, int window,
+                      float scale, Shape* sh, bool* empty) {
+    if (B < 0 || Hq < 0 || Hkv < 0 || Tq < 0 || Tk < 0) return FA_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    if (window < -1) return FA_ERR_INVALID_ARG;
+    if (window >= 0 && !causal) return FA_ERR_INVALID_ARG;  // the window hangs off the diagonal
     if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
     if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-    const long long bh = (long long)B * (long long)H;
-    *empty = (bh == 0 || N == 0);
-    if (*empty) return FA_OK;
-    if (bh > INT_MAX) return FA_ERR_UNSUPPORTED;
-    if ((long long)N + 256 > INT_MAX) return FA_ERR_UNSUPPORTED;
-    const long long nqb = ((long long)N + 255) / 256;
-    if (nqb * bh > INT_MAX) return FA_ERR_UNSUPPORTED;
+    if ((Hq == 0) != (Hkv == 0)) return FA_ERR_INVALID_ARG;
+    if (Hkv > 0 && Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+    const long long bhq = (long long)B * (long long)Hq;
+    const long long bhkv = (long long)B * (long long)Hkv;
+    *empty = (bhq == 0 || Tq == 0);
+    if (bhq > 0 && Tq > 0) {
+        // every query row must see at least one key
+        if (Tk == 0) return FA_ERR_INVALID_ARG;
+        if (causal && Tq > Tk) return FA_ERR_INVALID_ARG;
+    }
+    if (bhq > INT_MAX || bhkv > INT_MAX) return FA_ERR_UNSUPPORTED;
+    if ((long long)Tq + 256 > INT_MAX || (long long)Tk + 256 > INT_MAX) return FA_ERR_UNSUPPORTED;
+    if (((long long)Tq + 255) / 256 * bhq > INT_MAX) return FA_ERR_UNSUPPORTED;
+    if (((long long)Tk + 127) / 128 * bhkv > INT_MAX) return FA_ERR_UNSUPPORTED;
+    sh->B = B;
+    sh->Hq = Hq;
+    sh->Hkv = Hkv;
+    sh->Tq = Tq;
+    sh->Tk = Tk;
+    sh->d = d;
+    sh->causal = causal;
+    sh->window = window;
+    sh->BHq = (int)bhq;
+    sh->BHkv = (int)bhkv;
     return FA_OK;
+}
+
+size_t workspace_bytes(long long bhq, long long tq, int d) {
+    const size_t npad = ((size_t)tq + 127) / 128 * 128;
+    return 2 * (size_t)bhq * npad * sizeof(float) + (size_t)bhq * npad * (size_t)d * sizeof(float);
 }
 
 constexpr float kLog2e = 1.4426950408889634074f;
@@ -172,25 +204,30 @@ const char* fa_status_string(fa_status s) {
 
 int fa_last_cuda_error(void) { return t_last_cuda_error; }
 
-fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                     int H, int N, int d, int causal, float scale, struct CUstream_st* stream) {
+fa_status fa_forward_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                        int Hq, int Hkv, int Tq, int Tk, int d, int causal, int window,
+                        float scale, struct CUstream_st* stream) {
+    Shape sh;
     bool empty = false;
-    fa_status st = check_common(B, H, N, d, causal, scale, &empty);
+    fa_status st = check_shape(B, Hq, Hkv, Tq, Tk, d, causal, window, scale, &sh, &empty);
     if (st != FA_OK || empty) return st;
     if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
         return FA_ERR_ALIGNMENT;
-    const int BH = B * H;
     fa::FwdLaunch a;
     std::memset(&a, 0, sizeof a);
-    if ((st = make_map(&a.tm_q, q, BH, N, d, 128)) != FA_OK) return st;
-    if ((st = make_map(&a.tm_k, k, BH, N, d, 128)) != FA_OK) return st;
-    if ((st = make_map(&a.tm_v, v, BH, N, d, 128)) != FA_OK) return st;
-    if ((st = make_map(&a.tm_o, o, BH, N, d, 128)) != FA_OK) return st;
+    if ((st = make_map(&a.tm_q, q, sh.BHq, Tq, d, 128)) != FA_OK) return st;
+    if ((st = make_map(&a.tm_o, o, sh.BHq, Tq, d, 128)) != FA_OK) return st;
+    if ((st = make_map(&a.tm_k, k, sh.BHkv, Tk, d, 128)) != FA_OK) return st;
+    if ((st = make_map(&a.tm_v, v, sh.BHkv, Tk, d, 128)) != FA_OK) return st;
     if ((st = get_err_ptr(&a.err)) != FA_OK) return st;
     if ((st = get_num_sms(&a.num_sms)) != FA_OK) return st;
-    a.N = N;
-    a.BH = BH;
+    a.Tq = Tq;
+    a.Tk = Tk;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.BHq = sh.BHq;
+    a.window = window;
     a.c = scale * kLog2e;
     a.lse = lse;
     cudaError_t e = fa::launch_forward(a, d, causal != 0, reinterpret_cast<cudaStream_t>(stream));
@@ -198,40 +235,53 @@ fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float
     return FA_OK;
 }
 
-size_t fa_backward_workspace_bytes(int B, int H, int N, int d) {
-    if (B <= 0 || H <= 0 || N <= 0 || (d != 64 && d != 128)) return 0;
-    const size_t bh = (size_t)B * (size_t)H;
-    const size_t npad = ((size_t)N + 127) / 128 * 128;
-    return 2 * bh * npad * sizeof(float) + bh * npad * (size_t)d * sizeof(float);
+fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int H, int N, int d, int causal, float scale, struct CUstream_st* stream) {
+    return fa_forward_ex(q, k, v, o, lse, B, H, H, N, N, d, causal, -1, scale, stream);
 }
 
-fa_status fa_backward(const void* q, const void* k, const void* v, const void* o,
-                      const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
-                      int H, int N, int d, int causal, float scale, void* workspace,
-                      struct CUstream_st* stream) {
+size_t fa_backward_workspace_bytes(int B, int H, int N, int d) {
+    if (B <= 0 || H <= 0 || N <= 0 || (d != 64 && d != 128)) return 0;
+    return workspace_bytes((long long)B * H, N, d);
+}
+
+fa_status fa_backward_ex(const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                         int Hq, int Hkv, int Tq, int Tk, int d, int causal, int window,
+                         float scale, void* workspace, struct CUstream_st* stream) {
+    Shape sh;
     bool empty = false;
-    fa_status st = check_common(B, H, N, d, causal, scale, &empty);
-    if (st != FA_OK || empty) return st;
+    fa_status st = check_shape(B, Hq, Hkv, Tq, Tk, d, causal, window, scale, &sh, &empty);
+    if (st != FA_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (empty) {
+        // No query rows: every key gets zero gradient.
+        const size_t kv_bytes = (size_t)sh.BHkv * (size_t)Tk * (size_t)d * 2u;
+        if (kv_bytes == 0) return FA_OK;
+        if (!dk || !dv) return FA_ERR_INVALID_ARG;
+        cudaError_t e = cudaMemsetAsync(dk, 0, kv_bytes, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(dv, 0, kv_bytes, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+        return FA_OK;
+    }
     if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
         !aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
         !aligned(lse, 4))
         return FA_ERR_ALIGNMENT;
     if (workspace && !aligned(workspace, 256)) return FA_ERR_ALIGNMENT;
-    const int BH = B * H;
-    const int Npad = (N + 127) / 128 * 128;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int Npad = (Tq + 127) / 128 * 128;
     fa::BwdLaunch a;
     std::memset(&a, 0, sizeof a);
     const int q_rows = (d == 128) ? 64 : 128;  // query rows per backward step
-    if ((st = make_map(&a.tm_q, q, BH, N, d, q_rows)) != FA_OK) return st;
-    if ((st = make_map(&a.tm_do, dout, BH, N, d, q_rows)) != FA_OK) return st;
-    if ((st = make_map(&a.tm_k, k, BH, N, d, 128)) != FA_OK) return st;
-    if ((st = make_map(&a.tm_v, v, BH, N, d, 128)) != FA_OK) return st;
-    if ((st = make_map(&a.tm_dk, dk, BH, N, d, 128)) != FA_OK) return st;
-    if ((st = make_map(&a.tm_dv, dv, BH, N, d, 128)) != FA_OK) return st;
+    if ((st = make_map(&a.tm_q, q, sh.BHq, Tq, d, q_rows)) != FA_OK) return st;
+    if ((st = make_map(&a.tm_do, dout, sh.BHq, Tq, d, q_rows)) != FA_OK) return st;
+    if ((st = make_map(&a.tm_k, k, sh.BHkv, Tk, d, 128)) != FA_OK) return st;
+    if ((st = make_map(&a.tm_v, v, sh.BHkv, Tk, d, 128)) != FA_OK) return st;
+    if ((st = make_map(&a.tm_dk, dk, sh.BHkv, Tk, d, 128)) != FA_OK) return st;
+    if ((st = make_map(&a.tm_dv, dv, sh.BHkv, Tk, d, 128)) != FA_OK) return st;
     if ((st = get_err_ptr(&a.err)) != FA_OK) return st;
-    const size_t ws_bytes = fa_backward_workspace_bytes(B, H, N, d);
+    const size_t ws_bytes = workspace_bytes(sh.BHq, Tq, d);
     void* ws = workspace;
     bool owned = false;
     if (!ws) {
@@ -244,15 +294,20 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
     a.lse = lse;
     a.dq = dq;
     a.stats = static_cast<float*>(ws);
-    a.dq_acc = static_cast<float*>(ws) + 2 * (size_t)BH * (size_t)Npad;
-    if ((st = make_map(&a.tm_dqacc, a.dq_acc, BH, Npad, d, q_rows, true)) != FA_OK) {
+    a.dq_acc = static_cast<float*>(ws) + 2 * (size_t)sh.BHq * (size_t)Npad;
+    if ((st = make_map(&a.tm_dqacc, a.dq_acc, sh.BHq, Npad, d, q_rows, true)) != FA_OK) {
         if (owned) cudaFreeAsync(ws, s);
         return st;
     }
-    a.N = N;
+    a.Tq = Tq;
+    a.Tk = Tk;
     a.Npad = Npad;
-    a.BH = BH;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.BHq = sh.BHq;
+    a.BHkv = sh.BHkv;
     a.d = d;
+    a.window = window;
     a.scale = scale;
     a.c = scale * kLog2e;
     cudaError_t e = fa::launch_backward(a, causal != 0, s);
@@ -264,12 +319,21 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
     return FA_OK;
 }
 
+fa_status fa_backward(const void* q, const void* k, const void* v, const void* o,
+                      const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                      int H, int N, int d, int causal, float scale, void* workspace,
+                      struct CUstream_st* stream) {
+    return fa_backward_ex(q, k, v, o, lse, dout, dq, dk, dv, B, H, H, N, N, d, causal, -1, scale,
+                          workspace, stream);
+}
+
 fa_status fa_backward_noalloc(const void* q, const void* k, const void* v, const void* o,
                               const float* lse, const void* dout, void* dq, void* dk, void* dv,
                               int B, int H, int N, int d, int causal, float scale,
                               struct CUstream_st* stream) {
+    Shape sh;
     bool empty = false;
-    fa_status st = check_common(B, H, N, d, causal, scale, &empty);
+    fa_status st = check_shape(B, H, H, N, N, d, causal, -1, scale, &sh, &empty);
     if (st != FA_OK || empty) return st;
     if (fa_backward_workspace_bytes(B, H, N, d) > (size_t)FA_NOALLOC_SCRATCH_BYTES)
         return FA_ERR_UNSUPPORTED;

@@ -115,6 +115,12 @@ fa_bwd_dq_kernel(const float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ d
 // ----------------------------------------------------------------------------------------
 // Main backward kernel.
 // ----------------------------------------------------------------------------------------
+// Problem shape of the backward: as the forward (query head bh_q reads KV head bh_q / group,
+// query row i at key position offset + i, optional window), seen from a key tile.
+struct BwdShape {
+    int Tq, Tk, Npad, Hq, Hkv, group, offset, window, BHq, nkb;
+};
+
 template <int D>
 struct BwdCfg {
     static constexpr int KT = 128;                    // keys per CTA
@@ -161,14 +167,14 @@ struct BwdBars {
     int abort_flag;
 };
 
-template <int D, bool CAUSAL>
+// WINDOW (causal only): queries more than `window` positions past a key do not see it.
+template <int D, bool CAUSAL, bool WINDOW>
 __global__ void __launch_bounds__(512, 1)
 fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
               const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
               const __grid_constant__ CUtensorMap tm_dqacc, const float* __restrict__ stats,
-              const int N, const int Npad, const int BH, const int nkb, const float c,
-              const float scale, int* err) {
+              const BwdShape sh, const float c, const float scale, int* err) {
     using C = BwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
@@ -177,12 +183,35 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const int warp = tid >> 5;
     const int lane = tid & 31;
 
-    const int bh = blockIdx.x / nkb;
-    const int kb = blockIdx.x % nkb;
+    // This CTA: KV head bh_kv, keys [key0, key0 + 128). It visits every query head of the
+    // group and, for each, the query steps whose rows can see some key of the tile: from the
+    // causal diagonal (query position offset + q >= key) to the window's reach (position -
+    // window <= key). A tile no query sees has no steps and stores zero gradients.
+    const int bh_kv = blockIdx.x / sh.nkb;
+    const int kb = blockIdx.x % sh.nkb;
     const int key0 = kb * C::KT;
-    const int nq_total = (N + C::BMQ - 1) / C::BMQ;
-    const int i0 = CAUSAL ? (key0 / C::BMQ) : 0;
-    const int nsteps = nq_total - i0;  // >= 1 because key0 < N
+    const int nq_total = (sh.Tq + C::BMQ - 1) / C::BMQ;
+    const int i0 = CAUSAL ? max(0, key0 - sh.offset) / C::BMQ : 0;
+    int i1 = nq_total - 1;
+    if (WINDOW) {
+        const int reach = key0 + C::KT - 1 + sh.window - sh.offset;  // last query that sees a key
+        i1 = (reach < 0) ? -1 : min(i1, reach / C::BMQ);
+    }
+    const int nsteps_g = max(0, i1 - i0 + 1);
+    const int nsteps = nsteps_g * sh.group;
+    const int bhq_base = (bh_kv / sh.Hkv) * sh.Hq + (bh_kv % sh.Hkv) * sh.group;
+    // Steps run query head by query head of the group, each over query blocks i0 .. i1; a
+    // role walks them with a StepCursor (no division per step).
+    struct StepCursor {
+        int bhq, qi;
+    };
+    auto first_step = [&]() { return StepCursor{bhq_base, i0}; };
+    auto next_step = [&](StepCursor& cur) {
+        if (++cur.qi > i1) {
+            cur.qi = i0;
+            ++cur.bhq;
+        }
+    };
 
     if (tid == 0) {
         ptx::mbar_init(ptx::smem_addr(&bars->kv_full), 1);
@@ -230,27 +259,29 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             const uint32_t b_kv = ptx::smem_addr(&bars->kv_full);
             ptx::mbar_arrive_expect_tx(b_kv, 2 * C::KTILE);
             for (int ch = 0; ch < D / 64; ++ch) {
-                ptx::tma_load_3d(s_k + ch * C::KCHUNK, &tm_k, b_kv, ch * 64, key0, bh);
-                ptx::tma_load_3d(s_v + ch * C::KCHUNK, &tm_v, b_kv, ch * 64, key0, bh);
+                ptx::tma_load_3d(s_k + ch * C::KCHUNK, &tm_k, b_kv, ch * 64, key0, bh_kv);
+                ptx::tma_load_3d(s_v + ch * C::KCHUNK, &tm_v, b_kv, ch * 64, key0, bh_kv);
             }
             int issued = 0;
-            for (int si = 0; si < nsteps; ++si) {
+            StepCursor cur = first_step();
+            for (int si = 0; si < nsteps; ++si, next_step(cur)) {
                 const int st = si % C::NQS;
                 const uint32_t ph = (uint32_t)(si / C::NQS) & 1u;
                 if (!wait_phase(ptx::smem_addr(&bars->q_empty[st]), ph ^ 1u, abort_flag, err,
                                 kDevTimeoutConsumer))
                     break;
-                const int q0 = (i0 + si) * C::BMQ;
+                const int q0 = cur.qi * C::BMQ;
+                const int bhq = cur.bhq;
                 const uint32_t b_q = ptx::smem_addr(&bars->q_full[st]);
                 const uint32_t base = s_st + st * C::STAGE_BYTES;
                 ptx::mbar_arrive_expect_tx(b_q, 2 * C::QTILE + 2 * C::STAT_BYTES);
                 for (int ch = 0; ch < D / 64; ++ch) {
-                    ptx::tma_load_3d_hint(base + ch * C::QCHUNK, &tm_q, b_q, ch * 64, q0, bh, pol_keep);
+                    ptx::tma_load_3d_hint(base + ch * C::QCHUNK, &tm_q, b_q, ch * 64, q0, bhq, pol_keep);
                     ptx::tma_load_3d_hint(base + C::QTILE + ch * C::QCHUNK, &tm_do, b_q, ch * 64, q0,
-                                          bh, pol_keep);
+                                          bhq, pol_keep);
                 }
-                const float* lse2 = stats + (size_t)bh * Npad + q0;
-                const float* dvec = stats + (size_t)BH * Npad + (size_t)bh * Npad + q0;
+                const float* lse2 = stats + (size_t)bhq * sh.Npad + q0;
+                const float* dvec = stats + (size_t)sh.BHq * sh.Npad + (size_t)bhq * sh.Npad + q0;
                 ptx::bulk_load(base + 2 * C::QTILE, lse2, C::STAT_BYTES, b_q);
                 ptx::bulk_load(base + 2 * C::QTILE + C::STAT_BYTES, dvec, C::STAT_BYTES, b_q);
                 ++issued;
@@ -305,7 +336,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             // Two issuing warps (see the forward): warp 1 issues S^T/dP^T, warp 3 issues
             // dV/dK/dQ, so one warp's MMAs run while the other waits for operands.
             bool ok = warp_wait(ptx::smem_addr(&bars->kv_full), 0, abort_flag, err, kDevTimeoutLoad);
-            if (warp == 1) {
+            if (warp == 1 && nsteps > 0) {
                 if (ok) ok = warp_wait(ptx::smem_addr(&bars->q_full[0]), 0, abort_flag, err, kDevTimeoutLoad);
                 if (ok) {
                     ptx::tc_fence_after();
@@ -386,6 +417,8 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const int wq = warp & 3;
         const int k = wq * 32 + lane;  // key row within the tile
         const int key = key0 + k;
+        // (causal) queries at positions key .. key + window see this key; no window: all after it
+        const uint32_t vspan = WINDOW ? (uint32_t)sh.window : 0x7fffffffu;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const uint32_t t_s = tbase + lane_off + C::S_COL;
         const uint32_t t_dp = tbase + lane_off + C::DP_COL;
@@ -393,9 +426,10 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         constexpr int NCH = C::BMQ / 32;
         constexpr int NCH_H = NCH / 2;
         bool ok = true;
-        for (int si = 0; si < nsteps; ++si) {
+        StepCursor cur = first_step();
+        for (int si = 0; si < nsteps; ++si, next_step(cur)) {
             const int st = si % C::NQS;
-            const int q0 = (i0 + si) * C::BMQ;
+            const int q0 = cur.qi * C::BMQ;
             ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->s_full), (uint32_t)si & 1u,
                                                     abort_flag, err, kDevTimeoutMma));
             if (!ok) break;
@@ -407,7 +441,11 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             const float* lse2 = reinterpret_cast<const float*>(smem + C::OFF_ST + st * C::STAGE_BYTES + 2 * C::QTILE);
             const float* dvec = lse2 + C::BMQ;
             uint8_t* dsbuf = smem + C::OFF_DS + (si & 1) * C::DS_BYTES;
-            const bool need_mask = CAUSAL && (q0 < key0 + C::KT - 1);
+            // key visible to query q iff (!causal || key <= p) && (no window || key >= p - window),
+            // p = offset + q; elementwise masking only where the step crosses either edge.
+            const int p0 = sh.offset + q0;
+            const bool need_mask = CAUSAL && ((p0 < key0 + C::KT - 1) ||
+                                              (WINDOW && p0 + C::BMQ - 1 - sh.window > key0));
 #pragma unroll
             for (int ci = 0; ci < NCH_H; ++ci) {
                 const int cc = h * NCH_H + ci;
@@ -430,21 +468,23 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     float x0, x1, x2, x3;
                     ptx::ffma2(x0, x1, __uint_as_float(sv[j]), __uint_as_float(sv[j + 1]), c, c, -L.x, -L.y);
                     ptx::ffma2(x2, x3, __uint_as_float(sv[j + 2]), __uint_as_float(sv[j + 3]), c, c, -L.z, -L.w);
-                    float p0 = ptx::ex2_approx(x0), p1 = ptx::ex2_approx(x1);
-                    float p2 = ptx::ex2_approx(x2), p3 = ptx::ex2_approx(x3);
+                    float pe0 = ptx::ex2_approx(x0), pe1 = ptx::ex2_approx(x1);
+                    float pe2 = ptx::ex2_approx(x2), pe3 = ptx::ex2_approx(x3);
                     if (need_mask) {
-                        if (key > q0 + qi) p0 = 0.f;
-                        if (key > q0 + qi + 1) p1 = 0.f;
-                        if (key > q0 + qi + 2) p2 = 0.f;
-                        if (key > q0 + qi + 3) p3 = 0.f;
+                        // visible iff key <= p <= key + window, i.e. p - key in [0, vspan]
+                        const uint32_t dp = (uint32_t)(p0 + qi - key);
+                        if (dp > vspan) pe0 = 0.f;
+                        if (dp + 1u > vspan) pe1 = 0.f;
+                        if (dp + 2u > vspan) pe2 = 0.f;
+                        if (dp + 3u > vspan) pe3 = 0.f;
                     }
                     float y0, y1, y2, y3, d0, d1, d2, d3;
                     ptx::fadd2(y0, y1, __uint_as_float(dpv[j]), __uint_as_float(dpv[j + 1]), -Dq.x, -Dq.y);
                     ptx::fadd2(y2, y3, __uint_as_float(dpv[j + 2]), __uint_as_float(dpv[j + 3]), -Dq.z, -Dq.w);
-                    ptx::fmul2(d0, d1, p0, p1, y0, y1);
-                    ptx::fmul2(d2, d3, p2, p3, y2, y3);
-                    pk[j / 2] = ptx::pack_bf16x2(p0, p1);
-                    pk[j / 2 + 1] = ptx::pack_bf16x2(p2, p3);
+                    ptx::fmul2(d0, d1, pe0, pe1, y0, y1);
+                    ptx::fmul2(d2, d3, pe2, pe3, y2, y3);
+                    pk[j / 2] = ptx::pack_bf16x2(pe0, pe1);
+                    pk[j / 2 + 1] = ptx::pack_bf16x2(pe2, pe3);
                     dk[j / 2] = ptx::pack_bf16x2(d0, d1);
                     dk[j / 2 + 1] = ptx::pack_bf16x2(d2, d3);
                 }
@@ -481,16 +521,22 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             ptx::mbar_arrive(ptx::smem_addr(&bars->p_ready));
         }
         // ---- epilogue (first compute warpgroup): dV -> bf16 -> smem (stage 0 area) -> TMA store ----
-        if (ok && h == 0) ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->mma_done),
-                                                        (uint32_t)(nsteps - 1) & 1u, abort_flag,
-                                                        err, kDevTimeoutMma));
+        if (ok && h == 0 && nsteps > 0)
+            ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->mma_done),
+                                                    (uint32_t)(nsteps - 1) & 1u, abort_flag, err,
+                                                    kDevTimeoutMma));
         if (ok && h == 0) {
             ptx::tc_fence_after();
             uint8_t* stage = smem + C::OFF_ST;
 #pragma unroll
             for (int cc = 0; cc < D / 32; ++cc) {
                 uint32_t v[32];
-                ptx::tmem_ld32(tbase + lane_off + C::DV_COL + 32 * cc, v);
+                if (nsteps > 0) {
+                    ptx::tmem_ld32(tbase + lane_off + C::DV_COL + 32 * cc, v);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = 0u;  // no query sees these keys
+                }
                 uint8_t* chunk = stage + (cc >> 1) * C::KCHUNK;
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
@@ -506,7 +552,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             ptx::named_bar_sync(1, 128);
             if (k == 0) {
                 for (int ch = 0; ch < D / 64; ++ch)
-                    ptx::tma_store_3d(&tm_dv, ptx::smem_addr(stage + ch * C::KCHUNK), ch * 64, key0, bh);
+                    ptx::tma_store_3d(&tm_dv, ptx::smem_addr(stage + ch * C::KCHUNK), ch * 64, key0, bh_kv);
                 ptx::bulk_commit();
                 ptx::bulk_wait_read_all();
             }
@@ -518,8 +564,10 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         uint8_t* dqs = smem + C::OFF_DQS;
         bool ok = true;
-        for (int si = 0; si < nsteps; ++si) {
-            const int q0 = (i0 + si) * C::BMQ;
+        StepCursor cur = first_step();
+        for (int si = 0; si < nsteps; ++si, next_step(cur)) {
+            const int q0 = cur.qi * C::BMQ;
+            const int bhq = cur.bhq;
             ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->dq_full), (uint32_t)si & 1u,
                                                     abort_flag, err, kDevTimeoutMma));
             if (!ok) break;
@@ -561,22 +609,28 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             ptx::named_bar_sync(2, 128);
             if (r == 0) {
                 for (int bx = 0; bx < D / 32; ++bx)
-                    ptx::tma_reduce_add_3d(&tm_dqacc, ptx::smem_addr(dqs + bx * C::DQBOX), bx * 32, q0, bh);
+                    ptx::tma_reduce_add_3d(&tm_dqacc, ptx::smem_addr(dqs + bx * C::DQBOX), bx * 32, q0, bhq);
                 ptx::bulk_commit();
             }
         }
         if (r == 0) ptx::bulk_wait_all();
         // ---- epilogue: dK * scale -> bf16 -> smem (stage 1 area) -> TMA store ----
-        if (ok) ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->mma_done),
-                                                        (uint32_t)(nsteps - 1) & 1u, abort_flag,
-                                                        err, kDevTimeoutMma));
+        if (ok && nsteps > 0)
+            ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->mma_done),
+                                                    (uint32_t)(nsteps - 1) & 1u, abort_flag, err,
+                                                    kDevTimeoutMma));
         if (ok) {
             ptx::tc_fence_after();
             uint8_t* stage = smem + C::OFF_ST + C::STAGE_BYTES;
 #pragma unroll
             for (int cc = 0; cc < D / 32; ++cc) {
                 uint32_t v[32];
-                ptx::tmem_ld32(tbase + lane_off + C::DK_COL + 32 * cc, v);
+                if (nsteps > 0) {
+                    ptx::tmem_ld32(tbase + lane_off + C::DK_COL + 32 * cc, v);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = 0u;  // no query sees these keys
+                }
                 uint8_t* chunk = stage + (cc >> 1) * C::KCHUNK;
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
@@ -592,7 +646,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             ptx::named_bar_sync(2, 128);
             if (r == 0) {
                 for (int ch = 0; ch < D / 64; ++ch)
-                    ptx::tma_store_3d(&tm_dk, ptx::smem_addr(stage + ch * C::KCHUNK), ch * 64, key0, bh);
+                    ptx::tma_store_3d(&tm_dk, ptx::smem_addr(stage + ch * C::KCHUNK), ch * 64, key0, bh_kv);
                 ptx::bulk_commit();
                 ptx::bulk_wait_read_all();
             }
@@ -607,43 +661,54 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool WINDOW>
 cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t stream) {
+    static_assert(CAUSAL || !WINDOW, "a window hangs off the causal diagonal");
     using C = BwdCfg<D>;
-    // 1. preprocess
+    // 1. preprocess (query heads)
     {
-        const long long rows = (long long)a.BH * a.Npad;
+        const long long rows = (long long)a.BHq * a.Npad;
         const long long rpb = 256 / (D / 8);
         const long long blocks = (rows + rpb - 1) / rpb;
         if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
         fa_bwd_pre_kernel<D><<<(unsigned)blocks, 256, 0, stream>>>(
             static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.lse,
-            a.stats, a.dq_acc, a.N, a.Npad, a.BH);
+            a.stats, a.dq_acc, a.Tq, a.Npad, a.BHq);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    // 2. main
+    // 2. main (one CTA per KV head and 128-key tile)
     {
-        auto kern = fa_bwd_kernel<D, CAUSAL>;
+        auto kern = fa_bwd_kernel<D, CAUSAL, WINDOW>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        const int nkb = (a.N + C::KT - 1) / C::KT;
-        const long long blocks = (long long)nkb * a.BH;
+        BwdShape sh;
+        sh.Tq = a.Tq;
+        sh.Tk = a.Tk;
+        sh.Npad = a.Npad;
+        sh.Hq = a.Hq;
+        sh.Hkv = a.Hkv;
+        sh.group = a.Hq / a.Hkv;
+        sh.offset = a.Tk - a.Tq;
+        sh.window = a.window;
+        sh.BHq = a.BHq;
+        sh.nkb = (a.Tk + C::KT - 1) / C::KT;
+        const long long blocks = (long long)sh.nkb * a.BHkv;
         if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
         kern<<<(unsigned)blocks, C::THREADS, C::SMEM_BYTES, stream>>>(
-            a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dk, a.tm_dv, a.tm_dqacc, a.stats, a.N, a.Npad,
-            a.BH, nkb, a.c, a.scale, a.err);
+            a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dk, a.tm_dv, a.tm_dqacc, a.stats, sh, a.c,
+            a.scale, a.err);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    // 3. dQ convert
+    // 3. dQ convert (query heads)
     {
-        const long long total8 = (long long)a.BH * a.N * (D / 8);
+        const long long total8 = (long long)a.BHq * a.Tq * (D / 8);
         const long long blocks = (total8 + 255) / 256;
         if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
         fa_bwd_dq_kernel<D><<<(unsigned)blocks, 256, 0, stream>>>(
-            a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), a.N, a.Npad, a.BH, a.scale);
+            a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), a.Tq, a.Npad, a.BHq, a.scale);
         return cudaGetLastError();
     }
 }
@@ -651,8 +716,16 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_backward(const BwdLaunch& a, bool causal, cudaStream_t stream) {
-    if (a.d == 64) return causal ? launch_bwd_t<64, true>(a, stream) : launch_bwd_t<64, false>(a, stream);
-    if (a.d == 128) return causal ? launch_bwd_t<128, true>(a, stream) : launch_bwd_t<128, false>(a, stream);
+    const bool window = a.window >= 0;
+    if (window && !causal) return cudaErrorInvalidValue;
+    if (a.d == 64) {
+        if (!causal) return launch_bwd_t<64, false, false>(a, stream);
+        return window ? launch_bwd_t<64, true, true>(a, stream) : launch_bwd_t<64, true, false>(a, stream);
+    }
+    if (a.d == 128) {
+        if (!causal) return launch_bwd_t<128, false, false>(a, stream);
+        return window ? launch_bwd_t<128, true, true>(a, stream) : launch_bwd_t<128, true, false>(a, stream);
+    }
     return cudaErrorInvalidValue;
 }
 

@@ -94,9 +94,21 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     }
 }
 
-// One work unit: (bh, 256-row block qb).
+// Problem shape: query heads read KV head bh_q / group; query row i sits at key position
+// offset + i (offset = Tk - Tq, so the last query lines up with the last key); with a window,
+// keys before position - window are not visible.
+struct FwdShape {
+    int Tq, Tk, Hq, Hkv, group, offset, window, nqb;
+};
+
+// One work unit: (query head bh_q, 256-row block qb) and, per Q tile t, its range of key
+// tiles [jb_t, je_t) (empty when the tile lies past Tq).
 struct FwdUnit {
-    int bh, qb, n0, n1, nkv;
+    int bh_q, bh_kv, qb;
+    int jb0, je0, jb1, je1;
+    int jb_all, je_all;
+    __device__ __forceinline__ int jb(int t) const { return t ? jb1 : jb0; }
+    __device__ __forceinline__ int je(int t) const { return t ? je1 : je0; }
 };
 
 // The k-th unit of CTA `cta` (of G), or -1 past the end. Units are numbered head by head.
@@ -111,32 +123,48 @@ __device__ __forceinline__ int fwd_unit_index(int cta, int k, int G, int U) {
     return u < U ? (int)u : -1;
 }
 
-template <int D, bool CAUSAL>
-__device__ __forceinline__ FwdUnit fwd_unit(int u, int nqb, int N) {
+template <int D, bool CAUSAL, bool WINDOW>
+__device__ __forceinline__ FwdUnit fwd_unit(int u, const FwdShape& sh) {
     using C = FwdCfg<D>;
     FwdUnit w;
-    w.bh = u / nqb;
-    const int i = u % nqb;
+    w.bh_q = u / sh.nqb;
+    const int i = u % sh.nqb;
     if (CAUSAL) {
-        const int q = (i & 1) ? nqb - 1 - (i >> 1) : (i >> 1);  // rank by cost, 0 = heaviest
-        w.qb = nqb - 1 - q;
+        const int q = (i & 1) ? sh.nqb - 1 - (i >> 1) : (i >> 1);  // rank by cost, 0 = heaviest
+        w.qb = sh.nqb - 1 - q;
     } else {
         w.qb = i;
     }
-    const int nk_total = (N + C::BN - 1) / C::BN;
-    const int r1 = w.qb * C::ROWS + C::BM;
-    w.n0 = CAUSAL ? min(nk_total, w.qb * 2 + 1) : nk_total;
-    w.n1 = (r1 >= N) ? 0 : (CAUSAL ? min(nk_total, w.qb * 2 + 2) : nk_total);
-    w.nkv = max(w.n0, w.n1);
+    w.bh_kv = (w.bh_q / sh.Hq) * sh.Hkv + (w.bh_q % sh.Hq) / sh.group;
+    const int nk = (sh.Tk + C::BN - 1) / C::BN;
+    // key tiles [jb, je) of the Q tile starting at row r0 (empty past Tq)
+    auto range = [&](int r0, int& jb, int& je) {
+        if (r0 >= sh.Tq) {
+            jb = je = 0;
+            return;
+        }
+        const int p0 = sh.offset + r0;                                // first row's position
+        const int p1 = sh.offset + min(r0 + C::BM, sh.Tq) - 1;       // last row's position
+        je = CAUSAL ? min(nk, p1 / C::BN + 1) : nk;
+        jb = WINDOW ? max(0, p0 - sh.window) / C::BN : 0;
+        if (jb >= je) jb = je = 0;  // (cannot happen for valid shapes)
+    };
+    range(w.qb * C::ROWS, w.jb0, w.je0);
+    range(w.qb * C::ROWS + C::BM, w.jb1, w.je1);
+    w.jb_all = w.jb0;  // tile 0 is never empty
+    w.je_all = max(w.je0, w.je1);
+    if (w.je1 > w.jb1) w.jb_all = min(w.jb_all, w.jb1);
+    if (w.je_all <= w.jb_all) w.jb_all = w.je_all = 0;
     return w;
 }
 
-template <int D, bool CAUSAL>
+// WINDOW (causal only): keys before position - window are not visible.
+template <int D, bool CAUSAL, bool WINDOW>
 __global__ void __launch_bounds__(384, 1)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-              const int N, const int nqb, const int num_units, const float c,
-              float* __restrict__ lse_out, int* err) {
+              const FwdShape sh, const int num_units, const float c, float* __restrict__ lse_out,
+              int* err) {
     using C = FwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
@@ -196,7 +224,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             int last_q_use[2] = {-1, -1};
             bool ok = true;
             for (int u; ok && (u = fwd_unit_index<CAUSAL>(blockIdx.x, ul, G, num_units)) >= 0; ++ul) {
-                const FwdUnit w = fwd_unit<D, CAUSAL>(u, nqb, N);
+                const FwdUnit w = fwd_unit<D, CAUSAL, WINDOW>(u, sh);
                 const int b = ul % C::NQB;
                 const int use = ul / C::NQB;  // earlier uses of Q buffer b
                 if (use > 0) {
@@ -206,15 +234,15 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     if (!ok) break;
                 }
                 const uint32_t bq = ptx::smem_addr(&bars->q_full[b]);
-                const int ntl = 1 + (w.n1 > 0);
+                const int ntl = 1 + (w.je1 > w.jb1);
                 ptx::mbar_arrive_expect_tx(bq, ntl * C::TILE_BYTES);
                 for (int t = 0; t < ntl; ++t)
                     for (int ch = 0; ch < C::DCH; ++ch)
                         ptx::tma_load_3d_hint(s_q + (b * 2 + t) * C::TILE_BYTES + ch * C::CHUNK_BYTES,
-                                              &tm_q, bq, ch * 64, w.qb * C::ROWS + t * C::BM, w.bh,
+                                              &tm_q, bq, ch * 64, w.qb * C::ROWS + t * C::BM, w.bh_q,
                                               pol_q);
                 last_q_use[b] = use;
-                for (int j = 0; j < w.nkv; ++j, ++kv) {
+                for (int j = w.jb_all; j < w.je_all; ++j, ++kv) {
                     const int s = kv % C::NS;
                     const uint32_t ph = (uint32_t)(kv / C::NS) & 1u;
                     const uint32_t bkf = ptx::smem_addr(&bars->k_full[s]);
@@ -225,7 +253,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     ptx::mbar_arrive_expect_tx(bkf, C::TILE_BYTES);
                     for (int ch = 0; ch < C::DCH; ++ch)
                         ptx::tma_load_3d_hint(s_k + s * C::TILE_BYTES + ch * C::CHUNK_BYTES, &tm_k,
-                                              bkf, ch * 64, j * C::BN, w.bh, pol_kv);
+                                              bkf, ch * 64, j * C::BN, w.bh_kv, pol_kv);
                     ok = wait_phase(ptx::smem_addr(&bars->v_empty[s]), ph ^ 1u, abort_flag, err,
                                     kDevTimeoutConsumer);
                     if (!ok) {
@@ -235,7 +263,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     ptx::mbar_arrive_expect_tx(bvf, C::TILE_BYTES);
                     for (int ch = 0; ch < C::DCH; ++ch)
                         ptx::tma_load_3d_hint(s_v + s * C::TILE_BYTES + ch * C::CHUNK_BYTES, &tm_v,
-                                              bvf, ch * 64, j * C::BN, w.bh, pol_kv);
+                                              bvf, ch * 64, j * C::BN, w.bh_kv, pol_kv);
                 }
             }
             // Drain: every copy issued must have landed before the CTA can exit.
@@ -269,18 +297,17 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         int ul = 0;
         bool ok = true;
         for (int u; ok && (u = fwd_unit_index<CAUSAL>(blockIdx.x, ul, G, num_units)) >= 0; ++ul) {
-            const FwdUnit w = fwd_unit<D, CAUSAL>(u, nqb, N);
-            const int nt[2] = {w.n0, w.n1};
+            const FwdUnit w = fwd_unit<D, CAUSAL, WINDOW>(u, sh);
             const int b = ul % C::NQB;
             if (warp == 1) {
                 ok = warp_wait(ptx::smem_addr(&bars->q_full[b]), (uint32_t)(ul / C::NQB) & 1u,
                                abort_flag, err, kDevTimeoutLoad);
-                for (int j = 0; ok && j < w.nkv; ++j, ++kv) {
+                for (int j = w.jb_all; ok && j < w.je_all; ++j, ++kv) {
                     const int s = kv % C::NS;
                     ok = warp_wait(ptx::smem_addr(&bars->k_full[s]), (uint32_t)(kv / C::NS) & 1u,
                                    abort_flag, err, kDevTimeoutLoad);
                     for (int t = 0; ok && t < 2; ++t) {
-                        if (j >= nt[t]) continue;
+                        if (j < w.jb(t) || j >= w.je(t)) continue;
                         if (it[t] > 0) {
                             // S_t may be overwritten once the softmax has read S_t (P in its own
                             // columns) or once O_t += P_t V has consumed P_t (P over S).
@@ -309,13 +336,13 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     if (ok) commit(&bars->k_empty[s]);
                 }
             } else {
-                for (int j = 0; ok && j < w.nkv; ++j, ++kv) {
+                for (int j = w.jb_all; ok && j < w.je_all; ++j, ++kv) {
                     const int s = kv % C::NS;
                     ok = warp_wait(ptx::smem_addr(&bars->v_full[s]), (uint32_t)(kv / C::NS) & 1u,
                                    abort_flag, err, kDevTimeoutLoad);
                     for (int t = 0; ok && t < 2; ++t) {
-                        if (j >= nt[t]) continue;
-                        if (j == 0 && uo[t] > 0) {
+                        if (j < w.jb(t) || j >= w.je(t)) continue;
+                        if (j == w.jb(t) && uo[t] > 0) {
                             // O_t is about to be overwritten: the previous unit's epilogue must
                             // have read it (o_free completes once per unit in which tile t ran).
                             ok = warp_wait(ptx::smem_addr(&bars->o_free[t]),
@@ -334,7 +361,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 #pragma unroll
                             for (int kk = 0; kk < C::BN / 16; ++kk)
                                 ptx::mma_ts(d_tmem, p_tmem + kk * 8, ptx::sdesc_add(vd, kk * 2048),
-                                            idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                                            idesc_o, (j > w.jb(t) || kk > 0) ? 1u : 0u);
                             ptx::mma_commit(ptx::smem_addr(&bars->o_done[t]));
                         }
                         __syncwarp();
@@ -342,7 +369,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     }
                     if (ok) commit(&bars->v_empty[s]);
                 }
-                for (int t = 0; t < 2; ++t) uo[t] += (nt[t] > 0);
+                for (int t = 0; t < 2; ++t) uo[t] += (w.je(t) > w.jb(t));
             }
         }
         // Every MMA this warp issued (and every commit arrive) must be done before TMEM and
@@ -366,11 +393,18 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         int ul = 0;
         bool ok = true;
         for (int u; ok && (u = fwd_unit_index<CAUSAL>(blockIdx.x, ul, G, num_units)) >= 0; ++ul) {
-            const FwdUnit w = fwd_unit<D, CAUSAL>(u, nqb, N);
-            const int n = (t == 0) ? w.n0 : w.n1;
+            const FwdUnit w = fwd_unit<D, CAUSAL, WINDOW>(u, sh);
+            const int jb = w.jb(t), je = w.je(t);
+            const int n = je - jb;
             const int b = ul % C::NQB;
             const int row0 = w.qb * C::ROWS + t * C::BM;
             const int row = row0 + r;
+            const int pos = sh.offset + row;               // this row's key position
+            const int pos_first = sh.offset + row0;        // first row of the tile
+            const int pos_last = sh.offset + min(row0 + C::BM, sh.Tq) - 1;
+            // Keys [vis_lo, vis_hi] are visible to this row.
+            const int vis_lo = WINDOW ? max(0, pos - sh.window) : 0;
+            const int vis_hi = CAUSAL ? min(pos, sh.Tk - 1) : sh.Tk - 1;
             if (n == 0) {
                 // This Q tile is past N in this unit: release its share of the Q buffer. It
                 // first waits for this unit's Q load, so that its arrival counts towards this
@@ -388,7 +422,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             // alpha = exp2(m_old - m_new). O is rescaled only when some row of the warp moved.
             float m_ref = -INFINITY;  // reference (scaled log2 domain)
             float l = 0.f;            // running sum of exp2(c*s - m_ref)
-            for (int j = 0; j < n; ++j, ++it) {
+            for (int j = jb; j < je; ++j, ++it) {
                 ok = __all_sync(0xffffffffu, wait_phase(b_s_full, (uint32_t)it & 1u, abort_flag, err,
                                                         kDevTimeoutMma));
                 if (!ok) break;
@@ -417,13 +451,17 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     ptx::mbar_arrive(b_s_free);  // S_t columns may be overwritten now
                 }
                 const int key0 = j * C::BN;
-                const bool need_mask = (key0 + C::BN > N) || (CAUSAL && key0 + C::BN - 1 > row0);
+                // Elementwise masking only on tiles that cross the causal diagonal, the window's
+                // left edge or the end of the keys.
+                const bool need_mask = (key0 + C::BN > sh.Tk) ||
+                                       (CAUSAL && key0 + C::BN - 1 > pos_first) ||
+                                       (WINDOW && key0 < pos_last - sh.window);
                 if (need_mask) {
+                    const int klo = vis_lo - key0;
+                    const uint32_t span = (uint32_t)(vis_hi - vis_lo);
 #pragma unroll
-                    for (int k = 0; k < C::BN; ++k) {
-                        const int key = key0 + k;
-                        if (key >= N || (CAUSAL && key > row)) s[k] = -INFINITY;
-                    }
+                    for (int k = 0; k < C::BN; ++k)
+                        if ((uint32_t)(k - klo) > span) s[k] = -INFINITY;
                 }
                 // Row max: four independent chains of three-input max.
                 float a0 = s[0], a1 = s[1], a2 = s[2], a3 = s[3];
@@ -463,7 +501,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     for (int i = 0; i < 4; ++i) pk[k / 2 + i] = ptx::pack_bf16x2(s[k + 2 * i], s[k + 2 * i + 1]);
                 }
                 l = l * alpha + (((r0 + r1) + (r2 + r3)) + ((r4 + r5) + (r6 + r7)));
-                if (j > 0) {
+                if (j > jb) {
                     // O_t += P_t(j-1) V must be complete before P_t is overwritten (separate P
                     // columns) and before O_t is rescaled.
                     ok = __all_sync(0xffffffffu, wait_phase(b_o_done, (uint32_t)(it - 1) & 1u,
@@ -532,11 +570,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             }
             ptx::fence_proxy_async_smem();
             ptx::named_bar_sync(1 + t, C::BM);
-            if (row < N) lse_out[(size_t)w.bh * N + row] = (m_ref + __log2f(l)) * kLn2;
+            if (row < sh.Tq) lse_out[(size_t)w.bh_q * sh.Tq + row] = (m_ref + __log2f(l)) * kLn2;
             if (r == 0) {
                 for (int ch = 0; ch < C::DCH; ++ch)
                     ptx::tma_store_3d(&tm_o, ptx::smem_addr(stage + ch * C::CHUNK_BYTES), ch * 64,
-                                      row0, w.bh);
+                                      row0, w.bh_q);
                 ptx::bulk_commit();
                 ptx::bulk_wait_read_all();
                 // the staging area (this tile's half of Q buffer b) may be reloaded now
@@ -553,20 +591,29 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool WINDOW>
 cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
+    static_assert(CAUSAL || !WINDOW, "a window hangs off the causal diagonal");
     using C = FwdCfg<D>;
-    auto kern = fa_fwd_kernel<D, CAUSAL>;
+    auto kern = fa_fwd_kernel<D, CAUSAL, WINDOW>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    const int nqb = (a.N + C::ROWS - 1) / C::ROWS;
-    const long long units = (long long)nqb * a.BH;
+    FwdShape sh;
+    sh.Tq = a.Tq;
+    sh.Tk = a.Tk;
+    sh.Hq = a.Hq;
+    sh.Hkv = a.Hkv;
+    sh.group = a.Hq / a.Hkv;
+    sh.offset = a.Tk - a.Tq;
+    sh.window = a.window;
+    sh.nqb = (a.Tq + C::ROWS - 1) / C::ROWS;
+    const long long units = (long long)sh.nqb * a.BHq;
     if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     // Persistent grid: one CTA per SM (the shared-memory footprint admits no more), each
-    // walking units blockIdx.x, blockIdx.x + gridDim.x, ...
+    // walking its units in the order fwd_unit_index gives.
     const int grid = (int)std::min<long long>(units, (long long)a.num_sms);
-    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.N, nqb,
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, sh,
                                                       (int)units, a.c, a.lse, a.err);
     return cudaGetLastError();
 }
@@ -574,8 +621,16 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_forward(const FwdLaunch& a, int d, bool causal, cudaStream_t stream) {
-    if (d == 64) return causal ? launch_fwd_t<64, true>(a, stream) : launch_fwd_t<64, false>(a, stream);
-    if (d == 128) return causal ? launch_fwd_t<128, true>(a, stream) : launch_fwd_t<128, false>(a, stream);
+    const bool window = a.window >= 0;
+    if (window && !causal) return cudaErrorInvalidValue;
+    if (d == 64) {
+        if (!causal) return launch_fwd_t<64, false, false>(a, stream);
+        return window ? launch_fwd_t<64, true, true>(a, stream) : launch_fwd_t<64, true, false>(a, stream);
+    }
+    if (d == 128) {
+        if (!causal) return launch_fwd_t<128, false, false>(a, stream);
+        return window ? launch_fwd_t<128, true, true>(a, stream) : launch_fwd_t<128, true, false>(a, stream);
+    }
     return cudaErrorInvalidValue;
 }
 

@@ -8,11 +8,14 @@
 namespace fa {
 
 struct FwdLaunch {
-    CUtensorMap tm_q, tm_k, tm_v, tm_o;  // 3-D maps over [B*H, N, d] bf16, box {64, 128, 1}
-    int N;                               // sequence length
-    int BH;                              // B * H
+    CUtensorMap tm_q, tm_o;              // 3-D maps over [B*Hq, Tq, d] bf16, box {64, 128, 1}
+    CUtensorMap tm_k, tm_v;              // 3-D maps over [B*Hkv, Tk, d] bf16, box {64, 128, 1}
+    int Tq, Tk;                          // query and key sequence lengths
+    int Hq, Hkv;                         // query heads, KV heads (Hq % Hkv == 0)
+    int BHq;                             // B * Hq
+    int window;                          // -1: none; else keys >= position - window (causal)
     float c;                             // scale * log2(e)
-    float* lse;                          // [B*H, N] fp32
+    float* lse;                          // [B*Hq, Tq] fp32
     int* err;                            // device error word
     int num_sms;                         // SMs of the device (persistent grid size)
 };
@@ -21,16 +24,17 @@ struct FwdLaunch {
 cudaError_t launch_forward(const FwdLaunch& a, int d, bool causal, cudaStream_t stream);
 
 struct BwdLaunch {
-    CUtensorMap tm_q, tm_k, tm_v, tm_do;  // loads, box {64, rows, 1}
-    CUtensorMap tm_dk, tm_dv;             // stores, box {64, 128, 1}
+    CUtensorMap tm_q, tm_do;              // [B*Hq, Tq, d] loads, box {64, query rows, 1}
+    CUtensorMap tm_k, tm_v;               // [B*Hkv, Tk, d] loads, box {64, 128, 1}
+    CUtensorMap tm_dk, tm_dv;             // [B*Hkv, Tk, d] stores, box {64, 128, 1}
     CUtensorMap tm_dqacc;                 // fp32 [B*H, Npad, d] accumulator, box {32, rows, 1}
     const void* o;                        // bf16 [B*H, N, d]
     const void* dout;                     // bf16 [B*H, N, d]
-    const float* lse;                     // fp32 [B*H, N]
-    void* dq;                             // bf16 [B*H, N, d]
-    float* stats;                         // workspace: [B*H, Npad] (LSE*log2e) then [B*H, Npad] (D)
-    float* dq_acc;                        // workspace: fp32 [B*H, Npad, d]
-    int N, Npad, BH, d;
+    const float* lse;                     // fp32 [B*Hq, Tq]
+    void* dq;                             // bf16 [B*Hq, Tq, d]
+    float* stats;                         // workspace: [B*Hq, Npad] (LSE*log2e) then (D)
+    float* dq_acc;                        // workspace: fp32 [B*Hq, Npad, d]
+    int Tq, Tk, Npad, Hq, Hkv, BHq, BHkv, d, window;
     float scale;
     float c;                              // scale * log2(e)
     int* err;

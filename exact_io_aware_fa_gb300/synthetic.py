@@ -121,6 +121,21 @@ def attention_inputs(B: int, H: int, N: int, d: int, seed: int, qk_sigma: float 
     return res
 
 
+def attention_inputs_ex(B: int, Hq: int, Hkv: int, Tq: int, Tk: int, d: int, seed: int,
+                        qk_sigma: float = 1.0, v_sigma: float = 1.0,
+                        with_dout: bool = False) -> dict:
+    """Q [B, Hq, Tq, d], K and V [B, Hkv, Tk, d] (and dO like Q) as bf16 bit arrays, for
+    grouped KV heads and query blocks shorter than the key sequence."""
+    res = {
+        "q": normal_bf16_bits((B, Hq, Tq, d), seed, TENSOR_Q, qk_sigma),
+        "k": normal_bf16_bits((B, Hkv, Tk, d), seed, TENSOR_K, qk_sigma),
+        "v": normal_bf16_bits((B, Hkv, Tk, d), seed, TENSOR_V, v_sigma),
+    }
+    if with_dout:
+        res["do"] = normal_bf16_bits((B, Hq, Tq, d), seed, TENSOR_DO, 1.0)
+    return res
+
+
 def sample_rows(N: int, count: int, seed: int, tile: int = 128) -> np.ndarray:
     """Sorted unique row indices: ``count`` seeded rows plus the tile-boundary rows
     {0, tile-1, tile, 2*tile-1, N-tile-1, N-1} that fall inside [0, N)."""

@@ -70,6 +70,27 @@ fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float
                      int H, int N, int d, int causal, float scale, struct CUstream_st* stream);
 
 /*
+ * Forward with grouped KV heads, a query offset and an optional sliding window ("15.
+ * FlashAttention", inference.shantanugoel.com, sections "The algorithm in plain PyTorch" and
+ * "Details worth noticing": query head h reads KV head h / (Hq / Hkv); query row i sits at
+ * absolute position Tk - Tq + i, so the newest query lines up with the newest key and one call
+ * serves prefill (Tq = Tk), chunked prefill (Tq < Tk) and decode (Tq = 1); section "Stretch
+ * exercises", item 3: a window of W keeps only keys at positions >= position - W).
+ * Key j is visible to query row i, at position p = Tk - Tq + i, iff
+ *     (causal == 0 || j <= p)  and  (window < 0 || j >= p - window).
+ *   q        in : bf16 [B,Hq,Tq,d]      k, v in : bf16 [B,Hkv,Tk,d]
+ *   o        out: bf16 [B,Hq,Tq,d]      lse  out: fp32 [B,Hq,Tq]
+ *   Hq % Hkv == 0 (Hkv = Hq: multi-head; Hkv = 1: multi-query).
+ *   window = -1 for none; window >= 0 requires causal = 1 (the window is measured back from the
+ *   diagonal). Every query row must see a key: Tk >= 1, and with causal Tq <= Tk; otherwise
+ *   FA_ERR_INVALID_ARG. Other arguments and errors as fa_forward, which is this call with
+ *   Hq = Hkv = H, Tq = Tk = N, window = -1. B*Hq*Tq == 0 launches nothing.
+ */
+fa_status fa_forward_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                        int Hq, int Hkv, int Tq, int Tk, int d, int causal, int window,
+                        float scale, struct CUstream_st* stream);
+
+/*
  * Bytes of device workspace fa_backward needs for these sizes: two fp32 row statistics
  * [B*H, Npad] and an fp32 dQ accumulator [B*H, Npad, d], Npad = N rounded up to 128.
  * Returns 0 for invalid sizes or when B*H*N == 0.
@@ -93,6 +114,21 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
                       const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
                       int H, int N, int d, int causal, float scale, void* workspace,
                       struct CUstream_st* stream);
+
+/*
+ * Backward of fa_forward_ex (same visibility rule and shapes): dq bf16 [B,Hq,Tq,d]; dk, dv
+ * bf16 [B,Hkv,Tk,d], where the gradient of a KV head sums the contributions of all Hq / Hkv
+ * query heads that read it. Keys no query sees get zero gradient; with B*Hq*Tq == 0 and
+ * B*Hkv*Tk > 0 the call only zeroes dk and dv (q, k, v, o, lse, dout, dq may then be NULL).
+ *   workspace: >= fa_backward_workspace_bytes(B, Hq, Tq, d) bytes, 256-byte aligned, or NULL
+ *              (allocated and freed on `stream`).
+ * Errors as fa_forward_ex and fa_backward. fa_backward is this call with Hq = Hkv = H,
+ * Tq = Tk = N, window = -1.
+ */
+fa_status fa_backward_ex(const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                         int Hq, int Hkv, int Tq, int Tk, int d, int causal, int window,
+                         float scale, void* workspace, struct CUstream_st* stream);
 
 /*
  * Allocation-free backward (no counterpart in the pages: an integration convenience).

@@ -101,3 +101,51 @@ def test_missing_library_fails_loudly(tmp_path):
             api.library(str(tmp_path / "nope.so"))
     finally:
         api._LIB = saved
+
+
+def fwd_ex(lib, B=1, Hq=4, Hkv=2, Tq=128, Tk=256, d=64, causal=1, window=-1, scale=0.125, **ptrs):
+    p = {n: A for n in ("q", "k", "v", "o", "lse")}
+    p.update(ptrs)
+    return lib.fa_forward_ex(p["q"], p["k"], p["v"], p["o"], p["lse"], B, Hq, Hkv, Tq, Tk, d,
+                             causal, window, scale, None)
+
+
+def bwd_ex(lib, B=1, Hq=4, Hkv=2, Tq=128, Tk=256, d=64, causal=1, window=-1, scale=0.125, ws=0,
+           **ptrs):
+    p = {n: A for n in ("q", "k", "v", "o", "lse", "do", "dq", "dk", "dv")}
+    p.update(ptrs)
+    return lib.fa_backward_ex(p["q"], p["k"], p["v"], p["o"], p["lse"], p["do"], p["dq"],
+                              p["dk"], p["dv"], B, Hq, Hkv, Tq, Tk, d, causal, window, scale, ws,
+                              None)
+
+
+EX_REJECT = [
+    (dict(Hq=3, Hkv=2), 1),               # Hq not a multiple of Hkv
+    (dict(Hq=4, Hkv=0), 1), (dict(Hq=0, Hkv=2), 1),
+    (dict(Hkv=-1), 1), (dict(Tq=-1), 1), (dict(Tk=-3), 1),
+    (dict(causal=0, window=10), 1),       # a window needs the causal diagonal
+    (dict(window=-2), 1),
+    (dict(Tq=300, Tk=200), 1),            # causal with more queries than keys: empty rows
+    (dict(causal=0, Tk=0), 1),            # no keys at all
+    (dict(d=96), 2), (dict(scale=0.0), 1), (dict(causal=2), 1),
+    (dict(k=0), 1), (dict(v=A + 2), 3), (dict(lse=A + 1), 3),
+]
+
+
+@pytest.mark.parametrize("kw,status", EX_REJECT)
+def test_forward_ex_rejects(lib, kw, status):
+    assert fwd_ex(lib, **kw) == status
+
+
+@pytest.mark.parametrize("kw,status", EX_REJECT + [(dict(dk=0), 1), (dict(ws=A + 32), 3)])
+def test_backward_ex_rejects(lib, kw, status):
+    assert bwd_ex(lib, **kw) == status
+
+
+def test_ex_empty_is_ok(lib):
+    assert fwd_ex(lib, Tq=0) == 0
+    assert fwd_ex(lib, B=0) == 0
+    assert fwd_ex(lib, Hq=0, Hkv=0, q=0, k=0, v=0, o=0, lse=0) == 0
+    assert fwd_ex(lib, causal=0, Tq=500, Tk=200) != 1  # non-causal: Tq > Tk is fine
+    assert bwd_ex(lib, B=0) == 0
+    assert bwd_ex(lib, Tq=0, Tk=0) == 0

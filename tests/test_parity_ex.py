@@ -1,0 +1,155 @@
+"""Parity of the extended entry points (grouped KV heads, query offset, sliding window):
+fa_forward_ex / fa_backward_ex against the fp64 oracle's forward_ex / backward_ex on the same
+seeded bf16 inputs. Query row i sits at key position Tk - Tq + i; a window W keeps keys at
+positions >= position - W. Sizes span several tiles with ragged tails; the backward is fed
+the CUDA forward's O and LSE."""
+import numpy as np
+import pytest
+
+import oracle
+from parity_util import (assert_close_grad, assert_close_lse, assert_close_o, default_scale,
+                         to_dev, to_f64)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def env():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    import __graft_entry__
+    __graft_entry__.build()
+    from exact_io_aware_fa_gb300 import api
+    return api, oracle.oracle()
+
+
+# (B, Hq, Hkv, Tq, Tk, d, causal, window)
+CASES = [
+    (1, 4, 1, 200, 200, 64, False, -1),     # multi-query, non-causal
+    (2, 8, 2, 300, 300, 128, True, -1),     # grouped, causal
+    (1, 2, 2, 100, 513, 64, True, -1),      # chunked prefill: offset 413
+    (1, 4, 2, 1, 1000, 128, True, -1),      # decode: one query row
+    (1, 3, 1, 5, 300, 64, True, -1),        # a few query rows, offset not tile-aligned
+    (1, 2, 2, 130, 257, 64, False, -1),     # Tq != Tk, non-causal
+    (1, 2, 1, 600, 600, 64, True, 100),     # window inside one key tile
+    (1, 2, 2, 300, 700, 128, True, 0),      # window 0: each row sees its own key only
+    (1, 4, 2, 512, 512, 64, True, 256),     # window on a tile multiple
+    (1, 2, 2, 1000, 1000, 128, True, 129),  # window straddling two key tiles
+    (2, 4, 4, 384, 1200, 64, True, 300),    # offset and window together
+    (1, 8, 1, 257, 257, 128, True, 1000),   # window wider than the sequence
+]
+
+
+def ids(c):
+    B, Hq, Hkv, Tq, Tk, d, causal, w = c
+    return f"B{B}Hq{Hq}Hkv{Hkv}Tq{Tq}Tk{Tk}d{d}{'c' if causal else 'n'}w{w}"
+
+
+def run_fwd(api, bits, causal, window, scale):
+    import torch
+    q, k, v = (to_dev(bits[n]) for n in ("q", "k", "v"))
+    o, lse = api.forward(q, k, v, causal=causal, scale=scale, window=window)
+    torch.cuda.synchronize()
+    assert api.device_error() == 0
+    return q, k, v, o, lse
+
+
+@pytest.mark.parametrize("case", CASES, ids=ids)
+def test_forward_ex(env, case):
+    from exact_io_aware_fa_gb300 import synthetic
+    api, orc = env
+    B, Hq, Hkv, Tq, Tk, d, causal, window = case
+    bits = synthetic.attention_inputs_ex(B, Hq, Hkv, Tq, Tk, d, seed=Tq * 7 + Tk)
+    scale = default_scale(d)
+    _, _, _, o, lse = run_fwd(api, bits, causal, window, scale)
+    o_ref, lse_ref = orc.forward_ex(bits["q"], bits["k"], bits["v"], causal, scale, window)
+    small = Tq * Tk < 4096 or 0 <= window < 16
+    assert_close_o(to_f64(o), o_ref, ids(case), small_case=small)
+    assert_close_lse(to_f64(lse), lse_ref, ids(case))
+
+
+@pytest.mark.parametrize("case", CASES, ids=ids)
+def test_backward_ex(env, case):
+    import torch
+    from exact_io_aware_fa_gb300 import synthetic
+    api, orc = env
+    B, Hq, Hkv, Tq, Tk, d, causal, window = case
+    bits = synthetic.attention_inputs_ex(B, Hq, Hkv, Tq, Tk, d, seed=Tq * 7 + Tk + 1,
+                                         with_dout=True)
+    scale = default_scale(d)
+    q, k, v, o, lse = run_fwd(api, bits, causal, window, scale)
+    do = to_dev(bits["do"])
+    dq, dk, dv = api.backward(q, k, v, o, lse, do, causal=causal, scale=scale, window=window)
+    torch.cuda.synchronize()
+    assert api.device_error() == 0
+    ref = orc.backward_ex(bits["q"], bits["k"], bits["v"], bits["do"], causal, scale, window)
+    for name, a, b in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
+        assert_close_grad(to_f64(a), b, name, ids(case))
+
+
+def test_mha_call_matches_ex_call(env):
+    """fa_forward / fa_backward are the extended calls with Hq = Hkv, Tq = Tk, no window:
+    bit-identical results."""
+    import torch
+    from exact_io_aware_fa_gb300 import synthetic
+    api, _ = env
+    B, H, N, d = 1, 3, 333, 64
+    bits = synthetic.attention_inputs(B, H, N, d, seed=5, with_dout=True)
+    q, k, v, do = (to_dev(bits[n]) for n in ("q", "k", "v", "do"))
+    scale = default_scale(d)
+    o1 = torch.empty_like(q)
+    l1 = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    st = api.forward_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o1.data_ptr(), l1.data_ptr(),
+                         B, H, N, d, 1, scale, 0)
+    assert st == api.FA_OK
+    o2, l2 = api.forward(q, k, v, causal=True, scale=scale)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    g1 = [torch.empty_like(q) for _ in range(3)]
+    st = api.backward_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o1.data_ptr(), l1.data_ptr(),
+                          do.data_ptr(), *(t.data_ptr() for t in g1), B, H, N, d, 1, scale, 0, 0)
+    assert st == api.FA_OK
+    g2 = api.backward(q, k, v, o2, l2, do, causal=True, scale=scale)
+    torch.cuda.synchronize()
+    for a, b in zip(g1, g2):
+        assert torch.equal(a, b)
+
+
+def test_no_query_rows_zeroes_kv_gradients(env):
+    """Tq = 0: nothing attends to the keys, so dK = dV = 0 (written, not left as they were)."""
+    import torch
+    api, _ = env
+    B, H, Tk, d = 1, 2, 300, 64
+    dk = torch.full((B, H, Tk, d), 3.0, dtype=torch.bfloat16, device="cuda")
+    dv = torch.full_like(dk, 3.0)
+    st = api.backward_ex_raw(0, 0, 0, 0, 0, 0, 0, dk.data_ptr(), dv.data_ptr(), B, H, H, 0, Tk, d,
+                             1, -1, 0.125, 0, 0)
+    assert st == api.FA_OK
+    torch.cuda.synchronize()
+    assert int(torch.count_nonzero(dk)) == 0 and int(torch.count_nonzero(dv)) == 0
+
+
+def test_window_covers_unseen_key_tiles(env):
+    """Key tiles that no query row can see (window far behind a short query block) get zero
+    gradient from their CTA, which runs no step."""
+    import torch
+    from exact_io_aware_fa_gb300 import synthetic
+    api, orc = env
+    B, Hq, Hkv, Tq, Tk, d, window = 1, 2, 1, 64, 1024, 128, 50
+    bits = synthetic.attention_inputs_ex(B, Hq, Hkv, Tq, Tk, d, seed=91, with_dout=True)
+    scale = default_scale(d)
+    q, k, v, o, lse = run_fwd(api, bits, True, window, scale)
+    do = to_dev(bits["do"])
+    dk = torch.full_like(k, 7.0)
+    dv = torch.full_like(v, 7.0)
+    dq, dk, dv = api.backward(q, k, v, o, lse, do, causal=True, scale=scale, window=window,
+                              dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    assert api.device_error() == 0
+    first_seen = Tk - Tq - window
+    assert int(torch.count_nonzero(dk[:, :, : first_seen // 128 * 128])) == 0
+    assert int(torch.count_nonzero(dv[:, :, : first_seen // 128 * 128])) == 0
+    ref = orc.backward_ex(bits["q"], bits["k"], bits["v"], bits["do"], True, scale, window)
+    for name, a, b in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
+        assert_close_grad(to_f64(a), b, name, "unseen tiles")
