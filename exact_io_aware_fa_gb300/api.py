@@ -218,9 +218,13 @@ def backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = 
     _check_tensor("dq", dq, q.shape)
     _check_tensor("dk", dk, k.shape)
     _check_tensor("dv", dv, v.shape)
+    need = backward_workspace_bytes(B, Hq, Tq, d)
+    if workspace is None and need > 0:
+        # torch's caching allocator keeps the block between calls (a stream-ordered
+        # allocation inside the library would be returned to the driver at every sync)
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_ptr = 0
     if workspace is not None:
-        need = backward_workspace_bytes(B, Hq, Tq, d)
         if workspace.numel() * workspace.element_size() < need:
             raise ValueError(f"workspace needs {need} bytes")
         ws_ptr = workspace.data_ptr()

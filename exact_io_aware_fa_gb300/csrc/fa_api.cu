@@ -155,9 +155,11 @@ fa_status check_shape(int B, int Hq, int Hkv, int Tq, int Tk, int d, int causal,
     return FA_OK;
 }
 
+// Backward workspace: two 32-byte fold records per (padded) query row, then the fp32 dQ
+// accumulator.
 size_t workspace_bytes(long long bhq, long long tq, int d) {
     const size_t npad = ((size_t)tq + 127) / 128 * 128;
-    return 2 * (size_t)bhq * npad * sizeof(float) + (size_t)bhq * npad * (size_t)d * sizeof(float);
+    return 2 * (size_t)bhq * npad * 32u + (size_t)bhq * npad * (size_t)d * sizeof(float);
 }
 
 constexpr float kLog2e = 1.4426950408889634074f;
@@ -281,6 +283,7 @@ fa_status fa_backward_ex(const void* q, const void* k, const void* v, const void
     if ((st = make_map(&a.tm_dk, dk, sh.BHkv, Tk, d, 128)) != FA_OK) return st;
     if ((st = make_map(&a.tm_dv, dv, sh.BHkv, Tk, d, 128)) != FA_OK) return st;
     if ((st = get_err_ptr(&a.err)) != FA_OK) return st;
+    if ((st = get_num_sms(&a.num_sms)) != FA_OK) return st;
     const size_t ws_bytes = workspace_bytes(sh.BHq, Tq, d);
     void* ws = workspace;
     bool owned = false;
@@ -293,8 +296,8 @@ fa_status fa_backward_ex(const void* q, const void* k, const void* v, const void
     a.dout = dout;
     a.lse = lse;
     a.dq = dq;
-    a.stats = static_cast<float*>(ws);
-    a.dq_acc = static_cast<float*>(ws) + 2 * (size_t)sh.BHq * (size_t)Npad;
+    a.folds = ws;
+    a.dq_acc = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + 2 * (size_t)sh.BHq * (size_t)Npad * 32u);
     if ((st = make_map(&a.tm_dqacc, a.dq_acc, sh.BHq, Npad, d, q_rows, true)) != FA_OK) {
         if (owned) cudaFreeAsync(ws, s);
         return st;

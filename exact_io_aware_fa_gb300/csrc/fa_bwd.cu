@@ -43,16 +43,43 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     }
 }
 
-constexpr float kLog2e = 1.4426950408889634074f;
-
 // ----------------------------------------------------------------------------------------
 // Preprocess: D/8 threads per row, 16-byte loads; 256 threads cover 2048/D rows.
+//
+// Per query row it writes two "fold" records that let the main kernel's MMAs subtract the row
+// statistics themselves: S'^T = K Q^T + 1 * (-LSE/scale) and dP'^T = V dO^T + 1 * (-D), added as
+// one more K=16 MMA against a constant tile of ones. A record is 16 bf16 (k = 0..15): the value
+// split exactly into three bf16 parts (hi + mid + lo) at k = 0, 1, 2, zeros elsewhere, stored in
+// the tcgen05 no-swizzle K-major layout (8-row core matrices of 16-byte rows; the two K halves
+// 128 bytes apart, 8-row groups 256 bytes apart), so one bulk copy of a query block's records
+// lands in shared memory ready for the MMA.
 // ----------------------------------------------------------------------------------------
+// Exact three-part bf16 split of v: hi = bf16(v), mid = bf16(v - hi), lo = v - hi - mid (each
+// difference is exact in fp32, and lo has at most 8 significant bits).
+__device__ __forceinline__ uint4 fold_record(float v) {
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    const float r1 = v - __bfloat162float(hi);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(mid);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(r2);
+    uint4 w;
+    w.x = (uint32_t)__bfloat16_as_ushort(hi) | ((uint32_t)__bfloat16_as_ushort(mid) << 16);
+    w.y = (uint32_t)__bfloat16_as_ushort(lo);
+    w.z = 0u;
+    w.w = 0u;
+    return w;
+}
+
+// Byte offset of row n's record (first K half) in a head's fold array.
+__device__ __forceinline__ size_t fold_offset(size_t bh, int Npad, int n) {
+    return ((bh * (size_t)(Npad / 8) + (size_t)(n / 8)) * 256u) + (size_t)(n % 8) * 16u;
+}
+
 template <int D>
 __global__ void __launch_bounds__(256)
 fa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
-                  const float* __restrict__ lse, float* __restrict__ stats,
-                  float* __restrict__ dq_acc, int N, int Npad, int BH) {
+                  const float* __restrict__ lse, uint8_t* __restrict__ folds,
+                  float* __restrict__ dq_acc, int N, int Npad, int BH, float inv_scale) {
     constexpr int TPR = D / 8;            // threads per row
     constexpr int RPB = 256 / TPR;        // rows per block
     const int sub = threadIdx.x % TPR;
@@ -79,9 +106,17 @@ fa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __re
     for (int off = TPR / 2; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
     if (!valid_row) return;
     if (sub == 0) {
-        const size_t si = (size_t)bh * Npad + n;
-        stats[si] = (n < N) ? lse[(size_t)bh * N + n] * kLog2e : __int_as_float(0x7f800000);
-        stats[(size_t)BH * Npad + si] = (n < N) ? dot : 0.f;
+        // Padded rows get a large finite negative shift (their P must be 0; a finite value keeps
+        // the zero products of the fold MMA free of 0 * inf).
+        const float v = (n < N) ? -lse[(size_t)bh * N + n] * inv_scale : -0x1.0p100f;
+        const size_t off = fold_offset((size_t)bh, Npad, n);
+        uint8_t* lf = folds + off;
+        uint8_t* df = folds + (size_t)BH * Npad * 32u + off;
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(lf) = fold_record(v);
+        *reinterpret_cast<uint4*>(lf + 128) = z;
+        *reinterpret_cast<uint4*>(df) = fold_record((n < N) ? -dot : 0.f);
+        *reinterpret_cast<uint4*>(df + 128) = z;
     }
     float4* acc = reinterpret_cast<float4*>(dq_acc + ((size_t)bh * Npad + n) * D + sub * 8);
     acc[0] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -118,7 +153,7 @@ fa_bwd_dq_kernel(const float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ d
 // Problem shape of the backward: as the forward (query head bh_q reads KV head bh_q / group,
 // query row i at key position offset + i, optional window), seen from a key tile.
 struct BwdShape {
-    int Tq, Tk, Npad, Hq, Hkv, group, offset, window, BHq, nkb;
+    int Tq, Tk, Npad, Hq, Hkv, group, offset, window, BHq, BHkv, nkb, kb_major;
 };
 
 template <int D>
@@ -130,9 +165,9 @@ struct BwdCfg {
     static constexpr uint32_t KCHUNK = 128u * 128u;   // 128 rows x 64 cols
     static constexpr uint32_t QTILE = (uint32_t)BMQ * D * 2u;
     static constexpr uint32_t QCHUNK = (uint32_t)BMQ * 128u;  // BMQ rows x 64 cols
-    static constexpr uint32_t STAT_BYTES = (uint32_t)BMQ * 4u;
-    // stage: [Q][dO][LSE2][Dvec], padded to 1024
-    static constexpr uint32_t STAGE_BYTES = ((2 * QTILE + 2 * STAT_BYTES) + 1023u) / 1024u * 1024u;
+    static constexpr uint32_t FOLD_BYTES = (uint32_t)BMQ * 32u;  // fold records of a query block
+    // stage: [Q][dO][-LSE/scale fold][-D fold], padded to 1024
+    static constexpr uint32_t STAGE_BYTES = ((2 * QTILE + 2 * FOLD_BYTES) + 1023u) / 1024u * 1024u;
     // dS tile: 128 key rows, BMQ queries contiguous per row, in 64-query (128-byte) regions
     static constexpr uint32_t DS_BYTES = (uint32_t)BMQ * 128u * 2u;
     static constexpr uint32_t DSREG = 128u * 128u;           // one 64-query region
@@ -143,7 +178,8 @@ struct BwdCfg {
     static constexpr uint32_t OFF_ST = OFF_V + KTILE;
     static constexpr uint32_t OFF_DS = OFF_ST + NQS * STAGE_BYTES;
     static constexpr uint32_t OFF_DQS = OFF_DS + 2 * DS_BYTES;
-    static constexpr uint32_t OFF_BAR = OFF_DQS + DQS_BYTES;
+    static constexpr uint32_t OFF_ONES = OFF_DQS + DQS_BYTES;  // ones tile [128 keys x 16]
+    static constexpr uint32_t OFF_BAR = OFF_ONES + 128u * 32u;
     static constexpr uint32_t SMEM_BYTES = OFF_BAR + 512 + 1024;
     static constexpr int THREADS = 512;
     // TMEM columns. d=128: dV[0,128) dK[128,256) S^T[256,320) dP^T[320,384) dQ^T[384,448)
@@ -173,7 +209,7 @@ __global__ void __launch_bounds__(512, 1)
 fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
               const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
-              const __grid_constant__ CUtensorMap tm_dqacc, const float* __restrict__ stats,
+              const __grid_constant__ CUtensorMap tm_dqacc, const uint8_t* __restrict__ folds,
               const BwdShape sh, const float c, const float scale, int* err) {
     using C = BwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -187,8 +223,11 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     // group and, for each, the query steps whose rows can see some key of the tile: from the
     // causal diagonal (query position offset + q >= key) to the window's reach (position -
     // window <= key). A tile no query sees has no steps and stores zero gradients.
-    const int bh_kv = blockIdx.x / sh.nkb;
-    const int kb = blockIdx.x % sh.nkb;
+    // CTA order: head by head (neighbouring CTAs share their query heads' Q/dO in L2), or, for
+    // short causal launches, key tile by key tile (the costliest tiles, whose queries reach
+    // back to the diagonal, start first instead of a head's heavy tiles being left for last).
+    const int bh_kv = sh.kb_major ? (int)(blockIdx.x % (uint32_t)sh.BHkv) : (int)(blockIdx.x / (uint32_t)sh.nkb);
+    const int kb = sh.kb_major ? (int)(blockIdx.x / (uint32_t)sh.BHkv) : (int)(blockIdx.x % (uint32_t)sh.nkb);
     const int key0 = kb * C::KT;
     const int nq_total = (sh.Tq + C::BMQ - 1) / C::BMQ;
     const int i0 = CAUSAL ? max(0, key0 - sh.offset) / C::BMQ : 0;
@@ -242,6 +281,16 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         ptx::tmem_alloc(ptx::smem_addr(&bars->tmem_base), 512);
         ptx::tmem_relinquish();
     }
+    if (warp >= 4 && warp < 8) {
+        // Ones tile [128 keys x 16], no-swizzle K-major: key r has 1 at k = 0, 1, 2 (the fold
+        // records' three parts) and 0 elsewhere.
+        const int r = tid - 128;
+        uint8_t* row = smem + C::OFF_ONES + (uint32_t)(r / 8) * 256u + (uint32_t)(r % 8) * 16u;
+        const uint32_t one = 0x3F80u;  // bf16 1.0
+        *reinterpret_cast<uint4*>(row) = make_uint4(one | (one << 16), one, 0u, 0u);
+        *reinterpret_cast<uint4*>(row + 128) = make_uint4(0u, 0u, 0u, 0u);
+        ptx::fence_proxy_async_smem();
+    }
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
@@ -274,16 +323,16 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 const int bhq = cur.bhq;
                 const uint32_t b_q = ptx::smem_addr(&bars->q_full[st]);
                 const uint32_t base = s_st + st * C::STAGE_BYTES;
-                ptx::mbar_arrive_expect_tx(b_q, 2 * C::QTILE + 2 * C::STAT_BYTES);
+                ptx::mbar_arrive_expect_tx(b_q, 2 * C::QTILE + 2 * C::FOLD_BYTES);
                 for (int ch = 0; ch < D / 64; ++ch) {
                     ptx::tma_load_3d_hint(base + ch * C::QCHUNK, &tm_q, b_q, ch * 64, q0, bhq, pol_keep);
                     ptx::tma_load_3d_hint(base + C::QTILE + ch * C::QCHUNK, &tm_do, b_q, ch * 64, q0,
                                           bhq, pol_keep);
                 }
-                const float* lse2 = stats + (size_t)bhq * sh.Npad + q0;
-                const float* dvec = stats + (size_t)sh.BHq * sh.Npad + (size_t)bhq * sh.Npad + q0;
-                ptx::bulk_load(base + 2 * C::QTILE, lse2, C::STAT_BYTES, b_q);
-                ptx::bulk_load(base + 2 * C::QTILE + C::STAT_BYTES, dvec, C::STAT_BYTES, b_q);
+                const uint8_t* lf = folds + ((size_t)bhq * (size_t)(sh.Npad / 8) + (size_t)(q0 / 8)) * 256u;
+                const uint8_t* df = lf + (size_t)sh.BHq * sh.Npad * 32u;
+                ptx::bulk_load(base + 2 * C::QTILE, lf, C::FOLD_BYTES, b_q);
+                ptx::bulk_load(base + 2 * C::QTILE + C::FOLD_BYTES, df, C::FOLD_BYTES, b_q);
                 ++issued;
             }
             drain_wait(b_kv, 0);
@@ -306,6 +355,9 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             const uint64_t st_mn = ptx::sdesc_sw128(s_st, C::QCHUNK, 1024);
             const uint64_t ds_kmaj = ptx::sdesc_sw128(s_ds, 16, 1024);
             const uint64_t ds_mn = ptx::sdesc_sw128(s_ds, C::DSREG, 1024);
+            // fold MMAs: A = ones tile, B = a stage's fold records (both no-swizzle K-major)
+            const uint64_t ones_d = ptx::sdesc_noswz(ptx::smem_addr(smem + C::OFF_ONES), 128, 256);
+            const uint64_t fold_d = ptx::sdesc_noswz(s_st + 2 * C::QTILE, 128, 256);
             auto issue_s_dp = [&](int si) {
                 const uint32_t st_off = (uint32_t)(si % C::NQS) * C::STAGE_BYTES;
                 const uint64_t qd = ptx::sdesc_add(st_kmaj, st_off);
@@ -318,6 +370,8 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     ptx::mma_ss(tbase + C::S_COL, ptx::sdesc_add(k_kmaj, koff), ptx::sdesc_add(qd, qoff),
                                 idesc_s, kk > 0);
                 }
+                // S'^T = S^T + (-LSE/scale) per query column
+                ptx::mma_ss(tbase + C::S_COL, ones_d, ptx::sdesc_add(fold_d, st_off), idesc_s, 1u);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t koff = (kk >> 2) * C::KCHUNK + (kk & 3) * 32;
@@ -325,6 +379,9 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     ptx::mma_ss(tbase + C::DP_COL, ptx::sdesc_add(v_kmaj, koff), ptx::sdesc_add(dod, qoff),
                                 idesc_s, kk > 0);
                 }
+                // dP'^T = dP^T + (-D) per query column
+                ptx::mma_ss(tbase + C::DP_COL, ones_d,
+                            ptx::sdesc_add(fold_d, st_off + C::FOLD_BYTES), idesc_s, 1u);
                 ptx::mma_commit(ptx::smem_addr(&bars->s_full));
                 }
                 __syncwarp();
@@ -430,16 +487,11 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         for (int si = 0; si < nsteps; ++si, next_step(cur)) {
             const int st = si % C::NQS;
             const int q0 = cur.qi * C::BMQ;
+            // S'^T and dP'^T already carry the row statistics (fold MMAs): nothing else to read.
             ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->s_full), (uint32_t)si & 1u,
                                                     abort_flag, err, kDevTimeoutMma));
             if (!ok) break;
-            ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->q_full[st]),
-                                                    (uint32_t)(si / C::NQS) & 1u, abort_flag, err,
-                                                    kDevTimeoutLoad));
-            if (!ok) break;
             ptx::tc_fence_after();
-            const float* lse2 = reinterpret_cast<const float*>(smem + C::OFF_ST + st * C::STAGE_BYTES + 2 * C::QTILE);
-            const float* dvec = lse2 + C::BMQ;
             uint8_t* dsbuf = smem + C::OFF_DS + (si & 1) * C::DS_BYTES;
             // key visible to query q iff (!causal || key <= p) && (no window || key >= p - window),
             // p = offset + q; elementwise masking only where the step crosses either edge.
@@ -463,11 +515,10 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 #pragma unroll
                 for (int j = 0; j < 32; j += 4) {
                     const int qi = 32 * cc + j;
-                    const float4 L = *reinterpret_cast<const float4*>(lse2 + qi);  // broadcast
-                    const float4 Dq = *reinterpret_cast<const float4*>(dvec + qi);
+                    // x = c * S' = c * S - LSE * log2(e)
                     float x0, x1, x2, x3;
-                    ptx::ffma2(x0, x1, __uint_as_float(sv[j]), __uint_as_float(sv[j + 1]), c, c, -L.x, -L.y);
-                    ptx::ffma2(x2, x3, __uint_as_float(sv[j + 2]), __uint_as_float(sv[j + 3]), c, c, -L.z, -L.w);
+                    ptx::fmul2(x0, x1, __uint_as_float(sv[j]), __uint_as_float(sv[j + 1]), c, c);
+                    ptx::fmul2(x2, x3, __uint_as_float(sv[j + 2]), __uint_as_float(sv[j + 3]), c, c);
                     float pe0 = ptx::ex2_approx(x0), pe1 = ptx::ex2_approx(x1);
                     float pe2 = ptx::ex2_approx(x2), pe3 = ptx::ex2_approx(x3);
                     if (need_mask) {
@@ -478,11 +529,10 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                         if (dp + 2u > vspan) pe2 = 0.f;
                         if (dp + 3u > vspan) pe3 = 0.f;
                     }
-                    float y0, y1, y2, y3, d0, d1, d2, d3;
-                    ptx::fadd2(y0, y1, __uint_as_float(dpv[j]), __uint_as_float(dpv[j + 1]), -Dq.x, -Dq.y);
-                    ptx::fadd2(y2, y3, __uint_as_float(dpv[j + 2]), __uint_as_float(dpv[j + 3]), -Dq.z, -Dq.w);
-                    ptx::fmul2(d0, d1, pe0, pe1, y0, y1);
-                    ptx::fmul2(d2, d3, pe2, pe3, y2, y3);
+                    // dS = P (dP - D) = P dP'
+                    float d0, d1, d2, d3;
+                    ptx::fmul2(d0, d1, pe0, pe1, __uint_as_float(dpv[j]), __uint_as_float(dpv[j + 1]));
+                    ptx::fmul2(d2, d3, pe2, pe3, __uint_as_float(dpv[j + 2]), __uint_as_float(dpv[j + 3]));
                     pk[j / 2] = ptx::pack_bf16x2(pe0, pe1);
                     pk[j / 2 + 1] = ptx::pack_bf16x2(pe2, pe3);
                     dk[j / 2] = ptx::pack_bf16x2(d0, d1);
@@ -673,7 +723,7 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t stream) {
         if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
         fa_bwd_pre_kernel<D><<<(unsigned)blocks, 256, 0, stream>>>(
             static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.lse,
-            a.stats, a.dq_acc, a.Tq, a.Npad, a.BHq);
+            static_cast<uint8_t*>(a.folds), a.dq_acc, a.Tq, a.Npad, a.BHq, 1.0f / a.scale);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -693,11 +743,16 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t stream) {
         sh.offset = a.Tk - a.Tq;
         sh.window = a.window;
         sh.BHq = a.BHq;
+        sh.BHkv = a.BHkv;
         sh.nkb = (a.Tk + C::KT - 1) / C::KT;
         const long long blocks = (long long)sh.nkb * a.BHkv;
         if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+        // Key-tile-major order pays when the launch is a few waves of very unequal CTAs (causal)
+        // and costs L2 reuse when it is many waves; measured crossover between 7 and 13 waves.
+        sh.kb_major = (CAUSAL && blocks <= 8LL * a.num_sms) ? 1 : 0;
         kern<<<(unsigned)blocks, C::THREADS, C::SMEM_BYTES, stream>>>(
-            a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dk, a.tm_dv, a.tm_dqacc, a.stats, sh, a.c,
+            a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dk, a.tm_dv, a.tm_dqacc,
+            static_cast<const uint8_t*>(a.folds), sh, a.c,
             a.scale, a.err);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;

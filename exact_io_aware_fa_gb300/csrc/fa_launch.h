@@ -27,17 +27,19 @@ struct BwdLaunch {
     CUtensorMap tm_q, tm_do;              // [B*Hq, Tq, d] loads, box {64, query rows, 1}
     CUtensorMap tm_k, tm_v;               // [B*Hkv, Tk, d] loads, box {64, 128, 1}
     CUtensorMap tm_dk, tm_dv;             // [B*Hkv, Tk, d] stores, box {64, 128, 1}
-    CUtensorMap tm_dqacc;                 // fp32 [B*H, Npad, d] accumulator, box {32, rows, 1}
-    const void* o;                        // bf16 [B*H, N, d]
-    const void* dout;                     // bf16 [B*H, N, d]
+    CUtensorMap tm_dqacc;                 // fp32 [B*Hq, Npad, d] accumulator, box {32, rows, 1}
+    const void* o;                        // bf16 [B*Hq, Tq, d]
+    const void* dout;                     // bf16 [B*Hq, Tq, d]
     const float* lse;                     // fp32 [B*Hq, Tq]
     void* dq;                             // bf16 [B*Hq, Tq, d]
-    float* stats;                         // workspace: [B*Hq, Npad] (LSE*log2e) then (D)
+    void* folds;                          // workspace: per query row, 32-byte records of
+                                          // -LSE/scale then of -D ([B*Hq, Npad] each)
     float* dq_acc;                        // workspace: fp32 [B*Hq, Npad, d]
     int Tq, Tk, Npad, Hq, Hkv, BHq, BHkv, d, window;
     float scale;
     float c;                              // scale * log2(e)
     int* err;
+    int num_sms;                          // SMs of the device (CTA order choice)
 };
 
 cudaError_t launch_backward(const BwdLaunch& a, bool causal, cudaStream_t stream);

@@ -253,6 +253,18 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
     return d;
 }
 
+// Shared-memory matrix descriptor, no swizzle (layout 0), K-major: 8-row core matrices of
+// 16-byte rows (128 contiguous bytes each); `lbo` = bytes between the two K-adjacent core
+// matrices of a 16-element K slice, `sbo` = bytes between consecutive 8-row groups.
+__device__ __forceinline__ uint64_t sdesc_noswz(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
+}
+
 // Advance a descriptor's start address by `bytes` (a multiple of 16): the start field holds
 // addr >> 4 in bits 0-13 and shared addresses stay below 256 KB, so the add never carries out
 // of the field. Lets the MMA issuer build each descriptor once and step it with constants.

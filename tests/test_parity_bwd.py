@@ -26,11 +26,17 @@ def run_fwd_bwd(api, bits, causal, scale, workspace=True):
     import torch
     q, k, v, do = (to_dev(bits[n]) for n in ("q", "k", "v", "do"))
     o, lse = api.forward(q, k, v, causal=causal, scale=scale)
-    ws = None
+    B, H, N, d = q.shape
     if workspace:
-        B, H, N, d = q.shape
         ws = torch.empty(api.backward_workspace_bytes(B, H, N, d), dtype=torch.uint8, device="cuda")
-    dq, dk, dv = api.backward(q, k, v, o, lse, do, causal=causal, scale=scale, workspace=ws)
+        dq, dk, dv = api.backward(q, k, v, o, lse, do, causal=causal, scale=scale, workspace=ws)
+    else:
+        # raw call with workspace = NULL (the Python wrapper always passes a buffer)
+        dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+        st = api.backward_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                              do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d,
+                              int(causal), scale, 0, torch.cuda.current_stream().cuda_stream)
+        assert st == api.FA_OK
     torch.cuda.synchronize()
     assert api.device_error() == 0
     return to_f64(dq), to_f64(dk), to_f64(dv)
