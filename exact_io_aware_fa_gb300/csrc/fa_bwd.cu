@@ -160,7 +160,8 @@ template <int D>
 struct BwdCfg {
     static constexpr int KT = 128;                    // keys per CTA
     static constexpr int BMQ = (D == 128) ? 64 : 128; // query rows per step
-    static constexpr int NQS = 2;                     // Q/dO ring depth
+    static constexpr int NQS = 3;                     // Q/dO ring depth
+    static constexpr int NDS = 1;                     // dS buffers
     static constexpr uint32_t KTILE = 128u * D * 2u;  // K or V tile bytes
     static constexpr uint32_t KCHUNK = 128u * 128u;   // 128 rows x 64 cols
     static constexpr uint32_t QTILE = (uint32_t)BMQ * D * 2u;
@@ -177,10 +178,12 @@ struct BwdCfg {
     static constexpr uint32_t OFF_V = OFF_K + KTILE;
     static constexpr uint32_t OFF_ST = OFF_V + KTILE;
     static constexpr uint32_t OFF_DS = OFF_ST + NQS * STAGE_BYTES;
-    static constexpr uint32_t OFF_DQS = OFF_DS + 2 * DS_BYTES;
+    static constexpr uint32_t OFF_DQS = OFF_DS + NDS * DS_BYTES;
     static constexpr uint32_t OFF_ONES = OFF_DQS + DQS_BYTES;  // ones tile [128 keys x 16]
     static constexpr uint32_t OFF_BAR = OFF_ONES + 128u * 32u;
     static constexpr uint32_t SMEM_BYTES = OFF_BAR + 512 + 1024;
+    static_assert(NQS <= 3 && NDS >= 1 && NDS <= 2, "barrier arrays");
+    static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
     static constexpr int THREADS = 512;
     // TMEM columns. d=128: dV[0,128) dK[128,256) S^T[256,320) dP^T[320,384) dQ^T[384,448)
     // P^T[448,480). d=64: dV[0,64) dK[64,128) S^T[128,256) dP^T[256,384) dQ[384,448) P^T[448,512).
@@ -194,9 +197,9 @@ struct BwdCfg {
 
 struct BwdBars {
     uint64_t kv_full;
-    uint64_t q_full[2], q_empty[2];
+    uint64_t q_full[3], q_empty[3];
     uint64_t s_full, s_free, p_ready, mma_done;
-    uint64_t ds_free[2];
+    uint64_t ds_free[2];  // one per dS buffer (NDS <= 2)
     uint64_t dq_full, dq_free;
     uint64_t final_bar;
     uint32_t tmem_base;
@@ -214,6 +217,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     using C = BwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
+    static_assert(sizeof(BwdBars) <= 512, "barrier block");
     BwdBars* bars = reinterpret_cast<BwdBars*>(smem + C::OFF_BAR);
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -262,8 +266,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         ptx::mbar_init(ptx::smem_addr(&bars->s_free), 256);
         ptx::mbar_init(ptx::smem_addr(&bars->p_ready), 256);
         ptx::mbar_init(ptx::smem_addr(&bars->mma_done), 1);
-        ptx::mbar_init(ptx::smem_addr(&bars->ds_free[0]), 1);
-        ptx::mbar_init(ptx::smem_addr(&bars->ds_free[1]), 1);
+        for (int b = 0; b < C::NDS; ++b) ptx::mbar_init(ptx::smem_addr(&bars->ds_free[b]), 1);
         ptx::mbar_init(ptx::smem_addr(&bars->dq_full), 1);
         ptx::mbar_init(ptx::smem_addr(&bars->dq_free), 128);
         ptx::mbar_init(ptx::smem_addr(&bars->final_bar), 2);
@@ -419,7 +422,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 ptx::tc_fence_after();
                 // dV += P^T dO (A = P^T in TMEM) and dK += dS^T Q (A = dS^T, K-major in smem).
                 const uint32_t st_off = (uint32_t)st * C::STAGE_BYTES;
-                const uint32_t ds_off = (uint32_t)(si & 1) * C::DS_BYTES;
+                const uint32_t ds_off = (uint32_t)(si % C::NDS) * C::DS_BYTES;
                 const uint64_t do_mn = ptx::sdesc_add(st_mn, st_off + C::QTILE);
                 const uint64_t q_mn = ptx::sdesc_add(st_mn, st_off);
                 const uint64_t dsk = ptx::sdesc_add(ds_kmaj, ds_off);
@@ -459,7 +462,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     }
                 }
                 ptx::mma_commit(ptx::smem_addr(&bars->dq_full));
-                ptx::mma_commit(ptx::smem_addr(&bars->ds_free[si & 1]));
+                ptx::mma_commit(ptx::smem_addr(&bars->ds_free[si % C::NDS]));
                 }
                 __syncwarp();
             }
@@ -492,7 +495,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                                                     abort_flag, err, kDevTimeoutMma));
             if (!ok) break;
             ptx::tc_fence_after();
-            uint8_t* dsbuf = smem + C::OFF_DS + (si & 1) * C::DS_BYTES;
+            uint8_t* dsbuf = smem + C::OFF_DS + (si % C::NDS) * C::DS_BYTES;
             // key visible to query q iff (!causal || key <= p) && (no window || key >= p - window),
             // p = offset + q; elementwise masking only where the step crosses either edge.
             const int p0 = sh.offset + q0;
@@ -546,10 +549,10 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                                                                 err, kDevTimeoutMma));
                         if (!ok) break;
                     }
-                    if (si >= 2) {
-                        // dK(si-2) and dQ(si-2) must have read this dS buffer.
-                        ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->ds_free[si & 1]),
-                                                                (uint32_t)((si >> 1) - 1) & 1u,
+                    if (si >= C::NDS) {
+                        // dK and dQ of step si - NDS must have read this dS buffer.
+                        ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->ds_free[si % C::NDS]),
+                                                                (uint32_t)(si / C::NDS - 1) & 1u,
                                                                 abort_flag, err, kDevTimeoutMma));
                         if (!ok) break;
                     }
