@@ -237,5 +237,66 @@ def _ex_methods():
 _ex_methods()
 
 
+# ---- flash-decoding partials and their merge --------------------------------------------
+#
+# "15. FlashAttention" (inference.shantanugoel.com), section "Decode is different:
+# flash-decoding": the key sequence is cut into chunks; each chunk i yields a partial
+# (m_i, l_i, a_i) -- the running max, the sum of exp(s - m_i) and the unnormalised accumulator
+# sum of exp(s - m_i) v over the chunk's visible keys -- and the partials combine by
+#   m = max_i m_i,  l = sum_i exp(m_i - m) l_i,  a = sum_i exp(m_i - m) a_i,  O = a / l,
+# a rule that is associative (any grouping gives the same triple). Plain numpy in fp64, for
+# small cases; the visibility rule is that of forward_ex.
+
+def _visible_ex(pos: int, j: int, causal: bool, window: int) -> bool:
+    if causal and j > pos:
+        return False
+    if window >= 0 and j < pos - window:
+        return False
+    return True
+
+
+def partials_f64(q, k, v, causal: bool, scale: float, window: int, bounds):
+    """Partials (m, l, a) of every key chunk [bounds[i], bounds[i+1]) for every query row.
+
+    Returns m [C, B, Hq, Tq], l [C, B, Hq, Tq], a [C, B, Hq, Tq, d] (m = -inf, l = 0, a = 0
+    for a chunk in which the row sees no key)."""
+    q, k, v = (np.asarray(x, dtype=np.float64) for x in (q, k, v))
+    B, Hq, Hkv, Tq, Tk, d = _ex_shapes(q, k)
+    group = Hq // Hkv
+    C = len(bounds) - 1
+    m = np.full((C, B, Hq, Tq), -np.inf)
+    l = np.zeros((C, B, Hq, Tq))
+    a = np.zeros((C, B, Hq, Tq, d))
+    for b in range(B):
+        for h in range(Hq):
+            kh, vh = k[b, h // group], v[b, h // group]
+            for i in range(Tq):
+                pos = Tk - Tq + i
+                for c in range(C):
+                    js = [j for j in range(bounds[c], bounds[c + 1])
+                          if _visible_ex(pos, j, causal, window)]
+                    if not js:
+                        continue
+                    s = scale * (kh[js] @ q[b, h, i])
+                    m[c, b, h, i] = s.max()
+                    e = np.exp(s - m[c, b, h, i])
+                    l[c, b, h, i] = e.sum()
+                    a[c, b, h, i] = e @ vh[js]
+    return m, l, a
+
+
+def merge_partials(m, l, a):
+    """Combine partials along axis 0 by the flash-decoding rule; returns the merged partial
+    (m, l, a) and O = a / l, LSE = m + ln l. A row whose chunks all lack keys is an error."""
+    m, l, a = (np.asarray(x, dtype=np.float64) for x in (m, l, a))
+    mm = m.max(axis=0)
+    if np.any(np.isneginf(mm)):
+        raise NoVisibleKey("merge: a query row has no visible key in any chunk")
+    w = np.where(np.isneginf(m), 0.0, np.exp(m - mm[None]))
+    ll = (w * l).sum(axis=0)
+    aa = (w[..., None] * a).sum(axis=0)
+    return mm, ll, aa, aa / ll[..., None], mm + np.log(ll)
+
+
 def oracle(threads: int | None = None) -> Oracle:
     return Oracle(0, threads)

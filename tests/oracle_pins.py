@@ -14,6 +14,8 @@ import os
 
 import numpy as np
 
+import oracle
+
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
 
@@ -497,6 +499,44 @@ def check_ex_backward_finite_differences(orc):
             assert err <= 1e-6, (name, window, err)
 
 
+def check_split_merge_equals_unsplit(orc):
+    """Flash-decoding: partials over any chunking of the keys (including empty chunks and
+    chunks some rows cannot see) merge to the unsplit attention ("15. FlashAttention",
+    section "Decode is different: flash-decoding")."""
+    r = _rng(40)
+    B, Hkv, group, Tq, Tk, d = 1, 2, 2, 6, 23, 3
+    q = r.standard_normal((B, Hkv * group, Tq, d))
+    k = r.standard_normal((B, Hkv, Tk, d))
+    v = r.standard_normal((B, Hkv, Tk, d))
+    for causal, window in ((False, -1), (True, -1), (True, 4)):
+        o_ref, lse_ref = orc.forward_ex(q, k, v, causal, 0.7, window)
+        for bounds in ([0, Tk], [0, 11, Tk], [0, 0, 5, 5, 17, Tk], [0, 1, 2, 3, 20, Tk],
+                       list(range(0, Tk + 1))):
+            m, l, a = oracle.partials_f64(q, k, v, causal, 0.7, window, bounds)
+            _, _, _, o, lse = oracle.merge_partials(m, l, a)
+            assert np.allclose(o, o_ref, rtol=0, atol=1e-12), (causal, window, bounds)
+            assert np.allclose(lse, lse_ref, rtol=0, atol=1e-12), (causal, window, bounds)
+
+
+def check_merge_is_associative(orc):
+    """Merging partials in any grouping gives the same (m, l, a) (the page states the rule is
+    associative); a merged triple is itself a partial."""
+    r = _rng(41)
+    q = r.standard_normal((1, 1, 4, 3))
+    k = r.standard_normal((1, 1, 30, 3))
+    v = r.standard_normal((1, 1, 30, 3))
+    m, l, a = oracle.partials_f64(q, k, v, True, 1.3, -1, [0, 7, 9, 21, 30])
+    whole = oracle.merge_partials(m, l, a)
+    left = oracle.merge_partials(m[:2], l[:2], a[:2])
+    right = oracle.merge_partials(m[2:], l[2:], a[2:])
+    grouped = oracle.merge_partials(np.stack([left[0], right[0]]), np.stack([left[1], right[1]]),
+                                    np.stack([left[2], right[2]]))
+    for x, y in zip(whole, grouped):
+        assert np.allclose(x, y, rtol=1e-13, atol=1e-13)
+    # the merged max is the largest partial max; l >= the l of the chunk holding it
+    assert np.array_equal(whole[0], m.max(axis=0))
+
+
 ALL_CHECKS = [
     check_worked_example_oracle,
     check_worked_example_two_tiles,
@@ -519,4 +559,6 @@ ALL_CHECKS = [
     check_ex_query_offset_bottom_right,
     check_ex_sliding_window,
     check_ex_backward_finite_differences,
+    check_split_merge_equals_unsplit,
+    check_merge_is_associative,
 ]

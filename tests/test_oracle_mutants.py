@@ -1,5 +1,6 @@
 """Each planted mistake in the oracle (built with -DORACLE_MUTANT=n) must fail at least
 one pin; this shows the pins can tell a correct oracle from a plausibly wrong one."""
+import numpy as np
 import pytest
 
 import oracle
@@ -30,3 +31,38 @@ def test_mutant_is_caught(mutant):
             failed.append(check.__name__)
             break
     assert failed, f"no pin caught mutant {mutant}: {MUTANTS[mutant]}"
+
+
+# Planted mistakes in the flash-decoding merge (numpy part of the oracle): each must fail the
+# split/merge pin.
+def _merge_flipped_weights(m, l, a):
+    mm = m.max(axis=0)
+    w = np.where(np.isneginf(m), 0.0, np.exp(mm[None] - m))  # exp(m - m_i) instead of exp(m_i - m)
+    ll = (w * l).sum(axis=0)
+    aa = (w[..., None] * a).sum(axis=0)
+    return mm, ll, aa, aa / ll[..., None], mm + np.log(ll)
+
+
+def _merge_unweighted_l(m, l, a):
+    mm = m.max(axis=0)
+    w = np.where(np.isneginf(m), 0.0, np.exp(m - mm[None]))
+    ll = l.sum(axis=0)  # l summed without the rescale
+    aa = (w[..., None] * a).sum(axis=0)
+    return mm, ll, aa, aa / ll[..., None], mm + np.log(ll)
+
+
+def _merge_first_max(m, l, a):
+    mm = np.where(np.isneginf(m[0]), m.max(axis=0), m[0])  # reference from the first chunk only
+    w = np.where(np.isneginf(m), 0.0, np.exp(np.minimum(m - mm[None], 0.0)))
+    ll = (w * l).sum(axis=0)
+    aa = (w[..., None] * a).sum(axis=0)
+    return mm, ll, aa, aa / ll[..., None], mm + np.log(ll)
+
+
+@pytest.mark.parametrize("broken", [_merge_flipped_weights, _merge_unweighted_l, _merge_first_max],
+                         ids=lambda f: f.__name__)
+def test_merge_mutant_is_caught(broken, monkeypatch):
+    monkeypatch.setattr(oracle, "merge_partials", broken)
+    orc = oracle.Oracle(threads=2)
+    with pytest.raises(AssertionError):
+        oracle_pins.check_split_merge_equals_unsplit(orc)
