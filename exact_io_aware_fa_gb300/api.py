@@ -23,7 +23,8 @@ FA_ERR_CUDA = 4
 FA_ERR_TIMEOUT = 5
 
 # Every symbol include/fa.h declares.
-EXPORTS = ("fa_forward", "fa_forward_ex", "fa_backward_workspace_bytes", "fa_backward",
+EXPORTS = ("fa_forward", "fa_forward_ex", "fa_forward_splitkv_workspace_bytes",
+           "fa_forward_splitkv", "fa_backward_workspace_bytes", "fa_backward",
            "fa_backward_ex", "fa_backward_noalloc", "fa_status_string", "fa_last_cuda_error",
            "fa_device_error")
 
@@ -64,6 +65,10 @@ def library(path: str | None = None):
         lib.fa_forward.restype = I
         lib.fa_forward_ex.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, F, P]
         lib.fa_forward_ex.restype = I
+        lib.fa_forward_splitkv_workspace_bytes.argtypes = [I, I, I, I, I]
+        lib.fa_forward_splitkv_workspace_bytes.restype = Z
+        lib.fa_forward_splitkv.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, P, P]
+        lib.fa_forward_splitkv.restype = I
         lib.fa_backward_workspace_bytes.argtypes = [I, I, I, I]
         lib.fa_backward_workspace_bytes.restype = Z
         lib.fa_backward.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, P, P]
@@ -104,6 +109,18 @@ def forward_ex_raw(q: int, k: int, v: int, o: int, lse: int, B: int, Hq: int, Hk
     """fa_forward_ex: grouped KV heads, query offset Tk - Tq, optional sliding window."""
     return library().fa_forward_ex(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, causal, window, scale,
                                    stream)
+
+
+def forward_splitkv_raw(q: int, k: int, v: int, o: int, lse: int, B: int, Hq: int, Hkv: int,
+                        Tq: int, Tk: int, d: int, causal: int, window: int, scale: float,
+                        nsplit: int, workspace: int, stream: int) -> int:
+    """fa_forward_splitkv: the key range of every query block cut into `nsplit` chunks."""
+    return library().fa_forward_splitkv(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, causal, window,
+                                        scale, nsplit, workspace, stream)
+
+
+def splitkv_workspace_bytes(B: int, Hq: int, Tq: int, d: int, nsplit: int) -> int:
+    return int(library().fa_forward_splitkv_workspace_bytes(B, Hq, Tq, d, nsplit))
 
 
 def backward_ex_raw(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Tq, Tk, d, causal, window,
@@ -171,13 +188,30 @@ def _shapes(q, k, v):
     return B, Hq, Hkv, Tq, Tk, d
 
 
+MAX_SPLITS = 64  # FA_MAX_SPLITS in include/fa.h
+
+
+def choose_splits(B: int, Hq: int, Tq: int, Tk: int, num_sms: int) -> int:
+    """Key-range splits for the forward: 1 when the 256-row query blocks alone give every SM
+    two or more work units, else enough splits for about four units per SM, each keeping at
+    least four 128-key tiles."""
+    units = -(-Tq // 256) * B * Hq
+    if units <= 0 or units >= 2 * num_sms:
+        return 1
+    tiles = -(-Tk // 128)
+    want = -(-4 * num_sms // units)
+    return max(1, min(MAX_SPLITS, want, tiles // 4))
+
+
 def forward(q, k, v, causal: bool = False, scale: float | None = None, window: int = -1,
-            out=None, lse=None, stream=None):
+            out=None, lse=None, nsplit: int | None = None, workspace=None, stream=None):
     """O, LSE = attention(q, k, v).
 
     q is bf16 [B, Hq, Tq, d]; k and v are bf16 [B, Hkv, Tk, d] with Hq % Hkv == 0. Query row i
     sits at key position Tk - Tq + i; ``window`` >= 0 (causal only) keeps keys no more than
     ``window`` positions before it. Multi-head attention is Hkv = Hq, Tq = Tk.
+    ``nsplit``: key-range splits (flash-decoding); None picks them from the shape
+    (``choose_splits``), 1 disables them.
     """
     import torch
     B, Hq, Hkv, Tq, Tk, d = _shapes(q, k, v)
@@ -189,12 +223,24 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, window: i
         lse = torch.empty((B, Hq, Tq), dtype=torch.float32, device=q.device)
     _check_tensor("out", out, q.shape)
     _check_tensor("lse", lse, (B, Hq, Tq))
+    if nsplit is None:
+        sms = torch.cuda.get_device_properties(q.device).multi_processor_count
+        nsplit = choose_splits(B, Hq, Tq, Tk, sms)
+    ws_ptr = 0
+    if nsplit > 1:
+        need = splitkv_workspace_bytes(B, Hq, Tq, d, nsplit)
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        if workspace is not None:
+            if workspace.numel() * workspace.element_size() < need:
+                raise ValueError(f"workspace needs {need} bytes")
+            ws_ptr = workspace.data_ptr()
     s = stream if stream is not None else torch.cuda.current_stream(q.device).cuda_stream
     with torch.cuda.device(q.device):
-        st = forward_ex_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                            lse.data_ptr(), B, Hq, Hkv, Tq, Tk, d, int(bool(causal)), int(window),
-                            float(scale), s)
-    _check(st, "fa_forward_ex")
+        st = forward_splitkv_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                 lse.data_ptr(), B, Hq, Hkv, Tq, Tk, d, int(bool(causal)),
+                                 int(window), float(scale), int(nsplit), ws_ptr, s)
+    _check(st, "fa_forward_splitkv")
     return out, lse
 
 

@@ -206,9 +206,27 @@ const char* fa_status_string(fa_status s) {
 
 int fa_last_cuda_error(void) { return t_last_cuda_error; }
 
-fa_status fa_forward_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                        int Hq, int Hkv, int Tq, int Tk, int d, int causal, int window,
-                        float scale, struct CUstream_st* stream) {
+// Split-KV workspace: nsplit partial O (fp32 [B*Hq, Tq, d]) then nsplit partial LSE
+// (fp32 [B*Hq, Tq]), each part 256-byte aligned.
+static size_t splitkv_bytes(long long bhq, long long tq, int d, int nsplit, size_t* lse_off) {
+    const size_t rows = (size_t)bhq * (size_t)tq * (size_t)nsplit;
+    const size_t o_bytes = (rows * (size_t)d * sizeof(float) + 255) / 256 * 256;
+    if (lse_off) *lse_off = o_bytes;
+    return o_bytes + (rows * sizeof(float) + 255) / 256 * 256;
+}
+
+size_t fa_forward_splitkv_workspace_bytes(int B, int Hq, int Tq, int d, int nsplit) {
+    if (B <= 0 || Hq <= 0 || Tq <= 0 || (d != 64 && d != 128) || nsplit < 2 ||
+        nsplit > FA_MAX_SPLITS)
+        return 0;
+    return splitkv_bytes((long long)B * Hq, Tq, d, nsplit, nullptr);
+}
+
+fa_status fa_forward_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int B, int Hq, int Hkv, int Tq, int Tk, int d, int causal,
+                             int window, float scale, int nsplit, void* workspace,
+                             struct CUstream_st* stream) {
+    if (nsplit < 1 || nsplit > FA_MAX_SPLITS) return FA_ERR_INVALID_ARG;
     Shape sh;
     bool empty = false;
     fa_status st = check_shape(B, Hq, Hkv, Tq, Tk, d, causal, window, scale, &sh, &empty);
@@ -216,6 +234,9 @@ fa_status fa_forward_ex(const void* q, const void* k, const void* v, void* o, fl
     if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
         return FA_ERR_ALIGNMENT;
+    if (nsplit > 1 && workspace && !aligned(workspace, 256)) return FA_ERR_ALIGNMENT;
+    if (((long long)Tq + 255) / 256 * sh.BHq * nsplit > INT_MAX) return FA_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     fa::FwdLaunch a;
     std::memset(&a, 0, sizeof a);
     if ((st = make_map(&a.tm_q, q, sh.BHq, Tq, d, 128)) != FA_OK) return st;
@@ -232,9 +253,35 @@ fa_status fa_forward_ex(const void* q, const void* k, const void* v, void* o, fl
     a.window = window;
     a.c = scale * kLog2e;
     a.lse = lse;
-    cudaError_t e = fa::launch_forward(a, d, causal != 0, reinterpret_cast<cudaStream_t>(stream));
+    a.o = o;
+    a.nsplit = nsplit;
+    void* ws = workspace;
+    bool owned = false;
+    if (nsplit > 1) {
+        size_t lse_off = 0;
+        const size_t bytes = splitkv_bytes(sh.BHq, Tq, d, nsplit, &lse_off);
+        if (!ws) {
+            cudaError_t e = cudaMallocAsync(&ws, bytes, s);
+            if (e != cudaSuccess) return cuda_fail(e);
+            owned = true;
+        }
+        a.part_o = static_cast<float*>(ws);
+        a.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + lse_off);
+    }
+    cudaError_t e = fa::launch_forward(a, d, causal != 0, s);
+    if (owned) {
+        cudaError_t e2 = cudaFreeAsync(ws, s);
+        if (e == cudaSuccess) e = e2;
+    }
     if (e != cudaSuccess) return cuda_fail(e);
     return FA_OK;
+}
+
+fa_status fa_forward_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                        int Hq, int Hkv, int Tq, int Tk, int d, int causal, int window,
+                        float scale, struct CUstream_st* stream) {
+    return fa_forward_splitkv(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, causal, window, scale, 1,
+                              nullptr, stream);
 }
 
 fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B,

@@ -27,6 +27,8 @@
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 and O_1 after column 256.
 #include <algorithm>
 
+#include <cuda_bf16.h>
+
 #include "fa_common.cuh"
 #include "fa_launch.h"
 
@@ -99,12 +101,14 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 // keys before position - window are not visible.
 struct FwdShape {
     int Tq, Tk, Hq, Hkv, group, offset, window, nqb;
+    int nsplit;  // key-range splits per unit (flash-decoding); 1 = whole range, final output
+    int BHq;     // B * Hq (partial-result indexing)
 };
 
 // One work unit: (query head bh_q, 256-row block qb) and, per Q tile t, its range of key
 // tiles [jb_t, je_t) (empty when the tile lies past Tq).
 struct FwdUnit {
-    int bh_q, bh_kv, qb;
+    int bh_q, bh_kv, qb, split;
     int jb0, je0, jb1, je1;
     int jb_all, je_all;
     __device__ __forceinline__ int jb(int t) const { return t ? jb1 : jb0; }
@@ -123,10 +127,15 @@ __device__ __forceinline__ int fwd_unit_index(int cta, int k, int G, int U) {
     return u < U ? (int)u : -1;
 }
 
-template <int D, bool CAUSAL, bool WINDOW>
+template <int D, bool CAUSAL, bool WINDOW, bool SPLIT>
 __device__ __forceinline__ FwdUnit fwd_unit(int u, const FwdShape& sh) {
     using C = FwdCfg<D>;
     FwdUnit w;
+    w.split = 0;
+    if (SPLIT) {
+        w.split = u % sh.nsplit;  // the splits of one query block are consecutive units
+        u /= sh.nsplit;
+    }
     w.bh_q = u / sh.nqb;
     const int i = u % sh.nqb;
     if (CAUSAL) {
@@ -148,23 +157,38 @@ __device__ __forceinline__ FwdUnit fwd_unit(int u, const FwdShape& sh) {
         je = CAUSAL ? min(nk, p1 / C::BN + 1) : nk;
         jb = WINDOW ? max(0, p0 - sh.window) / C::BN : 0;
         if (jb >= je) jb = je = 0;  // (cannot happen for valid shapes)
+        if (SPLIT && je > jb) {
+            // this split's chunk of the range (empty when the range is short)
+            const int c = (je - jb + sh.nsplit - 1) / sh.nsplit;
+            const int b0 = jb + w.split * c;
+            jb = min(je, b0);
+            je = min(je, b0 + c);
+        }
     };
     range(w.qb * C::ROWS, w.jb0, w.je0);
     range(w.qb * C::ROWS + C::BM, w.jb1, w.je1);
-    w.jb_all = w.jb0;  // tile 0 is never empty
-    w.je_all = max(w.je0, w.je1);
-    if (w.je1 > w.jb1) w.jb_all = min(w.jb_all, w.jb1);
-    if (w.je_all <= w.jb_all) w.jb_all = w.je_all = 0;
+    if (!SPLIT) {
+        // tile 0 always has keys without splits
+        w.jb_all = w.jb0;
+        w.je_all = max(w.je0, w.je1);
+        if (w.je1 > w.jb1) w.jb_all = min(w.jb_all, w.jb1);
+    } else {
+        // a split chunk may be empty for either tile
+        const bool e0 = w.je0 > w.jb0, e1 = w.je1 > w.jb1;
+        w.jb_all = e0 ? (e1 ? min(w.jb0, w.jb1) : w.jb0) : (e1 ? w.jb1 : 0);
+        w.je_all = e0 ? (e1 ? max(w.je0, w.je1) : w.je0) : (e1 ? w.je1 : 0);
+    }
     return w;
 }
 
-// WINDOW (causal only): keys before position - window are not visible.
-template <int D, bool CAUSAL, bool WINDOW>
+// WINDOW (causal only): keys before position - window are not visible. SPLIT: every unit is
+// one key chunk of a query block and writes a partial result for the merge kernel.
+template <int D, bool CAUSAL, bool WINDOW, bool SPLIT>
 __global__ void __launch_bounds__(384, 1)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
               const FwdShape sh, const int num_units, const float c, float* __restrict__ lse_out,
-              int* err) {
+              float* __restrict__ part_o, float* __restrict__ part_lse, int* err) {
     using C = FwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
@@ -224,7 +248,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             int last_q_use[2] = {-1, -1};
             bool ok = true;
             for (int u; ok && (u = fwd_unit_index<CAUSAL>(blockIdx.x, ul, G, num_units)) >= 0; ++ul) {
-                const FwdUnit w = fwd_unit<D, CAUSAL, WINDOW>(u, sh);
+                const FwdUnit w = fwd_unit<D, CAUSAL, WINDOW, SPLIT>(u, sh);
                 const int b = ul % C::NQB;
                 const int use = ul / C::NQB;  // earlier uses of Q buffer b
                 if (use > 0) {
@@ -297,7 +321,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         int ul = 0;
         bool ok = true;
         for (int u; ok && (u = fwd_unit_index<CAUSAL>(blockIdx.x, ul, G, num_units)) >= 0; ++ul) {
-            const FwdUnit w = fwd_unit<D, CAUSAL, WINDOW>(u, sh);
+            const FwdUnit w = fwd_unit<D, CAUSAL, WINDOW, SPLIT>(u, sh);
             const int b = ul % C::NQB;
             if (warp == 1) {
                 ok = warp_wait(ptx::smem_addr(&bars->q_full[b]), (uint32_t)(ul / C::NQB) & 1u,
@@ -393,7 +417,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         int ul = 0;
         bool ok = true;
         for (int u; ok && (u = fwd_unit_index<CAUSAL>(blockIdx.x, ul, G, num_units)) >= 0; ++ul) {
-            const FwdUnit w = fwd_unit<D, CAUSAL, WINDOW>(u, sh);
+            const FwdUnit w = fwd_unit<D, CAUSAL, WINDOW, SPLIT>(u, sh);
             const int jb = w.jb(t), je = w.je(t);
             const int n = je - jb;
             const int b = ul % C::NQB;
@@ -405,11 +429,18 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             // Keys [vis_lo, vis_hi] are visible to this row.
             const int vis_lo = WINDOW ? max(0, pos - sh.window) : 0;
             const int vis_hi = CAUSAL ? min(pos, sh.Tk - 1) : sh.Tk - 1;
+            // A warp whose rows all lie past Tq skips the per-step arithmetic (its P rows feed only
+            // O rows that are never stored) but keeps every barrier step with the others.
+            const bool live = !SPLIT || (row0 + wq * 32) < sh.Tq;
+            // partial-result row of this thread (split mode): [split][B*Hq][Tq]
+            const size_t prow = ((size_t)w.split * sh.BHq + w.bh_q) * (size_t)sh.Tq + row;
             if (n == 0) {
-                // This Q tile is past N in this unit: release its share of the Q buffer. It
-                // first waits for this unit's Q load, so that its arrival counts towards this
-                // use of the buffer and cannot complete an earlier use's phase ahead of the
-                // other tile's epilogue (an mbarrier counts arrivals, not arrivers).
+                // No key tile of this Q tile in this unit (rows past Tq, or an empty split
+                // chunk): release its share of the Q buffer. It first waits for this unit's Q
+                // load, so that its arrival counts towards this use of the buffer and cannot
+                // complete an earlier use's phase ahead of the other tile's epilogue (an
+                // mbarrier counts arrivals, not arrivers).
+                if (SPLIT && row < sh.Tq) part_lse[prow] = -INFINITY;  // merge skips it
                 ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->q_full[b]),
                                                         (uint32_t)(ul / C::NQB) & 1u, abort_flag,
                                                         err, kDevTimeoutLoad));
@@ -422,6 +453,26 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             // alpha = exp2(m_old - m_new). O is rescaled only when some row of the warp moved.
             float m_ref = -INFINITY;  // reference (scaled log2 domain)
             float l = 0.f;            // running sum of exp2(c*s - m_ref)
+            if (!live) {
+                // rows all past Tq: only the barrier steps (see above)
+                for (int j = jb; j < je; ++j, ++it) {
+                    ok = __all_sync(0xffffffffu, wait_phase(b_s_full, (uint32_t)it & 1u, abort_flag,
+                                                            err, kDevTimeoutMma));
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+                    if (C::P_SEPARATE) {
+                        ptx::tc_fence_before();
+                        ptx::mbar_arrive(b_s_free);
+                    }
+                    if (j > jb) {
+                        ok = __all_sync(0xffffffffu, wait_phase(b_o_done, (uint32_t)(it - 1) & 1u,
+                                                                abort_flag, err, kDevTimeoutMma));
+                        if (!ok) break;
+                    }
+                    ptx::tc_fence_before();
+                    ptx::mbar_arrive(b_p_full);
+                }
+            } else
             for (int j = jb; j < je; ++j, ++it) {
                 ok = __all_sync(0xffffffffu, wait_phase(b_s_full, (uint32_t)it & 1u, abort_flag, err,
                                                         kDevTimeoutMma));
@@ -541,8 +592,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                                                     err, kDevTimeoutMma));
             if (!ok) break;
             ptx::tc_fence_after();
-            const float inv_l = 1.f / l;
-            uint32_t o_all[D];
+            uint32_t o_all[D];  // (loaded by every warp: a branch here costs registers)
 #pragma unroll
             for (int cc = 0; cc < D / 32; ++cc) {
                 uint32_t o[32];
@@ -553,6 +603,28 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             // O_t is in registers: the next unit's first O_t += P V may overwrite it.
             ptx::tc_fence_before();
             ptx::mbar_arrive(ptx::smem_addr(&bars->o_free[t]));
+            if (SPLIT) {
+                // Partial result of this key chunk ("15. FlashAttention", section "Decode is
+                // different: flash-decoding"): the normalised O_s = a_s / l_s in fp32 and
+                // LSE_s = m_s + ln l_s, merged later by weights exp(LSE_s - LSE). A row that
+                // sees no key of the chunk gets LSE_s = -inf (the merge skips it).
+                if (live && row < sh.Tq) {
+                    const bool any = l > 0.f;
+                    const float inv_l = any ? 1.f / l : 0.f;
+                    float4* dst = reinterpret_cast<float4*>(part_o + prow * D);
+#pragma unroll
+                    for (int e = 0; e < D; e += 4)
+                        dst[e / 4] = make_float4(__uint_as_float(o_all[e]) * inv_l,
+                                                 __uint_as_float(o_all[e + 1]) * inv_l,
+                                                 __uint_as_float(o_all[e + 2]) * inv_l,
+                                                 __uint_as_float(o_all[e + 3]) * inv_l);
+                    part_lse[prow] = any ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+                }
+                // no staging: this tile's share of the Q buffer is free once its MMAs are done
+                if (r == 0) ptx::mbar_arrive(ptx::smem_addr(&bars->q_free[b]));
+                continue;
+            }
+            const float inv_l = 1.f / l;
             uint8_t* stage = smem + C::OFF_Q + (b * 2 + t) * C::TILE_BYTES;
 #pragma unroll
             for (int cc = 0; cc < D / 32; ++cc) {
@@ -591,11 +663,52 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     }
 }
 
-template <int D, bool CAUSAL, bool WINDOW>
+// ----------------------------------------------------------------------------------------
+// Merge of the split partials ("15. FlashAttention", section "Decode is different:
+// flash-decoding"): with normalised partials O_s and LSE_s = m_s + ln l_s the page's rule
+// m = max m_s, l = sum e^(m_s - m) l_s, a = sum e^(m_s - m) a_s, O = a / l becomes
+// LSE = M + ln sum_s e^(LSE_s - M) and O = sum_s e^(LSE_s - LSE) O_s (M = max_s LSE_s).
+// One warp per query row; each lane owns D/32 columns. Splits with LSE_s = -inf saw no key.
+// ----------------------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256)
+fa_fwd_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse,
+                    __nv_bfloat16* __restrict__ o, float* __restrict__ lse, long long rows,
+                    int nsplit) {
+    constexpr int E = D / 32;
+    const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    float mx = -INFINITY;
+    for (int sp = 0; sp < nsplit; ++sp) mx = fmaxf(mx, part_lse[(size_t)sp * rows + row]);
+    float acc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    float sum = 0.f;
+    if (mx != -INFINITY) {
+        for (int sp = 0; sp < nsplit; ++sp) {
+            const float ls = part_lse[(size_t)sp * rows + row];
+            if (ls == -INFINITY) continue;
+            const float wgt = expf(ls - mx);
+            sum += wgt;
+            const float* src = part_o + ((size_t)sp * rows + row) * D + lane * E;
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[e] = fmaf(wgt, src[e], acc[e]);
+        }
+    }
+    const float inv = (sum > 0.f) ? 1.f / sum : 0.f;
+    __nv_bfloat16* dst = o + (size_t)row * D + lane * E;
+#pragma unroll
+    for (int e = 0; e < E; e += 2)
+        *reinterpret_cast<uint32_t*>(dst + e) = ptx::pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
+    if (lane == 0) lse[row] = (sum > 0.f) ? mx + logf(sum) : -INFINITY;
+}
+
+template <int D, bool CAUSAL, bool WINDOW, bool SPLIT>
 cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
     static_assert(CAUSAL || !WINDOW, "a window hangs off the causal diagonal");
     using C = FwdCfg<D>;
-    auto kern = fa_fwd_kernel<D, CAUSAL, WINDOW>;
+    auto kern = fa_fwd_kernel<D, CAUSAL, WINDOW, SPLIT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -608,29 +721,47 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
     sh.offset = a.Tk - a.Tq;
     sh.window = a.window;
     sh.nqb = (a.Tq + C::ROWS - 1) / C::ROWS;
-    const long long units = (long long)sh.nqb * a.BHq;
+    sh.nsplit = SPLIT ? a.nsplit : 1;
+    sh.BHq = a.BHq;
+    const long long units = (long long)sh.nqb * a.BHq * sh.nsplit;
     if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     // Persistent grid: one CTA per SM (the shared-memory footprint admits no more), each
     // walking its units in the order fwd_unit_index gives.
     const int grid = (int)std::min<long long>(units, (long long)a.num_sms);
     kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, sh,
-                                                      (int)units, a.c, a.lse, a.err);
+                                                      (int)units, a.c, a.lse, a.part_o,
+                                                      a.part_lse, a.err);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || !SPLIT) return e;
+    const long long rows = (long long)a.BHq * a.Tq;
+    const long long blocks = (rows + 7) / 8;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    fa_fwd_merge_kernel<D><<<(unsigned)blocks, 256, 0, stream>>>(
+        a.part_o, a.part_lse, static_cast<__nv_bfloat16*>(a.o), a.lse, rows, sh.nsplit);
     return cudaGetLastError();
 }
 
 }  // namespace
 
+template <int D>
+cudaError_t launch_fwd_mask(const FwdLaunch& a, bool causal, bool window, bool split,
+                            cudaStream_t stream) {
+    if (split) {
+        if (!causal) return launch_fwd_t<D, false, false, true>(a, stream);
+        return window ? launch_fwd_t<D, true, true, true>(a, stream)
+                      : launch_fwd_t<D, true, false, true>(a, stream);
+    }
+    if (!causal) return launch_fwd_t<D, false, false, false>(a, stream);
+    return window ? launch_fwd_t<D, true, true, false>(a, stream)
+                  : launch_fwd_t<D, true, false, false>(a, stream);
+}
+
 cudaError_t launch_forward(const FwdLaunch& a, int d, bool causal, cudaStream_t stream) {
     const bool window = a.window >= 0;
+    const bool split = a.nsplit > 1;
     if (window && !causal) return cudaErrorInvalidValue;
-    if (d == 64) {
-        if (!causal) return launch_fwd_t<64, false, false>(a, stream);
-        return window ? launch_fwd_t<64, true, true>(a, stream) : launch_fwd_t<64, true, false>(a, stream);
-    }
-    if (d == 128) {
-        if (!causal) return launch_fwd_t<128, false, false>(a, stream);
-        return window ? launch_fwd_t<128, true, true>(a, stream) : launch_fwd_t<128, true, false>(a, stream);
-    }
+    if (d == 64) return launch_fwd_mask<64>(a, causal, window, split, stream);
+    if (d == 128) return launch_fwd_mask<128>(a, causal, window, split, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -18,6 +18,10 @@ struct FwdLaunch {
     float* lse;                          // [B*Hq, Tq] fp32
     int* err;                            // device error word
     int num_sms;                         // SMs of the device (persistent grid size)
+    int nsplit;                          // key-range splits (1: none)
+    void* o;                             // bf16 [B*Hq, Tq, d] (written by the split merge)
+    float* part_o;                       // nsplit > 1: fp32 [nsplit, B*Hq, Tq, d] partial O
+    float* part_lse;                     // nsplit > 1: fp32 [nsplit, B*Hq, Tq] partial LSE
 };
 
 // Forward: O and LSE. d in {64, 128}.

@@ -91,6 +91,30 @@ fa_status fa_forward_ex(const void* q, const void* k, const void* v, void* o, fl
                         float scale, struct CUstream_st* stream);
 
 /*
+ * Split-KV forward ("flash-decoding"; "15. FlashAttention", inference.shantanugoel.com, section
+ * "Decode is different: flash-decoding"). Same operation, arguments and results as
+ * fa_forward_ex, but every query block's visible key range is cut into `nsplit` chunks that
+ * run as separate work units, so short query blocks (decode, small B*Hq*Tq) still fill the
+ * GPU. Each chunk writes its partial result -- the chunk's normalised O_s (fp32) and
+ * LSE_s = m_s + ln l_s, or LSE_s = -inf for a row that sees no key of the chunk -- and a
+ * second kernel merges them by the page's rule m = max m_s, l = sum e^(m_s - m) l_s,
+ * a = sum e^(m_s - m) a_s, O = a / l (with normalised partials: O = sum_s e^(LSE_s - LSE) O_s,
+ * LSE = ln sum_s e^LSE_s). Results equal fa_forward_ex's up to rounding order.
+ *   nsplit    1 .. FA_MAX_SPLITS; 1 is fa_forward_ex (no workspace used).
+ *   workspace device buffer of >= fa_forward_splitkv_workspace_bytes(B, Hq, Tq, d, nsplit)
+ *             bytes, 256-byte aligned, or NULL (allocated and freed on `stream`).
+ * Errors as fa_forward_ex; nsplit out of range -> FA_ERR_INVALID_ARG.
+ */
+#define FA_MAX_SPLITS 64
+
+size_t fa_forward_splitkv_workspace_bytes(int B, int Hq, int Tq, int d, int nsplit);
+
+fa_status fa_forward_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int B, int Hq, int Hkv, int Tq, int Tk, int d, int causal,
+                             int window, float scale, int nsplit, void* workspace,
+                             struct CUstream_st* stream);
+
+/*
  * Bytes of device workspace fa_backward needs for these sizes: two 32-byte records per query
  * row holding -LSE/scale and -D_i (D_i = O_i . dO_i) as exact three-part bf16 sums, [B*H, Npad]
  * each, and an fp32 dQ accumulator [B*H, Npad, d]; Npad = N rounded up to 128. In total

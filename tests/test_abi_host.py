@@ -150,3 +150,37 @@ def test_ex_empty_is_ok(lib):
     assert fwd_ex(lib, causal=0, Tq=500, Tk=200) != 1  # non-causal: Tq > Tk is fine
     assert bwd_ex(lib, B=0) == 0
     assert bwd_ex(lib, Tq=0, Tk=0) == 0
+
+
+def fwd_split(lib, nsplit=4, ws=0, B=1, Hq=4, Hkv=2, Tq=1, Tk=1024, d=64, causal=1, window=-1,
+              scale=0.125, **ptrs):
+    p = {n: A for n in ("q", "k", "v", "o", "lse")}
+    p.update(ptrs)
+    return lib.fa_forward_splitkv(p["q"], p["k"], p["v"], p["o"], p["lse"], B, Hq, Hkv, Tq, Tk, d,
+                                  causal, window, scale, nsplit, ws, None)
+
+
+@pytest.mark.parametrize("kw,status", EX_REJECT + [
+    (dict(nsplit=0), 1), (dict(nsplit=-2), 1), (dict(nsplit=65), 1), (dict(ws=A + 64), 3)])
+def test_forward_splitkv_rejects(lib, kw, status):
+    assert fwd_split(lib, **kw) == status
+
+
+def test_splitkv_workspace_bytes(lib):
+    from exact_io_aware_fa_gb300 import api
+    # nsplit partial rows of d fp32 values plus one fp32 LSE each, both parts 256-byte aligned
+    rows = 2 * 3 * 5 * 4
+    assert api.splitkv_workspace_bytes(2, 3, 5, 64, 4) == (rows * 64 * 4 + 255) // 256 * 256 + \
+        (rows * 4 + 255) // 256 * 256
+    assert api.splitkv_workspace_bytes(1, 1, 1, 128, 1) == 0   # no split, no workspace
+    assert api.splitkv_workspace_bytes(1, 1, 1, 128, 65) == 0
+    assert api.splitkv_workspace_bytes(1, 1, 1, 96, 4) == 0
+
+
+def test_split_choice():
+    from exact_io_aware_fa_gb300 import api
+    assert api.choose_splits(4, 16, 2048, 2048, 152) == 1        # 512 blocks fill the GPU
+    assert api.choose_splits(8, 32, 1, 16384, 152) == 3          # 256 decode rows: ~4 units/SM
+    assert api.choose_splits(1, 8, 1, 16384, 152) == 32          # 8 rows, 128 key tiles
+    assert api.choose_splits(1, 8, 1, 300, 152) == 1             # too few key tiles to split
+    assert api.choose_splits(1, 1, 1, 1 << 20, 152) == api.MAX_SPLITS

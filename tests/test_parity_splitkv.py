@@ -1,0 +1,112 @@
+"""Parity of the split-KV ("flash-decoding") forward: fa_forward_splitkv cuts every query
+block's key range into chunks, writes per-chunk partials and merges them; O and LSE must match
+the fp64 oracle's unsplit forward_ex on the same seeded bf16 inputs. Includes decode (one query
+row), chunks that some rows cannot see, chunks with no key tile at all, and the equality of
+nsplit = 1 with fa_forward_ex."""
+import pytest
+
+import oracle
+from parity_util import assert_close_lse, assert_close_o, default_scale, to_dev, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def env():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    import __graft_entry__
+    __graft_entry__.build()
+    from exact_io_aware_fa_gb300 import api
+    return api, oracle.oracle()
+
+
+# (B, Hq, Hkv, Tq, Tk, d, causal, window, nsplit)
+CASES = [
+    (2, 8, 2, 1, 3000, 128, True, -1, 8),     # decode against a long cache
+    (1, 4, 4, 1, 777, 64, False, -1, 3),      # decode, ragged cache, non-causal
+    (1, 2, 2, 300, 1000, 64, True, -1, 3),    # chunked prefill
+    (1, 3, 3, 700, 700, 64, False, -1, 4),    # plain multi-head attention
+    (1, 2, 1, 500, 900, 128, True, 200, 5),   # window: many rows see nothing in some chunks
+    (1, 2, 2, 129, 200, 64, True, -1, 7),     # more splits than key tiles: empty chunks
+    (1, 4, 2, 64, 4096, 128, True, -1, 16),   # short query block, many splits
+    (2, 2, 2, 256, 256, 128, True, -1, 2),    # causal square: tile 0 empty in split 1
+]
+
+
+def ids(c):
+    B, Hq, Hkv, Tq, Tk, d, causal, w, ns = c
+    return f"B{B}Hq{Hq}Hkv{Hkv}Tq{Tq}Tk{Tk}d{d}{'c' if causal else 'n'}w{w}s{ns}"
+
+
+@pytest.mark.parametrize("case", CASES, ids=ids)
+def test_splitkv_matches_oracle(env, case):
+    import torch
+    from exact_io_aware_fa_gb300 import synthetic
+    api, orc = env
+    B, Hq, Hkv, Tq, Tk, d, causal, window, nsplit = case
+    bits = synthetic.attention_inputs_ex(B, Hq, Hkv, Tq, Tk, d, seed=3 * Tk + Tq + nsplit)
+    q, k, v = (to_dev(bits[n]) for n in ("q", "k", "v"))
+    scale = default_scale(d)
+    o, lse = api.forward(q, k, v, causal=causal, scale=scale, window=window, nsplit=nsplit)
+    torch.cuda.synchronize()
+    assert api.device_error() == 0
+    o_ref, lse_ref = orc.forward_ex(bits["q"], bits["k"], bits["v"], causal, scale, window)
+    assert_close_o(to_f64(o), o_ref, ids(case), small_case=Tq * Tk < 4096)
+    assert_close_lse(to_f64(lse), lse_ref, ids(case))
+
+
+def test_one_split_is_the_plain_forward(env):
+    """nsplit = 1 runs fa_forward_ex: bit-identical output."""
+    import torch
+    from exact_io_aware_fa_gb300 import synthetic
+    api, _ = env
+    bits = synthetic.attention_inputs_ex(1, 4, 2, 300, 600, 64, seed=8)
+    q, k, v = (to_dev(bits[n]) for n in ("q", "k", "v"))
+    o1, l1 = api.forward(q, k, v, causal=True, nsplit=1)
+    o2 = torch.empty_like(q)
+    l2 = torch.empty_like(l1)
+    st = api.forward_ex_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o2.data_ptr(), l2.data_ptr(),
+                            1, 4, 2, 300, 600, 64, 1, -1, default_scale(64), 0)
+    assert st == api.FA_OK
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_library_allocated_split_workspace(env):
+    """workspace = NULL: the library allocates the partials on the stream."""
+    import torch
+    from exact_io_aware_fa_gb300 import synthetic
+    api, orc = env
+    B, Hq, Hkv, Tq, Tk, d = 1, 2, 1, 3, 2500, 128
+    bits = synthetic.attention_inputs_ex(B, Hq, Hkv, Tq, Tk, d, seed=12)
+    q, k, v = (to_dev(bits[n]) for n in ("q", "k", "v"))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, Tq), dtype=torch.float32, device="cuda")
+    st = api.forward_splitkv_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                 lse.data_ptr(), B, Hq, Hkv, Tq, Tk, d, 1, -1, default_scale(d), 6, 0,
+                                 torch.cuda.current_stream().cuda_stream)
+    assert st == api.FA_OK
+    torch.cuda.synchronize()
+    assert api.device_error() == 0
+    o_ref, lse_ref = orc.forward_ex(bits["q"], bits["k"], bits["v"], True, default_scale(d))
+    assert_close_o(to_f64(o), o_ref, "ws=NULL", small_case=True)
+    assert_close_lse(to_f64(lse), lse_ref, "ws=NULL")
+
+
+def test_automatic_split_choice_for_decode(env):
+    """api.forward picks splits by itself for a decode shape and stays exact."""
+    import torch
+    from exact_io_aware_fa_gb300 import synthetic
+    api, orc = env
+    B, Hq, Hkv, Tq, Tk, d = 2, 4, 1, 1, 4000, 64
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert api.choose_splits(B, Hq, Tq, Tk, sms) > 1
+    bits = synthetic.attention_inputs_ex(B, Hq, Hkv, Tq, Tk, d, seed=21)
+    q, k, v = (to_dev(bits[n]) for n in ("q", "k", "v"))
+    o, lse = api.forward(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = orc.forward_ex(bits["q"], bits["k"], bits["v"], True, default_scale(d))
+    assert_close_o(to_f64(o), o_ref, "auto", small_case=True)
+    assert_close_lse(to_f64(lse), lse_ref, "auto")
