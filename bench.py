@@ -30,6 +30,11 @@ WORKLOAD = dict(name="B4 H16 N2048 d64 non-causal fwd+bwd", B=4, H=16, N=2048, d
 FWD_KERNEL_SRC = os.path.join(ROOT, "exact_io_aware_fa_gb300", "csrc", "fa_fwd.cu")
 BWD_KERNEL_SRC = os.path.join(ROOT, "exact_io_aware_fa_gb300", "csrc", "fa_bwd.cu")
 TRAFFIC_JSON = os.path.join(ROOT, "profiles", "traffic.json")
+# What the "dominant kernel" timing covers: one ABI call, timed by CUDA events around it.
+KERNEL_LABEL = {
+    "fa_bwd": "fa_backward call (fa_bwd_pre_kernel + fa_bwd_kernel + fa_bwd_dq_kernel)",
+    "fa_fwd": "fa_forward call (fa_fwd_kernel)",
+}
 L2_FLUSH_BYTES = 512 << 20
 METRIC = ("attention fwd+bwd TFLOPS (bf16 in, fp32 accumulate), 1 step = fa_forward + fa_backward"
           " on B4 H16 N2048 d64")
@@ -351,7 +356,7 @@ def run_ours(args, rank, world, local):
                        l2="flushed between timed steps (512 MiB write outside the events)"),
         "fwd": {"ms": fwd_avg, "tflops": fwd_tf, "frac_of_peak": fwd_tf / peaks["bf16_tflops"]},
         "bwd": {"ms": bwd_avg, "tflops": bwd_tf, "frac_of_peak": bwd_tf / peaks["bf16_tflops"]},
-        "roofline": {"kernel": dominant, "bound": "tensor", "achieved": dom_tf,
+        "roofline": {"kernel": KERNEL_LABEL[dominant], "bound": "tensor", "achieved": dom_tf,
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": dom_tf / peaks["bf16_tflops"], "traffic": traffic,
                      "peak_source": f"{peaks['source']} bf16 burst"},
