@@ -48,11 +48,11 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 //
 // Per query row it writes two "fold" records that let the main kernel's MMAs subtract the row
 // statistics themselves: S'^T = K Q^T + 1 * (-LSE/scale) and dP'^T = V dO^T + 1 * (-D), added as
-// one more K=16 MMA against a constant tile of ones. A record is 16 bf16 (k = 0..15): the value
-// split exactly into three bf16 parts (hi + mid + lo) at k = 0, 1, 2, zeros elsewhere, stored in
-// the tcgen05 no-swizzle K-major layout (8-row core matrices of 16-byte rows; the two K halves
-// 128 bytes apart, 8-row groups 256 bytes apart), so one bulk copy of a query block's records
-// lands in shared memory ready for the MMA.
+// one more K=16 MMA against a constant tile of ones. A record is 8 bf16 (16 bytes): the value
+// split exactly into three bf16 parts (hi + mid + lo) at k = 0, 1, 2, zeros at k = 3..7.
+// Consecutive rows' records are 16 bytes apart, which is the tcgen05 no-swizzle K-major layout
+// of an 8-wide K slice (8-row core matrices of 16-byte rows, 8-row groups 128 bytes apart), so
+// one bulk copy of a query block's records lands in shared memory ready for the MMA.
 // ----------------------------------------------------------------------------------------
 // Exact three-part bf16 split of v: hi = bf16(v), mid = bf16(v - hi), lo = v - hi - mid (each
 // difference is exact in fp32, and lo has at most 8 significant bits).
@@ -70,9 +70,9 @@ __device__ __forceinline__ uint4 fold_record(float v) {
     return w;
 }
 
-// Byte offset of row n's record (first K half) in a head's fold array.
+// Byte offset of row n's record in a fold array: 16 bytes per row, rows contiguous.
 __device__ __forceinline__ size_t fold_offset(size_t bh, int Npad, int n) {
-    return ((bh * (size_t)(Npad / 8) + (size_t)(n / 8)) * 256u) + (size_t)(n % 8) * 16u;
+    return (bh * (size_t)Npad + (size_t)n) * 16u;
 }
 
 template <int D>
@@ -111,12 +111,9 @@ fa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __re
         const float v = (n < N) ? -lse[(size_t)bh * N + n] * inv_scale : -0x1.0p100f;
         const size_t off = fold_offset((size_t)bh, Npad, n);
         uint8_t* lf = folds + off;
-        uint8_t* df = folds + (size_t)BH * Npad * 32u + off;
-        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+        uint8_t* df = folds + (size_t)BH * Npad * 16u + off;
         *reinterpret_cast<uint4*>(lf) = fold_record(v);
-        *reinterpret_cast<uint4*>(lf + 128) = z;
         *reinterpret_cast<uint4*>(df) = fold_record((n < N) ? -dot : 0.f);
-        *reinterpret_cast<uint4*>(df + 128) = z;
     }
     float4* acc = reinterpret_cast<float4*>(dq_acc + ((size_t)bh * Npad + n) * D + sub * 8);
     acc[0] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -161,19 +158,21 @@ struct BwdCfg {
     static constexpr int KT = 128;                    // keys per CTA
     static constexpr int BMQ = (D == 128) ? 64 : 128; // query rows per step
     static constexpr int NQS = 3;                     // Q/dO ring depth
-    static constexpr int NDS = 1;                     // dS buffers
+    static constexpr int NDS = (D == 64) ? 2 : 1;     // dS buffers (shared memory allowing)
     static constexpr uint32_t KTILE = 128u * D * 2u;  // K or V tile bytes
     static constexpr uint32_t KCHUNK = 128u * 128u;   // 128 rows x 64 cols
     static constexpr uint32_t QTILE = (uint32_t)BMQ * D * 2u;
     static constexpr uint32_t QCHUNK = (uint32_t)BMQ * 128u;  // BMQ rows x 64 cols
-    static constexpr uint32_t FOLD_BYTES = (uint32_t)BMQ * 32u;  // fold records of a query block
+    static constexpr uint32_t FOLD_BYTES = (uint32_t)BMQ * 16u;  // fold records of a query block
     // stage: [Q][dO][-LSE/scale fold][-D fold], padded to 1024
     static constexpr uint32_t STAGE_BYTES = ((2 * QTILE + 2 * FOLD_BYTES) + 1023u) / 1024u * 1024u;
     // dS tile: 128 key rows, BMQ queries contiguous per row, in 64-query (128-byte) regions
     static constexpr uint32_t DS_BYTES = (uint32_t)BMQ * 128u * 2u;
     static constexpr uint32_t DSREG = 128u * 128u;           // one 64-query region
-    static constexpr uint32_t DQS_BYTES = (uint32_t)BMQ * D * 4u;  // fp32 dQ staging
     static constexpr uint32_t DQBOX = (uint32_t)BMQ * 128u;  // one 32-column fp32 box
+    // fp32 dQ staging: d=64 drains one box at a time through one box of staging (the shared
+    // memory goes to the second dS buffer); d=128 stages all four boxes at once.
+    static constexpr uint32_t DQS_BYTES = (D == 64) ? DQBOX : (uint32_t)BMQ * D * 4u;
     static constexpr uint32_t OFF_K = 0;
     static constexpr uint32_t OFF_V = OFF_K + KTILE;
     static constexpr uint32_t OFF_ST = OFF_V + KTILE;
@@ -332,8 +331,8 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     ptx::tma_load_3d_hint(base + C::QTILE + ch * C::QCHUNK, &tm_do, b_q, ch * 64, q0,
                                           bhq, pol_keep);
                 }
-                const uint8_t* lf = folds + ((size_t)bhq * (size_t)(sh.Npad / 8) + (size_t)(q0 / 8)) * 256u;
-                const uint8_t* df = lf + (size_t)sh.BHq * sh.Npad * 32u;
+                const uint8_t* lf = folds + ((size_t)bhq * (size_t)sh.Npad + (size_t)q0) * 16u;
+                const uint8_t* df = lf + (size_t)sh.BHq * sh.Npad * 16u;
                 ptx::bulk_load(base + 2 * C::QTILE, lf, C::FOLD_BYTES, b_q);
                 ptx::bulk_load(base + 2 * C::QTILE + C::FOLD_BYTES, df, C::FOLD_BYTES, b_q);
                 ++issued;
@@ -360,7 +359,9 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             const uint64_t ds_mn = ptx::sdesc_sw128(s_ds, C::DSREG, 1024);
             // fold MMAs: A = ones tile, B = a stage's fold records (both no-swizzle K-major)
             const uint64_t ones_d = ptx::sdesc_noswz(ptx::smem_addr(smem + C::OFF_ONES), 128, 256);
-            const uint64_t fold_d = ptx::sdesc_noswz(s_st + 2 * C::QTILE, 128, 256);
+            // A fold record is one 16-byte core-matrix row (k = 0..7); LBO = 0 makes the second K
+            // half read the same bytes, which the ones tile's zero second half cancels.
+            const uint64_t fold_d = ptx::sdesc_noswz(s_st + 2 * C::QTILE, 0, 128);
             auto issue_s_dp = [&](int si) {
                 const uint32_t st_off = (uint32_t)(si % C::NQS) * C::STAGE_BYTES;
                 const uint64_t qd = ptx::sdesc_add(st_kmaj, st_off);
@@ -632,12 +633,12 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             ptx::tmem_wait_ld(b);
             ptx::tc_fence_before();
             ptx::mbar_arrive(ptx::smem_addr(&bars->dq_free));
-            // The previous step's reduce must have finished reading the staging tile.
-            if (si > 0) {
-                if (r == 0) ptx::bulk_wait_read_all();
-                ptx::named_bar_sync(2, 128);
-            }
             if (D == 128) {
+                // The previous step's reduce must have finished reading the staging tile.
+                if (si > 0) {
+                    if (r == 0) ptx::bulk_wait_read_all();
+                    ptx::named_bar_sync(2, 128);
+                }
                 // lane r = head-dim column e; a/b hold query rows 0-31 / 32-63.
                 // fp32 box (e / 32): [BMQ rows x 128 B], element e at byte 4 (e % 32).
                 uint8_t* box = dqs + (r >> 5) * C::DQBOX;
@@ -648,22 +649,43 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     *reinterpret_cast<uint32_t*>(box + sw128_offset((uint32_t)j, u) + wb) = a[j];
                     *reinterpret_cast<uint32_t*>(box + sw128_offset((uint32_t)(32 + j), u) + wb) = b[j];
                 }
+                ptx::fence_proxy_async_smem();
+                ptx::named_bar_sync(2, 128);
+                if (r == 0) {
+                    for (int bx = 0; bx < D / 32; ++bx)
+                        ptx::tma_reduce_add_3d(&tm_dqacc, ptx::smem_addr(dqs + bx * C::DQBOX), bx * 32,
+                                               q0, bhq);
+                    ptx::bulk_commit();
+                }
             } else {
-                // lane r = query row; a/b hold head-dim columns 0-31 / 32-63 (one fp32 box each).
+                // lane r = query row; a/b hold head-dim columns 0-31 / 32-63, one fp32 box each,
+                // staged one after the other through the single box of staging.
+                if (si > 0) {
+                    if (r == 0) ptx::bulk_wait_read_all();
+                    ptx::named_bar_sync(2, 128);
+                }
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
+                for (int u = 0; u < 8; ++u)
                     *reinterpret_cast<uint4*>(dqs + sw128_offset((uint32_t)r, (uint32_t)u)) =
                         make_uint4(a[4 * u], a[4 * u + 1], a[4 * u + 2], a[4 * u + 3]);
-                    *reinterpret_cast<uint4*>(dqs + C::DQBOX + sw128_offset((uint32_t)r, (uint32_t)u)) =
-                        make_uint4(b[4 * u], b[4 * u + 1], b[4 * u + 2], b[4 * u + 3]);
+                ptx::fence_proxy_async_smem();
+                ptx::named_bar_sync(2, 128);
+                if (r == 0) {
+                    ptx::tma_reduce_add_3d(&tm_dqacc, ptx::smem_addr(dqs), 0, q0, bhq);
+                    ptx::bulk_commit();
+                    ptx::bulk_wait_read_all();
                 }
-            }
-            ptx::fence_proxy_async_smem();
-            ptx::named_bar_sync(2, 128);
-            if (r == 0) {
-                for (int bx = 0; bx < D / 32; ++bx)
-                    ptx::tma_reduce_add_3d(&tm_dqacc, ptx::smem_addr(dqs + bx * C::DQBOX), bx * 32, q0, bhq);
-                ptx::bulk_commit();
+                ptx::named_bar_sync(2, 128);
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    *reinterpret_cast<uint4*>(dqs + sw128_offset((uint32_t)r, (uint32_t)u)) =
+                        make_uint4(b[4 * u], b[4 * u + 1], b[4 * u + 2], b[4 * u + 3]);
+                ptx::fence_proxy_async_smem();
+                ptx::named_bar_sync(2, 128);
+                if (r == 0) {
+                    ptx::tma_reduce_add_3d(&tm_dqacc, ptx::smem_addr(dqs), 32, q0, bhq);
+                    ptx::bulk_commit();
+                }
             }
         }
         if (r == 0) ptx::bulk_wait_all();

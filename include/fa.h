@@ -115,10 +115,10 @@ fa_status fa_forward_splitkv(const void* q, const void* k, const void* v, void* 
                              struct CUstream_st* stream);
 
 /*
- * Bytes of device workspace fa_backward needs for these sizes: two 32-byte records per query
+ * Bytes of device workspace fa_backward needs for these sizes: two 16-byte records per query
  * row holding -LSE/scale and -D_i (D_i = O_i . dO_i) as exact three-part bf16 sums, [B*H, Npad]
  * each, and an fp32 dQ accumulator [B*H, Npad, d]; Npad = N rounded up to 128. In total
- * B*H*Npad*(64 + 4d) bytes. Returns 0 for invalid sizes or when B*H*N == 0.
+ * B*H*Npad*(32 + 4d) bytes. Returns 0 for invalid sizes or when B*H*N == 0.
  */
 size_t fa_backward_workspace_bytes(int B, int H, int N, int d);
 
@@ -168,7 +168,7 @@ fa_status fa_backward_ex(const void* q, const void* k, const void* v, const void
  * library routine).
  *   - Sizes whose workspace (fa_backward_workspace_bytes) exceeds FA_NOALLOC_SCRATCH_BYTES are
  *     rejected with FA_ERR_UNSUPPORTED before anything is launched (for example B*H = 64,
- *     N = 2048, d = 64 needs 41.9 MB and fits; B*H = 64, N = 4096, d = 128 needs 151 MB and
+ *     N = 2048, d = 64 needs 37.7 MB and fits; B*H = 64, N = 4096, d = 128 needs 143 MB and
  *     does not). Other argument errors are those of fa_backward.
  *   - The first call on a device looks up the array's device address (with that device
  *     current) and caches it; make that first call before any stream capture.

@@ -70,7 +70,7 @@ def test_noalloc_matches_allocating_backward_twice(api):
 
 
 def test_noalloc_rejects_sizes_beyond_its_workspace(api):
-    # B*H = 64, N = 4096, d = 128 needs 151 MB of workspace: rejected before any launch
+    # B*H = 64, N = 4096, d = 128 needs 143 MB of workspace: rejected before any launch
     # (the pointers are never used, so fake aligned addresses are enough).
     B, H, N, d = 4, 16, 4096, 128
     assert api.backward_workspace_bytes(B, H, N, d) > api.NOALLOC_SCRATCH_BYTES
