@@ -25,8 +25,8 @@ FA_ERR_TIMEOUT = 5
 # Every symbol include/fa.h declares.
 EXPORTS = ("fa_forward", "fa_forward_ex", "fa_forward_splitkv_workspace_bytes",
            "fa_forward_splitkv", "fa_backward_workspace_bytes", "fa_backward",
-           "fa_backward_ex", "fa_backward_noalloc", "fa_status_string", "fa_last_cuda_error",
-           "fa_device_error")
+           "fa_backward_ex", "fa_backward_noalloc", "fa_selftest_wait_timeout",
+           "fa_status_string", "fa_last_cuda_error", "fa_device_error")
 
 # Size of the library's own backward workspace (FA_NOALLOC_SCRATCH_BYTES in include/fa.h).
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
@@ -77,6 +77,8 @@ def library(path: str | None = None):
         lib.fa_backward_ex.restype = I
         lib.fa_backward_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, P]
         lib.fa_backward_noalloc.restype = I
+        lib.fa_selftest_wait_timeout.argtypes = [ctypes.c_uint, P]
+        lib.fa_selftest_wait_timeout.restype = I
         lib.fa_status_string.argtypes = [I]
         lib.fa_status_string.restype = ctypes.c_char_p
         lib.fa_last_cuda_error.argtypes = []
@@ -145,6 +147,14 @@ def backward_noalloc_raw(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, causal, 
 
 def backward_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
     return int(library().fa_backward_workspace_bytes(B, H, N, d))
+
+
+def selftest_wait_timeout(limit_us: int, stream: int | None = None) -> None:
+    """Launch the failure-path diagnostic (a bounded wait that runs out; see include/fa.h)."""
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    _check(library().fa_selftest_wait_timeout(int(limit_us), stream), "fa_selftest_wait_timeout")
 
 
 def device_error(stream: int | None = None) -> int:

@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "../../include/fa.h"
+#include "fa_common.cuh"
 #include "fa_launch.h"
 
 namespace {
@@ -186,6 +187,21 @@ fa_status get_noalloc_scratch(void** out) {
     }
     *out = g_noalloc_ptr[dev];
     return FA_OK;
+}
+
+// Diagnostic: one warp waits, through the attention kernels' bounded wait, on an mbarrier that
+// nothing ever arrives on; the wait gives up after limit_ns, records kDevTimeoutLoad in the error
+// word and the kernel returns.
+__global__ void fa_wait_selftest_kernel(int* err, unsigned long long limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        fa::ptx::mbar_init(fa::ptx::smem_addr(&bar), 1);
+        abort_flag = 0;
+        fa::ptx::fence_barrier_init();
+    }
+    __syncthreads();
+    fa::warp_wait(fa::ptx::smem_addr(&bar), 0, &abort_flag, err, fa::kDevTimeoutLoad, limit_ns);
 }
 
 }  // namespace
@@ -391,6 +407,18 @@ fa_status fa_backward_noalloc(const void* q, const void* k, const void* v, const
     if ((st = get_noalloc_scratch(&scratch)) != FA_OK) return st;
     return fa_backward(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, causal, scale, scratch,
                        stream);
+}
+
+fa_status fa_selftest_wait_timeout(unsigned int limit_us, struct CUstream_st* stream) {
+    if (limit_us == 0 || limit_us > 1000000u) return FA_ERR_INVALID_ARG;
+    int* err = nullptr;
+    fa_status st = get_err_ptr(&err);
+    if (st != FA_OK) return st;
+    fa_wait_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        err, (unsigned long long)limit_us * 1000ull);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    return FA_OK;
 }
 
 fa_status fa_device_error(struct CUstream_st* stream, int* code) {

@@ -20,16 +20,16 @@ enum DeviceError : int {
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 
 // Wait for phase `parity` of mbarrier `bar`. Returns false (and raises the CTA abort flag
-// and the global error word) if the limit expires, or if another role already aborted.
+// and the global error word) if `limit_ns` expires, or if another role already aborted.
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                           int* err, int code) {
+                                           int* err, int code, uint64_t limit_ns = kWaitLimitNs) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = ptx::globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (ptx::mbar_try_wait(bar, parity)) return true;
         if ((it & 15u) == 0) {
             if (*abort_flag) return false;
-            if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+            if (ptx::globaltimer_ns() - t0 > limit_ns) {
                 *abort_flag = 1;
                 atomicCAS(err, 0, code);
                 return false;
@@ -40,8 +40,8 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
 
 // wait_phase for a whole warp: every lane polls, and the outcome is made warp-uniform.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int* err, int code) {
-    return __all_sync(0xffffffffu, wait_phase(bar, parity, abort_flag, err, code));
+                                          int* err, int code, uint64_t limit_ns = kWaitLimitNs) {
+    return __all_sync(0xffffffffu, wait_phase(bar, parity, abort_flag, err, code, limit_ns));
 }
 
 // Byte offset of the 16-byte unit `u` (0..7) of row `r` inside a 128-byte-swizzled tile whose

@@ -184,6 +184,15 @@ fa_status fa_backward_noalloc(const void* q, const void* k, const void* v, const
                               int B, int H, int N, int d, int causal, float scale,
                               struct CUstream_st* stream);
 
+/*
+ * Diagnostic of the failure path (no counterpart in the pages). Launches one warp that waits,
+ * through the same bounded mbarrier wait the attention kernels use, on a barrier nothing ever
+ * arrives on; after `limit_us` microseconds (1 .. 1000000) the wait gives up, records code 1
+ * (load) in the device error word and the kernel returns, leaving the context usable. Read the
+ * code with fa_device_error. Nothing faults or hangs.
+ */
+fa_status fa_selftest_wait_timeout(unsigned int limit_us, struct CUstream_st* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* fa_status_string(fa_status s);
 
