@@ -7,20 +7,24 @@
 //   dV = P^T dO,  dP = dO V^T,  D_i = O_i . dO_i,  dS = P (.) (dP - D),
 //   dQ = scale dS K,  dK = scale dS^T Q  (the scale factors follow from S = scale Q K^T).
 //   Work is partitioned over key tiles (column-oriented): each CTA owns one 128-key tile
-//   K_j, V_j and its dK_j, dV_j; contributions to dQ from different key tiles are added in
-//   fp32 with (bulk) atomic reductions.
+//   K_j, V_j of one KV head and its dK_j, dV_j, summed over every query head that reads the
+//   KV head (grouped heads) and over the query steps that can see the tile (query offset,
+//   causal diagonal, sliding window); contributions to dQ from different key tiles are added
+//   in fp32 with (bulk) atomic reductions.
 //
 // Three kernels:
-//   fa_bwd_pre_kernel   D_i = sum_e dO_ie O_ie, LSE * log2(e) into a padded row-statistics
-//                       buffer (+inf / 0 on padded rows), dQ accumulator zeroed.
-//   fa_bwd_kernel<D>    per key tile: loop over query steps (from the diagonal when causal):
-//                       S^T = K Q_i^T and dP^T = V dO_i^T (tcgen05, TMEM); P^T (to TMEM) and
-//                       dS^T (to smem) by the compute warpgroup, one thread per key row;
-//                       dV += P^T dO_i (A from TMEM), dK += dS^T Q_i (A from smem), the dQ_i
-//                       partial (A/B from smem) drained from TMEM by a second warpgroup and
-//                       added into the fp32 dQ accumulator with a TMA bulk reduce-add.
-//                       The next step's S^T/dP^T are issued as soon as the compute warps
-//                       have read the current ones, so they overlap dV/dK/dQ of this step.
+//   fa_bwd_pre_kernel   D_i = sum_e dO_ie O_ie; per query row the fold records of -LSE/scale
+//                       and -D (exact three-part bf16 sums); dQ accumulator zeroed.
+//   fa_bwd_kernel<D>    per key tile: loop over query steps:
+//                       S'^T = K Q_i^T + fold and dP'^T = V dO_i^T + fold (tcgen05, TMEM; the
+//                       fold MMA against a ones tile subtracts LSE and D inside the MMA);
+//                       P^T = exp2(c S'^T) (to TMEM) and dS^T = P^T (.) dP'^T (to smem) by two
+//                       compute warpgroups, one thread per key row; dV += P^T dO_i (A from
+//                       TMEM), dK += dS^T Q_i (A from smem), the dQ_i partial (A/B from smem)
+//                       drained from TMEM by a third warpgroup and added into the fp32 dQ
+//                       accumulator with a TMA bulk reduce-add. The next step's S'^T/dP'^T
+//                       are issued as soon as the compute warps have read the current ones, so
+//                       they overlap dV/dK/dQ of this step; Q/dO ring 3 deep.
 //   fa_bwd_dq_kernel    dQ = bf16(scale * dQacc).
 //
 // d = 128: query steps of 64 rows, the dQ partial computed transposed (dQ^T = K^T dS^T,
@@ -489,7 +493,6 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         bool ok = true;
         StepCursor cur = first_step();
         for (int si = 0; si < nsteps; ++si, next_step(cur)) {
-            const int st = si % C::NQS;
             const int q0 = cur.qi * C::BMQ;
             // S'^T and dP'^T already carry the row statistics (fold MMAs): nothing else to read.
             ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->s_full), (uint32_t)si & 1u,

@@ -12,19 +12,27 @@
 //   at the end O = a / l and LSE = m + ln l. Tiles wholly above the causal diagonal are
 //   skipped; only the diagonal tile and the ragged last tile are masked elementwise.
 //
+// Grouped KV heads and the query offset (query row i at key position Tk - Tq + i) follow the
+// same page's "Details worth noticing"; the optional sliding window keeps keys at positions
+// >= position - window (its "Stretch exercises", item 3); the split-KV variant writes per-chunk
+// partials merged by the rule of its section "Decode is different: flash-decoding".
+//
 // GB300 mapping: a persistent grid of one CTA per SM; a CTA walks work units (one unit = 256
-// query rows of one (batch, head) = two 128-row Q tiles) so that the next unit's loads and
-// first score MMAs overlap the current unit's epilogue. Roles:
-//   warp 0      TMA producer: Q tiles once, then K_j / V_j into separate mbarrier rings
+// query rows of one query head = two 128-row Q tiles; in the split variant, one key chunk of
+// them) so that the next unit's loads and first score MMAs overlap the current unit's
+// epilogue. Roles:
+//   warp 0      TMA producer: Q tiles once per unit, then K_j / V_j into separate mbarrier rings
 //   warp 1      MMA issuer for S_t = Q_t K_j^T (tcgen05.mma, fp32 in TMEM)
-//   warp 3      MMA issuer for O_t += P_t V_j
+//   warp 3      MMA issuer for O_t += P_t V_j (A = P from TMEM)
 //   warp 2      TMEM allocation / release
 //   warps 4-7   softmax for Q tile 0, warps 8-11 softmax for Q tile 1: one thread per row,
 //               the whole row of S read from TMEM into registers (no cross-thread reduction),
-//               exp2 with log2(e) folded into the scale, P written back to TMEM as bf16
-//               over the S columns, O rescaled in TMEM when the row max moves, and the
-//               epilogue (O / l -> bf16 -> swizzled smem -> TMA store; LSE -> global).
-// TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 and O_1 after column 256.
+//               exp2 with log2(e) folded into the scale, P written back to TMEM as bf16, O
+//               rescaled in TMEM when some row of the warp raises its max, and the epilogue
+//               (O / l -> bf16 -> swizzled smem -> TMA store; LSE -> global; or, split, the
+//               fp32 partial O and LSE).
+// TMEM (512 columns): d=64: S_0, S_1 [0,256), O_0, O_1 [256,384), P_0, P_1 [384,512);
+// d=128: S_0, S_1 [0,256), O_0, O_1 [256,512), P written over S.
 #include <algorithm>
 
 #include <cuda_bf16.h>
