@@ -505,10 +505,6 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                         s[96 + k] = __uint_as_float(u3[k]);
                     }
                 }
-                if (C::P_SEPARATE) {
-                    ptx::tc_fence_before();
-                    ptx::mbar_arrive(b_s_free);  // S_t columns may be overwritten now
-                }
                 const int key0 = j * C::BN;
                 // Elementwise masking only on tiles that cross the causal diagonal, the window's
                 // left edge or the end of the keys.
@@ -560,6 +556,13 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     for (int i = 0; i < 4; ++i) pk[k / 2 + i] = ptx::pack_bf16x2(s[k + 2 * i], s[k + 2 * i + 1]);
                 }
                 l = l * alpha + (((r0 + r1) + (r2 + r3)) + ((r4 + r5) + (r6 + r7)));
+                if (C::P_SEPARATE) {
+                    // S_t (in registers since the loads) may be overwritten now. Signalled after
+                    // the exp2 phase, not before the row max: the next S_t has ample slack, and
+                    // the fence and arrival off the max -> exp2 chain gave +2-4 % at d = 64.
+                    ptx::tc_fence_before();
+                    ptx::mbar_arrive(b_s_free);
+                }
                 if (j > jb) {
                     // O_t += P_t(j-1) V must be complete before P_t is overwritten (separate P
                     // columns) and before O_t is rescaled.
