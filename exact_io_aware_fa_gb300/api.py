@@ -292,3 +292,42 @@ def backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = 
                              float(scale), ws_ptr, s)
     _check(st, "fa_backward_ex")
     return dq, dk, dv
+
+
+# ---- autograd -----------------------------------------------------------------------------
+
+def _autograd_function():
+    import torch
+
+    class _FlashAttention(torch.autograd.Function):
+        """Forward saves (q, k, v, o, lse); backward recomputes through fa_backward_ex."""
+
+        @staticmethod
+        def forward(ctx, q, k, v, causal, scale, window):
+            o, lse = forward(q, k, v, causal=causal, scale=scale, window=window)
+            ctx.save_for_backward(q, k, v, o, lse)
+            ctx.causal, ctx.scale, ctx.window = causal, scale, window
+            return o
+
+        @staticmethod
+        def backward(ctx, do):
+            q, k, v, o, lse = ctx.saved_tensors
+            dq, dk, dv = backward(q, k, v, o, lse, do.contiguous(), causal=ctx.causal,
+                                  scale=ctx.scale, window=ctx.window)
+            return dq, dk, dv, None, None, None
+
+    return _FlashAttention
+
+
+_FN = None
+
+
+def attention(q, k, v, causal: bool = False, scale: float | None = None, window: int = -1):
+    """Differentiable O = attention(q, k, v) (shapes as ``forward``); gradients through the
+    recompute backward."""
+    global _FN
+    if _FN is None:
+        _FN = _autograd_function()
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    return _FN.apply(q, k, v, bool(causal), float(scale), int(window))

@@ -36,6 +36,22 @@ fa_status cuda_fail(cudaError_t e) {
     return FA_ERR_CUDA;
 }
 
+// Make the current device's primary context current on the calling thread before any driver
+// call (tensor-map encoding needs one). A thread that only ever selected a device -- e.g. a
+// framework's worker thread for the default device -- may have none bound yet.
+thread_local int t_bound_dev = -1;
+fa_status bind_context() {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev != t_bound_dev) {
+        e = cudaSetDevice(dev);
+        if (e != cudaSuccess) return cuda_fail(e);
+        t_bound_dev = dev;
+    }
+    return FA_OK;
+}
+
 // Driver entry point for cuTensorMapEncodeTiled, resolved through the runtime so the
 // library does not link libcuda directly.
 fa_status get_encode(EncodeTiledFn* out) {
@@ -253,6 +269,7 @@ fa_status fa_forward_splitkv(const void* q, const void* k, const void* v, void* 
     if (nsplit > 1 && workspace && !aligned(workspace, 256)) return FA_ERR_ALIGNMENT;
     if (((long long)Tq + 255) / 256 * sh.BHq * nsplit > INT_MAX) return FA_ERR_UNSUPPORTED;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if ((st = bind_context()) != FA_OK) return st;
     fa::FwdLaunch a;
     std::memset(&a, 0, sizeof a);
     if ((st = make_map(&a.tm_q, q, sh.BHq, Tq, d, 128)) != FA_OK) return st;
@@ -336,6 +353,7 @@ fa_status fa_backward_ex(const void* q, const void* k, const void* v, const void
         return FA_ERR_ALIGNMENT;
     if (workspace && !aligned(workspace, 256)) return FA_ERR_ALIGNMENT;
     const int Npad = (Tq + 127) / 128 * 128;
+    if ((st = bind_context()) != FA_OK) return st;
     fa::BwdLaunch a;
     std::memset(&a, 0, sizeof a);
     const int q_rows = (d == 128) ? 64 : 128;  // query rows per backward step

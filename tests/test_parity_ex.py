@@ -153,3 +153,53 @@ def test_window_covers_unseen_key_tiles(env):
     ref = orc.backward_ex(bits["q"], bits["k"], bits["v"], bits["do"], True, scale, window)
     for name, a, b in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
         assert_close_grad(to_f64(a), b, name, "unseen tiles")
+
+
+def test_autograd_wrapper_matches_raw_calls(env):
+    """api.attention (torch.autograd) gives the same O and the same gradients as the direct
+    forward / backward calls."""
+    import torch
+    from exact_io_aware_fa_gb300 import synthetic
+    api, _ = env
+    bits = synthetic.attention_inputs_ex(1, 4, 2, 200, 300, 64, seed=17, with_dout=True)
+    q, k, v = (to_dev(bits[n]).requires_grad_(True) for n in ("q", "k", "v"))
+    do = to_dev(bits["do"])
+    o = api.attention(q, k, v, causal=True)
+    o.backward(do)
+    o2, lse2 = api.forward(q.detach(), k.detach(), v.detach(), causal=True)
+    dq2, dk2, dv2 = api.backward(q.detach(), k.detach(), v.detach(), o2, lse2, do, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o.detach(), o2)
+    assert torch.equal(q.grad, dq2) and torch.equal(k.grad, dk2) and torch.equal(v.grad, dv2)
+
+
+def test_calls_from_a_new_host_thread(env):
+    """A host thread that never touched CUDA before (as a framework's worker thread) can call
+    forward and backward: the library binds the device's context itself."""
+    import threading
+    import torch
+    from exact_io_aware_fa_gb300 import synthetic
+    api, _ = env
+    bits = synthetic.attention_inputs(1, 2, 300, 128, seed=23, with_dout=True)
+    q, k, v, do = (to_dev(bits[n]) for n in ("q", "k", "v", "do"))
+    ref_o, ref_lse = api.forward(q, k, v, causal=True)
+    ref_g = api.backward(q, k, v, ref_o, ref_lse, do, causal=True)
+    torch.cuda.synchronize()
+    out = {}
+
+    def work():
+        try:
+            o, lse = api.forward(q, k, v, causal=True)
+            out["g"] = api.backward(q, k, v, o, lse, do, causal=True)
+            out["o"] = o
+            torch.cuda.synchronize()
+        except Exception as e:  # reported below
+            out["err"] = e
+
+    t = threading.Thread(target=work)
+    t.start()
+    t.join()
+    assert "err" not in out, out.get("err")
+    assert torch.equal(out["o"], ref_o)
+    for a, b in zip(out["g"], ref_g):
+        assert torch.equal(a, b)
