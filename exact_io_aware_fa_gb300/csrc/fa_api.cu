@@ -172,11 +172,13 @@ fa_status check_shape(int B, int Hq, int Hkv, int Tq, int Tk, int d, int causal,
     return FA_OK;
 }
 
-// Backward workspace: two 16-byte fold records per (padded) query row, then the fp32 dQ
-// accumulator.
+// Backward workspace: two 16-byte fold records per (padded) query row, the fp32 dQ
+// accumulator, then a 256-byte tail holding the main kernel's unit counter.
+constexpr size_t kSchedBytes = 256;
 size_t workspace_bytes(long long bhq, long long tq, int d) {
     const size_t npad = ((size_t)tq + 127) / 128 * 128;
-    return 2 * (size_t)bhq * npad * 16u + (size_t)bhq * npad * (size_t)d * sizeof(float);
+    return 2 * (size_t)bhq * npad * 16u + (size_t)bhq * npad * (size_t)d * sizeof(float) +
+           kSchedBytes;
 }
 
 constexpr float kLog2e = 1.4426950408889634074f;
@@ -379,6 +381,7 @@ fa_status fa_backward_ex(const void* q, const void* k, const void* v, const void
     a.dq = dq;
     a.folds = ws;
     a.dq_acc = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + 2 * (size_t)sh.BHq * (size_t)Npad * 16u);
+    a.sched = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(ws) + ws_bytes - kSchedBytes);
     if ((st = make_map(&a.tm_dqacc, a.dq_acc, sh.BHq, Npad, d, q_rows, true)) != FA_OK) {
         if (owned) cudaFreeAsync(ws, s);
         return st;

@@ -6,16 +6,17 @@
 //   P_ij = exp(S_ij - L_i) rebuilt tile by tile from Q, K and the saved L = LSE;
 //   dV = P^T dO,  dP = dO V^T,  D_i = O_i . dO_i,  dS = P (.) (dP - D),
 //   dQ = scale dS K,  dK = scale dS^T Q  (the scale factors follow from S = scale Q K^T).
-//   Work is partitioned over key tiles (column-oriented): each CTA owns one 128-key tile
+//   Work is partitioned over key tiles (column-oriented): a work unit is one 128-key tile
 //   K_j, V_j of one KV head and its dK_j, dV_j, summed over every query head that reads the
 //   KV head (grouped heads) and over the query steps that can see the tile (query offset,
 //   causal diagonal, sliding window); contributions to dQ from different key tiles are added
-//   in fp32 with (bulk) atomic reductions.
+//   in fp32 with (bulk) atomic reductions. The main kernel is persistent: one CTA per SM
+//   takes units from an atomic counter until none are left.
 //
 // Three kernels:
 //   fa_bwd_pre_kernel   D_i = sum_e dO_ie O_ie; per query row the fold records of -LSE/scale
 //                       and -D (exact three-part bf16 sums); dQ accumulator zeroed.
-//   fa_bwd_kernel<D>    per key tile: loop over query steps:
+//   fa_bwd_kernel<D>    per unit (key tile): loop over query steps:
 //                       S'^T = K Q_i^T + fold and dP'^T = V dO_i^T + fold (tcgen05, TMEM; the
 //                       fold MMA against a ones tile subtracts LSE and D inside the MMA);
 //                       P^T = exp2(c S'^T) (to TMEM) and dS^T = P^T (.) dP'^T (to smem) by two
@@ -24,12 +25,15 @@
 //                       drained from TMEM by a third warpgroup and added into the fp32 dQ
 //                       accumulator with a TMA bulk reduce-add. The next step's S'^T/dP'^T
 //                       are issued as soon as the compute warps have read the current ones, so
-//                       they overlap dV/dK/dQ of this step; Q/dO ring 3 deep.
+//                       they overlap dV/dK/dQ of this step; Q/dO ring 3 deep. dV and scale*dK
+//                       leave through the drain warps while the next unit starts.
 //   fa_bwd_dq_kernel    dQ = bf16(scale * dQacc).
 //
 // d = 128: query steps of 64 rows, the dQ partial computed transposed (dQ^T = K^T dS^T,
 //          M = d = 128) so its TMEM lanes are head-dim columns.
 // d = 64:  query steps of 128 rows, dQ = dS K with M = 128 query rows.
+#include <algorithm>
+
 #include "fa_common.cuh"
 #include "fa_launch.h"
 
@@ -83,9 +87,11 @@ template <int D>
 __global__ void __launch_bounds__(256)
 fa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
                   const float* __restrict__ lse, uint8_t* __restrict__ folds,
-                  float* __restrict__ dq_acc, int N, int Npad, int BH, float inv_scale) {
+                  float* __restrict__ dq_acc, unsigned* __restrict__ sched, int N, int Npad, int BH,
+                  float inv_scale) {
     constexpr int TPR = D / 8;            // threads per row
     constexpr int RPB = 256 / TPR;        // rows per block
+    if (blockIdx.x == 0 && threadIdx.x == 0) *sched = 0u;  // the main kernel's unit counter
     const int sub = threadIdx.x % TPR;
     const long long row_global = (long long)blockIdx.x * RPB + threadIdx.x / TPR;  // over BH*Npad
     const bool valid_row = row_global < (long long)BH * Npad;
@@ -154,7 +160,8 @@ fa_bwd_dq_kernel(const float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ d
 // Problem shape of the backward: as the forward (query head bh_q reads KV head bh_q / group,
 // query row i at key position offset + i, optional window), seen from a key tile.
 struct BwdShape {
-    int Tq, Tk, Npad, Hq, Hkv, group, offset, window, BHq, BHkv, nkb, kb_major;
+    int Tq, Tk, Npad, Hq, Hkv, group, offset, window, BHq, BHkv, nkb;
+    int kv_chunk;  // KV heads per chunk of the unit order (1: head by head)
 };
 
 template <int D>
@@ -187,6 +194,7 @@ struct BwdCfg {
     static constexpr uint32_t SMEM_BYTES = OFF_BAR + 512 + 1024;
     static_assert(NQS <= 3 && NDS >= 1 && NDS <= 2, "barrier arrays");
     static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+    static_assert(DQS_BYTES >= (uint32_t)(D / 64) * KCHUNK, "dV / dK epilogue staged in the dQ staging");
     static constexpr int THREADS = 512;
     // TMEM columns. d=128: dV[0,128) dK[128,256) S^T[256,320) dP^T[320,384) dQ^T[384,448)
     // P^T[448,480). d=64: dV[0,64) dK[64,128) S^T[128,256) dP^T[256,384) dQ[384,448) P^T[448,512).
@@ -199,24 +207,82 @@ struct BwdCfg {
 };
 
 struct BwdBars {
-    uint64_t kv_full;
+    uint64_t kv_full, kv_empty;       // per unit: K/V landed / every MMA reading them done
+    uint64_t dkv_full, dkv_free;      // per unit: dV/dK final in TMEM / read by the epilogue
     uint64_t q_full[3], q_empty[3];
     uint64_t s_full, s_free, p_ready, mma_done;
     uint64_t ds_free[2];  // one per dS buffer (NDS <= 2)
     uint64_t dq_full, dq_free;
     uint64_t final_bar;
+    uint64_t uid_full[4], uid_empty[4];  // unit-id ring: published by the producer, read by all
+    int uid[4];
     uint32_t tmem_base;
     int abort_flag;
 };
 
+// One work unit: KV head bh_kv, keys [key0, key0 + 128). It visits every query head of the
+// group and, for each, the query steps whose rows can see some key of the tile: from the causal
+// diagonal (query position offset + q >= key) to the window's reach (position - window <= key).
+// A tile no query sees has no steps and stores zero gradients. Unit order: the KV heads are cut
+// into chunks of kv_chunk heads; chunk by chunk, and inside a chunk key tile by key tile. With
+// one head per chunk the walk is head by head (neighbouring units share their query heads' Q/dO
+// in L2, the best order when every unit costs the same); under a causal mask larger chunks put
+// each chunk's costliest tiles (whose queries reach back to the diagonal) first and its cheapest
+// last, so that the launch ends on short units, while a chunk's Q/dO still fits in L2.
+struct BwdUnit {
+    int bh_kv, key0, i0, i1, nsteps_g, nsteps, bhq_base;
+};
+
+template <int D, bool CAUSAL, bool WINDOW>
+__device__ __forceinline__ BwdUnit bwd_unit(int u, const BwdShape& sh) {
+    using C = BwdCfg<D>;
+    BwdUnit w;
+    const uint32_t per_chunk = (uint32_t)sh.kv_chunk * (uint32_t)sh.nkb;
+    const uint32_t chunk = (uint32_t)u / per_chunk;
+    const uint32_t r = (uint32_t)u - chunk * per_chunk;
+    const uint32_t h0 = chunk * (uint32_t)sh.kv_chunk;
+    const uint32_t hc = min((uint32_t)sh.kv_chunk, (uint32_t)sh.BHkv - h0);  // last chunk: fewer
+    w.bh_kv = (int)(h0 + r % hc);
+    const int kb = (int)(r / hc);
+    w.key0 = kb * C::KT;
+    const int nq_total = (sh.Tq + C::BMQ - 1) / C::BMQ;
+    w.i0 = CAUSAL ? max(0, w.key0 - sh.offset) / C::BMQ : 0;
+    w.i1 = nq_total - 1;
+    if (WINDOW) {
+        const int reach = w.key0 + C::KT - 1 + sh.window - sh.offset;  // last query seeing a key
+        w.i1 = (reach < 0) ? -1 : min(w.i1, reach / C::BMQ);
+    }
+    w.nsteps_g = max(0, w.i1 - w.i0 + 1);
+    w.nsteps = w.nsteps_g * sh.group;
+    w.bhq_base = (w.bh_kv / sh.Hkv) * sh.Hq + (w.bh_kv % sh.Hkv) * sh.group;
+    return w;
+}
+
+// Walks a unit's steps query head by query head of the group, each over query blocks i0 .. i1
+// (no division per step).
+struct StepCursor {
+    int bhq, qi;
+    __device__ __forceinline__ StepCursor(const BwdUnit& w) : bhq(w.bhq_base), qi(w.i0) {}
+    __device__ __forceinline__ void next(const BwdUnit& w) {
+        if (++qi > w.i1) {
+            qi = w.i0;
+            ++bhq;
+        }
+    }
+};
+
 // WINDOW (causal only): queries more than `window` positions past a key do not see it.
+// Persistent: one CTA per SM walks units taken from a launch-wide counter; every step barrier
+// counts steps over all of the CTA's units, so one unit's tail (last dQ drain, dV/dK epilogue)
+// overlaps the next unit's first steps.
 template <int D, bool CAUSAL, bool WINDOW>
 __global__ void __launch_bounds__(512, 1)
 fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
               const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
               const __grid_constant__ CUtensorMap tm_dqacc, const uint8_t* __restrict__ folds,
-              const BwdShape sh, const float c, const float scale, int* err) {
+              const BwdShape sh, const int num_units, unsigned* __restrict__ sched,
+              const float c, const float scale, int* err) {
     using C = BwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
@@ -226,41 +292,12 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const int warp = tid >> 5;
     const int lane = tid & 31;
 
-    // This CTA: KV head bh_kv, keys [key0, key0 + 128). It visits every query head of the
-    // group and, for each, the query steps whose rows can see some key of the tile: from the
-    // causal diagonal (query position offset + q >= key) to the window's reach (position -
-    // window <= key). A tile no query sees has no steps and stores zero gradients.
-    // CTA order: head by head (neighbouring CTAs share their query heads' Q/dO in L2), or, for
-    // short causal launches, key tile by key tile (the costliest tiles, whose queries reach
-    // back to the diagonal, start first instead of a head's heavy tiles being left for last).
-    const int bh_kv = sh.kb_major ? (int)(blockIdx.x % (uint32_t)sh.BHkv) : (int)(blockIdx.x / (uint32_t)sh.nkb);
-    const int kb = sh.kb_major ? (int)(blockIdx.x / (uint32_t)sh.BHkv) : (int)(blockIdx.x % (uint32_t)sh.nkb);
-    const int key0 = kb * C::KT;
-    const int nq_total = (sh.Tq + C::BMQ - 1) / C::BMQ;
-    const int i0 = CAUSAL ? max(0, key0 - sh.offset) / C::BMQ : 0;
-    int i1 = nq_total - 1;
-    if (WINDOW) {
-        const int reach = key0 + C::KT - 1 + sh.window - sh.offset;  // last query that sees a key
-        i1 = (reach < 0) ? -1 : min(i1, reach / C::BMQ);
-    }
-    const int nsteps_g = max(0, i1 - i0 + 1);
-    const int nsteps = nsteps_g * sh.group;
-    const int bhq_base = (bh_kv / sh.Hkv) * sh.Hq + (bh_kv % sh.Hkv) * sh.group;
-    // Steps run query head by query head of the group, each over query blocks i0 .. i1; a
-    // role walks them with a StepCursor (no division per step).
-    struct StepCursor {
-        int bhq, qi;
-    };
-    auto first_step = [&]() { return StepCursor{bhq_base, i0}; };
-    auto next_step = [&](StepCursor& cur) {
-        if (++cur.qi > i1) {
-            cur.qi = i0;
-            ++cur.bhq;
-        }
-    };
-
+    constexpr int kUidReaders = 14;  // warps 1, 3, 4-11, 12-15 (one arrival per warp)
     if (tid == 0) {
         ptx::mbar_init(ptx::smem_addr(&bars->kv_full), 1);
+        ptx::mbar_init(ptx::smem_addr(&bars->kv_empty), 2);   // both MMA-issuing warps
+        ptx::mbar_init(ptx::smem_addr(&bars->dkv_full), 1);
+        ptx::mbar_init(ptx::smem_addr(&bars->dkv_free), 128); // the epilogue warps' threads
         for (int s = 0; s < C::NQS; ++s) {
             ptx::mbar_init(ptx::smem_addr(&bars->q_full[s]), 1);
             ptx::mbar_init(ptx::smem_addr(&bars->q_empty[s]), 1);
@@ -273,6 +310,10 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         ptx::mbar_init(ptx::smem_addr(&bars->dq_full), 1);
         ptx::mbar_init(ptx::smem_addr(&bars->dq_free), 128);
         ptx::mbar_init(ptx::smem_addr(&bars->final_bar), 2);
+        for (int i = 0; i < 4; ++i) {
+            ptx::mbar_init(ptx::smem_addr(&bars->uid_full[i]), 1);
+            ptx::mbar_init(ptx::smem_addr(&bars->uid_empty[i]), kUidReaders);
+        }
         bars->abort_flag = 0;
         ptx::fence_barrier_init();
         ptx::tma_prefetch_desc(&tm_q);
@@ -302,6 +343,23 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     ptx::tc_fence_after();
     const uint32_t tbase = __shfl_sync(0xffffffffu, bars->tmem_base, 0);
     volatile int* abort_flag = &bars->abort_flag;
+    // Units are handed out dynamically: a CTA's first unit is its block index, each later one
+    // the next from a launch-wide counter (taken by the producer when it starts the unit), so
+    // CTAs that drew cheap units (causal tiles far from the diagonal) simply take more. The
+    // producer publishes each unit id in a four-slot ring; every other role reads it.
+    volatile int* uid_ring = bars->uid;
+    // (warp-wide) the unit id of this CTA's ul-th unit, -1 past the end; ok = false on abort
+    auto fetch_unit = [&](int ul, bool& ok) -> int {
+        const int slot = ul & 3;
+        ok = warp_wait(ptx::smem_addr(&bars->uid_full[slot]), (uint32_t)(ul >> 2) & 1u, abort_flag,
+                       err, kDevTimeoutLoad);
+        if (!ok) return -1;
+        const int u = uid_ring[slot];
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&bars->uid_empty[slot]));
+        return u;
+    };
+
     const uint32_t s_k = ptx::smem_addr(smem + C::OFF_K);
     const uint32_t s_v = ptx::smem_addr(smem + C::OFF_V);
     const uint32_t s_st = ptx::smem_addr(smem + C::OFF_ST);
@@ -312,38 +370,68 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         if (lane == 0) {
             const uint64_t pol_keep = ptx::l2_policy_evict_last();
             const uint32_t b_kv = ptx::smem_addr(&bars->kv_full);
-            ptx::mbar_arrive_expect_tx(b_kv, 2 * C::KTILE);
-            for (int ch = 0; ch < D / 64; ++ch) {
-                ptx::tma_load_3d(s_k + ch * C::KCHUNK, &tm_k, b_kv, ch * 64, key0, bh_kv);
-                ptx::tma_load_3d(s_v + ch * C::KCHUNK, &tm_v, b_kv, ch * 64, key0, bh_kv);
-            }
-            int issued = 0;
-            StepCursor cur = first_step();
-            for (int si = 0; si < nsteps; ++si, next_step(cur)) {
-                const int st = si % C::NQS;
-                const uint32_t ph = (uint32_t)(si / C::NQS) & 1u;
-                if (!wait_phase(ptx::smem_addr(&bars->q_empty[st]), ph ^ 1u, abort_flag, err,
-                                kDevTimeoutConsumer))
+            int g = 0;   // steps issued over all units
+            int ul = 0;  // units started
+            bool ok = true;
+            for (;; ++ul) {
+                // take and publish this CTA's next unit
+                const int slot = ul & 3;
+                if (ul >= 4 && !wait_phase(ptx::smem_addr(&bars->uid_empty[slot]),
+                                           (uint32_t)((ul >> 2) - 1) & 1u, abort_flag, err,
+                                           kDevTimeoutConsumer))
                     break;
-                const int q0 = cur.qi * C::BMQ;
-                const int bhq = cur.bhq;
-                const uint32_t b_q = ptx::smem_addr(&bars->q_full[st]);
-                const uint32_t base = s_st + st * C::STAGE_BYTES;
-                ptx::mbar_arrive_expect_tx(b_q, 2 * C::QTILE + 2 * C::FOLD_BYTES);
-                for (int ch = 0; ch < D / 64; ++ch) {
-                    ptx::tma_load_3d_hint(base + ch * C::QCHUNK, &tm_q, b_q, ch * 64, q0, bhq, pol_keep);
-                    ptx::tma_load_3d_hint(base + C::QTILE + ch * C::QCHUNK, &tm_do, b_q, ch * 64, q0,
-                                          bhq, pol_keep);
+                int u = (int)blockIdx.x;
+                if (ul > 0) {
+                    const unsigned t = atomicAdd(sched, 1u) + (unsigned)gridDim.x;
+                    u = (t < (unsigned)num_units) ? (int)t : -1;
                 }
-                const uint8_t* lf = folds + ((size_t)bhq * (size_t)sh.Npad + (size_t)q0) * 16u;
-                const uint8_t* df = lf + (size_t)sh.BHq * sh.Npad * 16u;
-                ptx::bulk_load(base + 2 * C::QTILE, lf, C::FOLD_BYTES, b_q);
-                ptx::bulk_load(base + 2 * C::QTILE + C::FOLD_BYTES, df, C::FOLD_BYTES, b_q);
-                ++issued;
+                uid_ring[slot] = u;
+                ptx::mbar_arrive(ptx::smem_addr(&bars->uid_full[slot]));
+                if (u < 0) break;
+                const BwdUnit w = bwd_unit<D, CAUSAL, WINDOW>(u, sh);
+                // K/V of the previous unit stay until every MMA reading them has completed.
+                if (ul > 0 && !wait_phase(ptx::smem_addr(&bars->kv_empty), (uint32_t)(ul - 1) & 1u,
+                                          abort_flag, err, kDevTimeoutMma))
+                    break;
+                ptx::mbar_arrive_expect_tx(b_kv, 2 * C::KTILE);
+                for (int ch = 0; ch < D / 64; ++ch) {
+                    ptx::tma_load_3d(s_k + ch * C::KCHUNK, &tm_k, b_kv, ch * 64, w.key0, w.bh_kv);
+                    ptx::tma_load_3d(s_v + ch * C::KCHUNK, &tm_v, b_kv, ch * 64, w.key0, w.bh_kv);
+                }
+                StepCursor cur(w);
+                for (int si = 0; si < w.nsteps; ++si, ++g, cur.next(w)) {
+                    const int st = g % C::NQS;
+                    const uint32_t ph = (uint32_t)(g / C::NQS) & 1u;
+                    if (!wait_phase(ptx::smem_addr(&bars->q_empty[st]), ph ^ 1u, abort_flag, err,
+                                    kDevTimeoutConsumer)) {
+                        ok = false;
+                        break;
+                    }
+                    const int q0 = cur.qi * C::BMQ;
+                    const int bhq = cur.bhq;
+                    const uint32_t b_q = ptx::smem_addr(&bars->q_full[st]);
+                    const uint32_t base = s_st + st * C::STAGE_BYTES;
+                    ptx::mbar_arrive_expect_tx(b_q, 2 * C::QTILE + 2 * C::FOLD_BYTES);
+                    for (int ch = 0; ch < D / 64; ++ch) {
+                        ptx::tma_load_3d_hint(base + ch * C::QCHUNK, &tm_q, b_q, ch * 64, q0, bhq, pol_keep);
+                        ptx::tma_load_3d_hint(base + C::QTILE + ch * C::QCHUNK, &tm_do, b_q, ch * 64, q0,
+                                              bhq, pol_keep);
+                    }
+                    const uint8_t* lf = folds + ((size_t)bhq * (size_t)sh.Npad + (size_t)q0) * 16u;
+                    const uint8_t* df = lf + (size_t)sh.BHq * sh.Npad * 16u;
+                    ptx::bulk_load(base + 2 * C::QTILE, lf, C::FOLD_BYTES, b_q);
+                    ptx::bulk_load(base + 2 * C::QTILE + C::FOLD_BYTES, df, C::FOLD_BYTES, b_q);
+                }
+                if (!ok) {
+                    ++ul;  // this unit's K/V load was issued
+                    break;
+                }
             }
-            drain_wait(b_kv, 0);
-            for (int si = max(0, issued - C::NQS); si < issued; ++si)
-                drain_wait(ptx::smem_addr(&bars->q_full[si % C::NQS]), (uint32_t)(si / C::NQS) & 1u);
+            // Every copy issued must have landed before the CTA exits: the last K/V load and
+            // the last ring stages.
+            if (ul > 0) drain_wait(b_kv, (uint32_t)(ul - 1) & 1u);
+            for (int gi = max(0, g - C::NQS); gi < g; ++gi)
+                drain_wait(ptx::smem_addr(&bars->q_full[gi % C::NQS]), (uint32_t)(gi / C::NQS) & 1u);
         }
     } else if (warp == 1 || warp == 3) {
         // ================================ MMA issuers =================================
@@ -399,77 +487,100 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 __syncwarp();
             };
             // Two issuing warps (see the forward): warp 1 issues S^T/dP^T, warp 3 issues
-            // dV/dK/dQ, so one warp's MMAs run while the other waits for operands.
-            bool ok = warp_wait(ptx::smem_addr(&bars->kv_full), 0, abort_flag, err, kDevTimeoutLoad);
-            if (warp == 1 && nsteps > 0) {
-                if (ok) ok = warp_wait(ptx::smem_addr(&bars->q_full[0]), 0, abort_flag, err, kDevTimeoutLoad);
-                if (ok) {
-                    ptx::tc_fence_after();
-                    issue_s_dp(0);
-                }
-                for (int si = 0; ok && si + 1 < nsteps; ++si) {
-                    // Next S^T/dP^T as soon as the compute warps have read this step's.
-                    const int st1 = (si + 1) % C::NQS;
-                    ok = warp_wait(ptx::smem_addr(&bars->q_full[st1]), (uint32_t)((si + 1) / C::NQS) & 1u,
-                                    abort_flag, err, kDevTimeoutLoad);
-                    if (ok) ok = warp_wait(ptx::smem_addr(&bars->s_free), (uint32_t)si & 1u, abort_flag,
-                                            err, kDevTimeoutSoftmax);
-                    if (!ok) break;
-                    ptx::tc_fence_after();
-                    issue_s_dp(si + 1);
-                }
-            }
-            for (int si = 0; warp == 3 && ok && si < nsteps; ++si) {
-                const int st = si % C::NQS;
-                ok = warp_wait(ptx::smem_addr(&bars->p_ready), (uint32_t)si & 1u, abort_flag, err,
-                                kDevTimeoutSoftmax);
+            // dV/dK/dQ, so one warp's MMAs run while the other waits for operands. Both count
+            // steps (g) and units (ul) over the CTA's whole walk.
+            bool ok = true;
+            int g = 0;
+            int ul = 0;
+            for (;; ++ul) {
+                const int u = fetch_unit(ul, ok);
+                if (!ok || u < 0) break;
+                const BwdUnit w = bwd_unit<D, CAUSAL, WINDOW>(u, sh);
+                ok = warp_wait(ptx::smem_addr(&bars->kv_full), (uint32_t)ul & 1u, abort_flag, err,
+                               kDevTimeoutLoad);
                 if (!ok) break;
-                ptx::tc_fence_after();
-                // dV += P^T dO (A = P^T in TMEM) and dK += dS^T Q (A = dS^T, K-major in smem).
-                const uint32_t st_off = (uint32_t)st * C::STAGE_BYTES;
-                const uint32_t ds_off = (uint32_t)(si % C::NDS) * C::DS_BYTES;
-                const uint64_t do_mn = ptx::sdesc_add(st_mn, st_off + C::QTILE);
-                const uint64_t q_mn = ptx::sdesc_add(st_mn, st_off);
-                const uint64_t dsk = ptx::sdesc_add(ds_kmaj, ds_off);
-                if (ptx::elect_one()) {
-#pragma unroll
-                for (int kk = 0; kk < C::BMQ / 16; ++kk) {
-                    ptx::mma_ts(tbase + C::DV_COL, tbase + C::PT_COL + kk * 8,
-                                ptx::sdesc_add(do_mn, kk * 2048), idesc_kv, (si > 0 || kk > 0) ? 1u : 0u);
-                }
-#pragma unroll
-                for (int kk = 0; kk < C::BMQ / 16; ++kk) {
-                    ptx::mma_ss(tbase + C::DK_COL, ptx::sdesc_add(dsk, (kk >> 2) * C::DSREG + (kk & 3) * 32),
-                                ptx::sdesc_add(q_mn, kk * 2048), idesc_kv, (si > 0 || kk > 0) ? 1u : 0u);
-                }
-                ptx::mma_commit(ptx::smem_addr(&bars->mma_done));
-                ptx::mma_commit(ptx::smem_addr(&bars->q_empty[st]));
-                }
-                __syncwarp();
-                if (si > 0) {
-                    ok = warp_wait(ptx::smem_addr(&bars->dq_free), (uint32_t)(si - 1) & 1u,
-                                    abort_flag, err, kDevTimeoutSoftmax);
-                    if (!ok) break;
-                    ptx::tc_fence_after();
-                }
-                const uint64_t dsm = ptx::sdesc_add(ds_mn, ds_off);
-                if (ptx::elect_one()) {
-#pragma unroll
-                for (int kk = 0; kk < C::KT / 16; ++kk) {
-                    if (D == 128) {
-                        // dQ^T = K^T dS^T: A = K as MN-major [d x keys], B = dS as MN-major [q x keys]
-                        ptx::mma_ss(tbase + C::DQ_COL, ptx::sdesc_add(k_mn, kk * 2048),
-                                    ptx::sdesc_add(dsm, kk * 2048), idesc_q, kk > 0);
-                    } else {
-                        // dQ = dS K: A = dS as MN-major [q x keys], B = K as MN-major [d x keys]
-                        ptx::mma_ss(tbase + C::DQ_COL, ptx::sdesc_add(dsm, kk * 2048),
-                                    ptx::sdesc_add(k_mn, kk * 2048), idesc_q, kk > 0);
+                if (warp == 1) {
+                    for (int si = 0; si < w.nsteps; ++si, ++g) {
+                        // S'^T/dP'^T of step g once its Q/dO stage has landed and the compute warps
+                        // have read step g - 1's.
+                        const int st = g % C::NQS;
+                        ok = warp_wait(ptx::smem_addr(&bars->q_full[st]), (uint32_t)(g / C::NQS) & 1u,
+                                       abort_flag, err, kDevTimeoutLoad);
+                        if (ok && g > 0)
+                            ok = warp_wait(ptx::smem_addr(&bars->s_free), (uint32_t)(g - 1) & 1u,
+                                           abort_flag, err, kDevTimeoutSoftmax);
+                        if (!ok) break;
+                        ptx::tc_fence_after();
+                        issue_s_dp(g);
                     }
+                } else {
+                    // This unit's first dV/dK overwrite TMEM the previous unit's epilogue must
+                    // have read. Waited for every unit, with or without steps, so dkv_full and
+                    // dkv_free strictly alternate.
+                    if (ul > 0)
+                        ok = warp_wait(ptx::smem_addr(&bars->dkv_free), (uint32_t)(ul - 1) & 1u,
+                                       abort_flag, err, kDevTimeoutSoftmax);
+                    for (int si = 0; ok && si < w.nsteps; ++si, ++g) {
+                        const int st = g % C::NQS;
+                        ok = warp_wait(ptx::smem_addr(&bars->p_ready), (uint32_t)g & 1u, abort_flag, err,
+                                       kDevTimeoutSoftmax);
+                        if (!ok) break;
+                        ptx::tc_fence_after();
+                        // dV += P^T dO (A = P^T in TMEM) and dK += dS^T Q (A = dS^T, K-major in smem).
+                        const uint32_t st_off = (uint32_t)st * C::STAGE_BYTES;
+                        const uint32_t ds_off = (uint32_t)(g % C::NDS) * C::DS_BYTES;
+                        const uint64_t do_mn = ptx::sdesc_add(st_mn, st_off + C::QTILE);
+                        const uint64_t q_mn = ptx::sdesc_add(st_mn, st_off);
+                        const uint64_t dsk = ptx::sdesc_add(ds_kmaj, ds_off);
+                        if (ptx::elect_one()) {
+#pragma unroll
+                            for (int kk = 0; kk < C::BMQ / 16; ++kk)
+                                ptx::mma_ts(tbase + C::DV_COL, tbase + C::PT_COL + kk * 8,
+                                            ptx::sdesc_add(do_mn, kk * 2048), idesc_kv,
+                                            (si > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                            for (int kk = 0; kk < C::BMQ / 16; ++kk)
+                                ptx::mma_ss(tbase + C::DK_COL,
+                                            ptx::sdesc_add(dsk, (kk >> 2) * C::DSREG + (kk & 3) * 32),
+                                            ptx::sdesc_add(q_mn, kk * 2048), idesc_kv,
+                                            (si > 0 || kk > 0) ? 1u : 0u);
+                            ptx::mma_commit(ptx::smem_addr(&bars->mma_done));
+                            ptx::mma_commit(ptx::smem_addr(&bars->q_empty[st]));
+                            if (si + 1 == w.nsteps) ptx::mma_commit(ptx::smem_addr(&bars->dkv_full));
+                        }
+                        __syncwarp();
+                        if (g > 0) {
+                            ok = warp_wait(ptx::smem_addr(&bars->dq_free), (uint32_t)(g - 1) & 1u,
+                                           abort_flag, err, kDevTimeoutSoftmax);
+                            if (!ok) break;
+                            ptx::tc_fence_after();
+                        }
+                        const uint64_t dsm = ptx::sdesc_add(ds_mn, ds_off);
+                        if (ptx::elect_one()) {
+#pragma unroll
+                            for (int kk = 0; kk < C::KT / 16; ++kk) {
+                                if (D == 128) {
+                                    // dQ^T = K^T dS^T: A = K MN-major [d x keys], B = dS MN-major [q x keys]
+                                    ptx::mma_ss(tbase + C::DQ_COL, ptx::sdesc_add(k_mn, kk * 2048),
+                                                ptx::sdesc_add(dsm, kk * 2048), idesc_q, kk > 0);
+                                } else {
+                                    // dQ = dS K: A = dS MN-major [q x keys], B = K MN-major [d x keys]
+                                    ptx::mma_ss(tbase + C::DQ_COL, ptx::sdesc_add(dsm, kk * 2048),
+                                                ptx::sdesc_add(k_mn, kk * 2048), idesc_q, kk > 0);
+                                }
+                            }
+                            ptx::mma_commit(ptx::smem_addr(&bars->dq_full));
+                            ptx::mma_commit(ptx::smem_addr(&bars->ds_free[g % C::NDS]));
+                        }
+                        __syncwarp();
+                    }
+                    // a unit without steps still completes its dV/dK phase (zeros are stored)
+                    if (ok && w.nsteps == 0) commit(&bars->dkv_full);
                 }
-                ptx::mma_commit(ptx::smem_addr(&bars->dq_full));
-                ptx::mma_commit(ptx::smem_addr(&bars->ds_free[si % C::NDS]));
-                }
-                __syncwarp();
+                if (!ok) break;
+                // this warp's MMAs reading K/V of the unit are issued: the producer may reload
+                // them once they complete
+                commit(&bars->kv_empty);
             }
             commit(&bars->final_bar);
             drain_wait(ptx::smem_addr(&bars->final_bar), 0);
@@ -481,7 +592,6 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const int h = (warp - 4) >> 2;
         const int wq = warp & 3;
         const int k = wq * 32 + lane;  // key row within the tile
-        const int key = key0 + k;
         // (causal) queries at positions key .. key + window see this key; no window: all after it
         const uint32_t vspan = WINDOW ? (uint32_t)sh.window : 0x7fffffffu;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
@@ -491,244 +601,230 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         constexpr int NCH = C::BMQ / 32;
         constexpr int NCH_H = NCH / 2;
         bool ok = true;
-        StepCursor cur = first_step();
-        for (int si = 0; si < nsteps; ++si, next_step(cur)) {
-            const int q0 = cur.qi * C::BMQ;
-            // S'^T and dP'^T already carry the row statistics (fold MMAs): nothing else to read.
-            ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->s_full), (uint32_t)si & 1u,
-                                                    abort_flag, err, kDevTimeoutMma));
-            if (!ok) break;
-            ptx::tc_fence_after();
-            uint8_t* dsbuf = smem + C::OFF_DS + (si % C::NDS) * C::DS_BYTES;
-            // key visible to query q iff (!causal || key <= p) && (no window || key >= p - window),
-            // p = offset + q; elementwise masking only where the step crosses either edge.
-            const int p0 = sh.offset + q0;
-            const bool need_mask = CAUSAL && ((p0 < key0 + C::KT - 1) ||
-                                              (WINDOW && p0 + C::BMQ - 1 - sh.window > key0));
+        int g = 0;
+        for (int ul = 0;; ++ul) {
+            const int u = fetch_unit(ul, ok);
+            if (!ok || u < 0) break;
+            const BwdUnit w = bwd_unit<D, CAUSAL, WINDOW>(u, sh);
+            const int key0 = w.key0;
+            const int key = key0 + k;
+            StepCursor cur(w);
+            for (int si = 0; si < w.nsteps; ++si, ++g, cur.next(w)) {
+                const int q0 = cur.qi * C::BMQ;
+                // S'^T and dP'^T already carry the row statistics (fold MMAs): nothing else to read.
+                ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->s_full), (uint32_t)g & 1u,
+                                                        abort_flag, err, kDevTimeoutMma));
+                if (!ok) break;
+                ptx::tc_fence_after();
+                uint8_t* dsbuf = smem + C::OFF_DS + (g % C::NDS) * C::DS_BYTES;
+                // key visible to query q iff (!causal || key <= p) && (no window || key >= p - window),
+                // p = offset + q; elementwise masking only where the step crosses either edge.
+                const int p0 = sh.offset + q0;
+                const bool need_mask = CAUSAL && ((p0 < key0 + C::KT - 1) ||
+                                                  (WINDOW && p0 + C::BMQ - 1 - sh.window > key0));
 #pragma unroll
-            for (int ci = 0; ci < NCH_H; ++ci) {
-                const int cc = h * NCH_H + ci;
-                uint32_t sv[32], dpv[32];
-                ptx::tmem_ld32_nowait(t_s + 32 * cc, sv);
-                ptx::tmem_ld32_nowait(t_dp + 32 * cc, dpv);
-                ptx::tmem_wait_ld(sv);
-                ptx::tmem_wait_ld(dpv);
-                if (ci == NCH_H - 1) {
-                    // this half's S^T/dP^T columns are in registers: release them
-                    ptx::tc_fence_before();
-                    ptx::mbar_arrive(ptx::smem_addr(&bars->s_free));
-                }
-                uint32_t pk[16], dk[16];
-#pragma unroll
-                for (int j = 0; j < 32; j += 4) {
-                    const int qi = 32 * cc + j;
-                    // x = c * S' = c * S - LSE * log2(e)
-                    float x0, x1, x2, x3;
-                    ptx::fmul2(x0, x1, __uint_as_float(sv[j]), __uint_as_float(sv[j + 1]), c, c);
-                    ptx::fmul2(x2, x3, __uint_as_float(sv[j + 2]), __uint_as_float(sv[j + 3]), c, c);
-                    float pe0 = ptx::ex2_approx(x0), pe1 = ptx::ex2_approx(x1);
-                    float pe2 = ptx::ex2_approx(x2), pe3 = ptx::ex2_approx(x3);
-                    if (need_mask) {
-                        // visible iff key <= p <= key + window, i.e. p - key in [0, vspan]
-                        const uint32_t dp = (uint32_t)(p0 + qi - key);
-                        if (dp > vspan) pe0 = 0.f;
-                        if (dp + 1u > vspan) pe1 = 0.f;
-                        if (dp + 2u > vspan) pe2 = 0.f;
-                        if (dp + 3u > vspan) pe3 = 0.f;
+                for (int ci = 0; ci < NCH_H; ++ci) {
+                    const int cc = h * NCH_H + ci;
+                    uint32_t sv[32], dpv[32];
+                    ptx::tmem_ld32_nowait(t_s + 32 * cc, sv);
+                    ptx::tmem_ld32_nowait(t_dp + 32 * cc, dpv);
+                    ptx::tmem_wait_ld(sv);
+                    ptx::tmem_wait_ld(dpv);
+                    if (ci == NCH_H - 1) {
+                        // this half's S^T/dP^T columns are in registers: release them
+                        ptx::tc_fence_before();
+                        ptx::mbar_arrive(ptx::smem_addr(&bars->s_free));
                     }
-                    // dS = P (dP - D) = P dP'
-                    float d0, d1, d2, d3;
-                    ptx::fmul2(d0, d1, pe0, pe1, __uint_as_float(dpv[j]), __uint_as_float(dpv[j + 1]));
-                    ptx::fmul2(d2, d3, pe2, pe3, __uint_as_float(dpv[j + 2]), __uint_as_float(dpv[j + 3]));
-                    pk[j / 2] = ptx::pack_bf16x2(pe0, pe1);
-                    pk[j / 2 + 1] = ptx::pack_bf16x2(pe2, pe3);
-                    dk[j / 2] = ptx::pack_bf16x2(d0, d1);
-                    dk[j / 2 + 1] = ptx::pack_bf16x2(d2, d3);
-                }
-                if (ci == 0) {
-                    if (si > 0) {
-                        // dV(si-1) must have read P^T before it is overwritten.
-                        ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->mma_done),
-                                                                (uint32_t)(si - 1) & 1u, abort_flag,
-                                                                err, kDevTimeoutMma));
-                        if (!ok) break;
+                    uint32_t pk[16], dk[16];
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) {
+                        const int qi = 32 * cc + j;
+                        // x = c * S' = c * S - LSE * log2(e)
+                        float x0, x1, x2, x3;
+                        ptx::fmul2(x0, x1, __uint_as_float(sv[j]), __uint_as_float(sv[j + 1]), c, c);
+                        ptx::fmul2(x2, x3, __uint_as_float(sv[j + 2]), __uint_as_float(sv[j + 3]), c, c);
+                        float pe0 = ptx::ex2_approx(x0), pe1 = ptx::ex2_approx(x1);
+                        float pe2 = ptx::ex2_approx(x2), pe3 = ptx::ex2_approx(x3);
+                        if (need_mask) {
+                            // visible iff key <= p <= key + window, i.e. p - key in [0, vspan]
+                            const uint32_t dp = (uint32_t)(p0 + qi - key);
+                            if (dp > vspan) pe0 = 0.f;
+                            if (dp + 1u > vspan) pe1 = 0.f;
+                            if (dp + 2u > vspan) pe2 = 0.f;
+                            if (dp + 3u > vspan) pe3 = 0.f;
+                        }
+                        // dS = P (dP - D) = P dP'
+                        float d0, d1, d2, d3;
+                        ptx::fmul2(d0, d1, pe0, pe1, __uint_as_float(dpv[j]), __uint_as_float(dpv[j + 1]));
+                        ptx::fmul2(d2, d3, pe2, pe3, __uint_as_float(dpv[j + 2]), __uint_as_float(dpv[j + 3]));
+                        pk[j / 2] = ptx::pack_bf16x2(pe0, pe1);
+                        pk[j / 2 + 1] = ptx::pack_bf16x2(pe2, pe3);
+                        dk[j / 2] = ptx::pack_bf16x2(d0, d1);
+                        dk[j / 2 + 1] = ptx::pack_bf16x2(d2, d3);
                     }
-                    if (si >= C::NDS) {
-                        // dK and dQ of step si - NDS must have read this dS buffer.
-                        ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->ds_free[si % C::NDS]),
-                                                                (uint32_t)(si / C::NDS - 1) & 1u,
-                                                                abort_flag, err, kDevTimeoutMma));
-                        if (!ok) break;
+                    if (ci == 0) {
+                        if (g > 0) {
+                            // dV of step g - 1 must have read P^T before it is overwritten.
+                            ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->mma_done),
+                                                                    (uint32_t)(g - 1) & 1u, abort_flag,
+                                                                    err, kDevTimeoutMma));
+                            if (!ok) break;
+                        }
+                        if (g >= C::NDS) {
+                            // dK and dQ of step g - NDS must have read this dS buffer.
+                            ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->ds_free[g % C::NDS]),
+                                                                    (uint32_t)(g / C::NDS - 1) & 1u,
+                                                                    abort_flag, err, kDevTimeoutMma));
+                            if (!ok) break;
+                        }
+                        ptx::tc_fence_after();
                     }
-                    ptx::tc_fence_after();
-                }
-                ptx::tmem_st16(t_pt + 16 * cc, pk);
-                // dS row k (queries contiguous) into the 128B-swizzled dS tile.
-                uint8_t* region = dsbuf + (cc >> 1) * C::DSREG;
+                    ptx::tmem_st16(t_pt + 16 * cc, pk);
+                    // dS row k (queries contiguous) into the 128B-swizzled dS tile.
+                    uint8_t* region = dsbuf + (cc >> 1) * C::DSREG;
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    uint4 w = make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
-                    *reinterpret_cast<uint4*>(region + sw128_offset((uint32_t)k, (uint32_t)((cc & 1) * 4 + u))) = w;
+                    for (int u = 0; u < 4; ++u) {
+                        const uint4 wv = make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
+                        *reinterpret_cast<uint4*>(region + sw128_offset((uint32_t)k, (uint32_t)((cc & 1) * 4 + u))) = wv;
+                    }
                 }
-            }
-            if (!ok) break;
-            ptx::tmem_wait_st();
-            ptx::fence_proxy_async_smem();
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(ptx::smem_addr(&bars->p_ready));
-        }
-        // ---- epilogue (first compute warpgroup): dV -> bf16 -> smem (stage 0 area) -> TMA store ----
-        if (ok && h == 0 && nsteps > 0)
-            ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->mma_done),
-                                                    (uint32_t)(nsteps - 1) & 1u, abort_flag, err,
-                                                    kDevTimeoutMma));
-        if (ok && h == 0) {
-            ptx::tc_fence_after();
-            uint8_t* stage = smem + C::OFF_ST;
-#pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
-                uint32_t v[32];
-                if (nsteps > 0) {
-                    ptx::tmem_ld32(tbase + lane_off + C::DV_COL + 32 * cc, v);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = 0u;  // no query sees these keys
-                }
-                uint8_t* chunk = stage + (cc >> 1) * C::KCHUNK;
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    uint4 w;
-                    w.x = ptx::pack_bf16x2(__uint_as_float(v[8 * u + 0]), __uint_as_float(v[8 * u + 1]));
-                    w.y = ptx::pack_bf16x2(__uint_as_float(v[8 * u + 2]), __uint_as_float(v[8 * u + 3]));
-                    w.z = ptx::pack_bf16x2(__uint_as_float(v[8 * u + 4]), __uint_as_float(v[8 * u + 5]));
-                    w.w = ptx::pack_bf16x2(__uint_as_float(v[8 * u + 6]), __uint_as_float(v[8 * u + 7]));
-                    *reinterpret_cast<uint4*>(chunk + sw128_offset((uint32_t)k, (uint32_t)((cc & 1) * 4 + u))) = w;
-                }
-            }
-            ptx::fence_proxy_async_smem();
-            ptx::named_bar_sync(1, 128);
-            if (k == 0) {
-                for (int ch = 0; ch < D / 64; ++ch)
-                    ptx::tma_store_3d(&tm_dv, ptx::smem_addr(stage + ch * C::KCHUNK), ch * 64, key0, bh_kv);
-                ptx::bulk_commit();
-                ptx::bulk_wait_read_all();
+                if (!ok) break;
+                ptx::tmem_wait_st();
+                ptx::fence_proxy_async_smem();
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(ptx::smem_addr(&bars->p_ready));
             }
         }
     } else if (warp >= 12) {
-        // ============== dQ drain warpgroup, then the dK epilogue ==============
+        // ======== dQ drain warpgroup, and each unit's dV / dK epilogue ========
         const int wq = warp & 3;
-        const int r = wq * 32 + lane;  // TMEM lane: d index (d=128) or query row (d=64)
+        const int r = wq * 32 + lane;  // TMEM lane: d index (d=128 dQ) or query / key row
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         uint8_t* dqs = smem + C::OFF_DQS;
         bool ok = true;
-        StepCursor cur = first_step();
-        for (int si = 0; si < nsteps; ++si, next_step(cur)) {
-            const int q0 = cur.qi * C::BMQ;
-            const int bhq = cur.bhq;
-            ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->dq_full), (uint32_t)si & 1u,
+        bool staged = false;  // a bulk copy issued from the staging tile may still be reading it
+        auto staging_free = [&]() {
+            if (staged) {
+                if (r == 0) ptx::bulk_wait_read_all();
+                ptx::named_bar_sync(2, 128);
+            }
+            staged = true;
+        };
+        int g = 0;
+        for (int ul = 0;; ++ul) {
+            const int u = fetch_unit(ul, ok);
+            if (!ok || u < 0) break;
+            const BwdUnit w = bwd_unit<D, CAUSAL, WINDOW>(u, sh);
+            StepCursor cur(w);
+            for (int si = 0; si < w.nsteps; ++si, ++g, cur.next(w)) {
+                const int q0 = cur.qi * C::BMQ;
+                const int bhq = cur.bhq;
+                ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->dq_full), (uint32_t)g & 1u,
+                                                        abort_flag, err, kDevTimeoutMma));
+                if (!ok) break;
+                ptx::tc_fence_after();
+                uint32_t a[32], b[32];
+                ptx::tmem_ld32_nowait(tbase + lane_off + C::DQ_COL, a);
+                ptx::tmem_ld32_nowait(tbase + lane_off + C::DQ_COL + 32, b);
+                ptx::tmem_wait_ld(a);
+                ptx::tmem_wait_ld(b);
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(ptx::smem_addr(&bars->dq_free));
+                staging_free();
+                if (D == 128) {
+                    // lane r = head-dim column e; a/b hold query rows 0-31 / 32-63.
+                    // fp32 box (e / 32): [BMQ rows x 128 B], element e at byte 4 (e % 32).
+                    uint8_t* box = dqs + (r >> 5) * C::DQBOX;
+                    const uint32_t uu = (uint32_t)((r & 31) >> 2);
+                    const uint32_t wb = (uint32_t)(r & 3) * 4u;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        *reinterpret_cast<uint32_t*>(box + sw128_offset((uint32_t)j, uu) + wb) = a[j];
+                        *reinterpret_cast<uint32_t*>(box + sw128_offset((uint32_t)(32 + j), uu) + wb) = b[j];
+                    }
+                    ptx::fence_proxy_async_smem();
+                    ptx::named_bar_sync(2, 128);
+                    if (r == 0) {
+                        for (int bx = 0; bx < D / 32; ++bx)
+                            ptx::tma_reduce_add_3d(&tm_dqacc, ptx::smem_addr(dqs + bx * C::DQBOX), bx * 32,
+                                                   q0, bhq);
+                        ptx::bulk_commit();
+                    }
+                } else {
+                    // lane r = query row; a/b hold head-dim columns 0-31 / 32-63, one fp32 box
+                    // each, staged one after the other through the single box of staging.
+#pragma unroll
+                    for (int uu = 0; uu < 8; ++uu)
+                        *reinterpret_cast<uint4*>(dqs + sw128_offset((uint32_t)r, (uint32_t)uu)) =
+                            make_uint4(a[4 * uu], a[4 * uu + 1], a[4 * uu + 2], a[4 * uu + 3]);
+                    ptx::fence_proxy_async_smem();
+                    ptx::named_bar_sync(2, 128);
+                    if (r == 0) {
+                        ptx::tma_reduce_add_3d(&tm_dqacc, ptx::smem_addr(dqs), 0, q0, bhq);
+                        ptx::bulk_commit();
+                    }
+                    staging_free();
+#pragma unroll
+                    for (int uu = 0; uu < 8; ++uu)
+                        *reinterpret_cast<uint4*>(dqs + sw128_offset((uint32_t)r, (uint32_t)uu)) =
+                            make_uint4(b[4 * uu], b[4 * uu + 1], b[4 * uu + 2], b[4 * uu + 3]);
+                    ptx::fence_proxy_async_smem();
+                    ptx::named_bar_sync(2, 128);
+                    if (r == 0) {
+                        ptx::tma_reduce_add_3d(&tm_dqacc, ptx::smem_addr(dqs), 32, q0, bhq);
+                        ptx::bulk_commit();
+                    }
+                }
+            }
+            if (!ok) break;
+            // ---- epilogue of the unit: dV, then dK * scale -> bf16 -> staging -> TMA store ----
+            // (runs while the next unit's first steps proceed; its first dV/dK MMA waits for
+            // dkv_free)
+            ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->dkv_full), (uint32_t)ul & 1u,
                                                     abort_flag, err, kDevTimeoutMma));
             if (!ok) break;
             ptx::tc_fence_after();
-            uint32_t a[32], b[32];
-            ptx::tmem_ld32_nowait(tbase + lane_off + C::DQ_COL, a);
-            ptx::tmem_ld32_nowait(tbase + lane_off + C::DQ_COL + 32, b);
-            ptx::tmem_wait_ld(a);
-            ptx::tmem_wait_ld(b);
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(ptx::smem_addr(&bars->dq_free));
-            if (D == 128) {
-                // The previous step's reduce must have finished reading the staging tile.
-                if (si > 0) {
-                    if (r == 0) ptx::bulk_wait_read_all();
-                    ptx::named_bar_sync(2, 128);
-                }
-                // lane r = head-dim column e; a/b hold query rows 0-31 / 32-63.
-                // fp32 box (e / 32): [BMQ rows x 128 B], element e at byte 4 (e % 32).
-                uint8_t* box = dqs + (r >> 5) * C::DQBOX;
-                const uint32_t u = (uint32_t)((r & 31) >> 2);
-                const uint32_t wb = (uint32_t)(r & 3) * 4u;
+#pragma unroll 1
+            for (int pass = 0; pass < 2; ++pass) {
+                const uint32_t col = pass ? C::DK_COL : C::DV_COL;
+                const float mul = pass ? scale : 1.f;
+                staging_free();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    *reinterpret_cast<uint32_t*>(box + sw128_offset((uint32_t)j, u) + wb) = a[j];
-                    *reinterpret_cast<uint32_t*>(box + sw128_offset((uint32_t)(32 + j), u) + wb) = b[j];
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t v[32];
+                    if (w.nsteps > 0) {
+                        ptx::tmem_ld32(tbase + lane_off + col + 32 * cc, v);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = 0u;  // no query sees these keys
+                    }
+                    uint8_t* chunk = dqs + (cc >> 1) * C::KCHUNK;
+#pragma unroll
+                    for (int uu = 0; uu < 4; ++uu) {
+                        uint4 wv;
+                        wv.x = ptx::pack_bf16x2(__uint_as_float(v[8 * uu + 0]) * mul, __uint_as_float(v[8 * uu + 1]) * mul);
+                        wv.y = ptx::pack_bf16x2(__uint_as_float(v[8 * uu + 2]) * mul, __uint_as_float(v[8 * uu + 3]) * mul);
+                        wv.z = ptx::pack_bf16x2(__uint_as_float(v[8 * uu + 4]) * mul, __uint_as_float(v[8 * uu + 5]) * mul);
+                        wv.w = ptx::pack_bf16x2(__uint_as_float(v[8 * uu + 6]) * mul, __uint_as_float(v[8 * uu + 7]) * mul);
+                        *reinterpret_cast<uint4*>(chunk + sw128_offset((uint32_t)r, (uint32_t)((cc & 1) * 4 + uu))) = wv;
+                    }
+                }
+                if (pass == 1) {
+                    // dV and dK are in registers / staging: the next unit may overwrite TMEM
+                    ptx::tc_fence_before();
+                    ptx::mbar_arrive(ptx::smem_addr(&bars->dkv_free));
                 }
                 ptx::fence_proxy_async_smem();
                 ptx::named_bar_sync(2, 128);
                 if (r == 0) {
-                    for (int bx = 0; bx < D / 32; ++bx)
-                        ptx::tma_reduce_add_3d(&tm_dqacc, ptx::smem_addr(dqs + bx * C::DQBOX), bx * 32,
-                                               q0, bhq);
-                    ptx::bulk_commit();
-                }
-            } else {
-                // lane r = query row; a/b hold head-dim columns 0-31 / 32-63, one fp32 box each,
-                // staged one after the other through the single box of staging.
-                if (si > 0) {
-                    if (r == 0) ptx::bulk_wait_read_all();
-                    ptx::named_bar_sync(2, 128);
-                }
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    *reinterpret_cast<uint4*>(dqs + sw128_offset((uint32_t)r, (uint32_t)u)) =
-                        make_uint4(a[4 * u], a[4 * u + 1], a[4 * u + 2], a[4 * u + 3]);
-                ptx::fence_proxy_async_smem();
-                ptx::named_bar_sync(2, 128);
-                if (r == 0) {
-                    ptx::tma_reduce_add_3d(&tm_dqacc, ptx::smem_addr(dqs), 0, q0, bhq);
-                    ptx::bulk_commit();
-                    ptx::bulk_wait_read_all();
-                }
-                ptx::named_bar_sync(2, 128);
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    *reinterpret_cast<uint4*>(dqs + sw128_offset((uint32_t)r, (uint32_t)u)) =
-                        make_uint4(b[4 * u], b[4 * u + 1], b[4 * u + 2], b[4 * u + 3]);
-                ptx::fence_proxy_async_smem();
-                ptx::named_bar_sync(2, 128);
-                if (r == 0) {
-                    ptx::tma_reduce_add_3d(&tm_dqacc, ptx::smem_addr(dqs), 32, q0, bhq);
+                    for (int ch = 0; ch < D / 64; ++ch)
+                        ptx::tma_store_3d(pass ? &tm_dk : &tm_dv, ptx::smem_addr(dqs + ch * C::KCHUNK),
+                                          ch * 64, w.key0, w.bh_kv);
                     ptx::bulk_commit();
                 }
             }
         }
         if (r == 0) ptx::bulk_wait_all();
-        // ---- epilogue: dK * scale -> bf16 -> smem (stage 1 area) -> TMA store ----
-        if (ok && nsteps > 0)
-            ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->mma_done),
-                                                    (uint32_t)(nsteps - 1) & 1u, abort_flag, err,
-                                                    kDevTimeoutMma));
-        if (ok) {
-            ptx::tc_fence_after();
-            uint8_t* stage = smem + C::OFF_ST + C::STAGE_BYTES;
-#pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
-                uint32_t v[32];
-                if (nsteps > 0) {
-                    ptx::tmem_ld32(tbase + lane_off + C::DK_COL + 32 * cc, v);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = 0u;  // no query sees these keys
-                }
-                uint8_t* chunk = stage + (cc >> 1) * C::KCHUNK;
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    uint4 w;
-                    w.x = ptx::pack_bf16x2(__uint_as_float(v[8 * u + 0]) * scale, __uint_as_float(v[8 * u + 1]) * scale);
-                    w.y = ptx::pack_bf16x2(__uint_as_float(v[8 * u + 2]) * scale, __uint_as_float(v[8 * u + 3]) * scale);
-                    w.z = ptx::pack_bf16x2(__uint_as_float(v[8 * u + 4]) * scale, __uint_as_float(v[8 * u + 5]) * scale);
-                    w.w = ptx::pack_bf16x2(__uint_as_float(v[8 * u + 6]) * scale, __uint_as_float(v[8 * u + 7]) * scale);
-                    *reinterpret_cast<uint4*>(chunk + sw128_offset((uint32_t)r, (uint32_t)((cc & 1) * 4 + u))) = w;
-                }
-            }
-            ptx::fence_proxy_async_smem();
-            ptx::named_bar_sync(2, 128);
-            if (r == 0) {
-                for (int ch = 0; ch < D / 64; ++ch)
-                    ptx::tma_store_3d(&tm_dk, ptx::smem_addr(stage + ch * C::KCHUNK), ch * 64, key0, bh_kv);
-                ptx::bulk_commit();
-                ptx::bulk_wait_read_all();
-            }
-        }
     }
 
     ptx::tc_fence_before();
@@ -738,6 +834,9 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         ptx::tmem_dealloc(tbase, 512);
     }
 }
+
+// L2 budget for one chunk of the causal unit order (about the size of the L2 cache).
+constexpr long long kChunkL2Bytes = 128LL << 20;
 
 template <int D, bool CAUSAL, bool WINDOW>
 cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t stream) {
@@ -751,11 +850,11 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t stream) {
         if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
         fa_bwd_pre_kernel<D><<<(unsigned)blocks, 256, 0, stream>>>(
             static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.lse,
-            static_cast<uint8_t*>(a.folds), a.dq_acc, a.Tq, a.Npad, a.BHq, 1.0f / a.scale);
+            static_cast<uint8_t*>(a.folds), a.dq_acc, a.sched, a.Tq, a.Npad, a.BHq, 1.0f / a.scale);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    // 2. main (one CTA per KV head and 128-key tile)
+    // 2. main (persistent; a work unit is one KV head and 128-key tile)
     {
         auto kern = fa_bwd_kernel<D, CAUSAL, WINDOW>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -773,15 +872,20 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t stream) {
         sh.BHq = a.BHq;
         sh.BHkv = a.BHkv;
         sh.nkb = (a.Tk + C::KT - 1) / C::KT;
-        const long long blocks = (long long)sh.nkb * a.BHkv;
-        if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-        // Key-tile-major order pays when the launch is a few waves of very unequal CTAs (causal)
-        // and costs L2 reuse when it is many waves; measured crossover between 7 and 13 waves.
-        sh.kb_major = (CAUSAL && blocks <= 8LL * a.num_sms) ? 1 : 0;
-        kern<<<(unsigned)blocks, C::THREADS, C::SMEM_BYTES, stream>>>(
+        const long long units = (long long)sh.nkb * a.BHkv;
+        if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+        // Causal: as many KV heads per chunk as keep the chunk's Q and dO (all query heads of
+        // each KV head) within kChunkL2Bytes of L2.
+        sh.kv_chunk = 1;
+        if (CAUSAL) {
+            const long long per_head = (long long)sh.group * a.Tq * D * 2 * (long long)sizeof(uint16_t);
+            sh.kv_chunk = (int)std::max(1LL, std::min<long long>(a.BHkv, kChunkL2Bytes / std::max(1LL, per_head)));
+        }
+        // Persistent grid: one CTA per SM walking units (the shared memory admits one CTA).
+        const int grid = (int)std::min<long long>(units, (long long)std::max(1, a.num_sms));
+        kern<<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, stream>>>(
             a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dk, a.tm_dv, a.tm_dqacc,
-            static_cast<const uint8_t*>(a.folds), sh, a.c,
-            a.scale, a.err);
+            static_cast<const uint8_t*>(a.folds), sh, (int)units, a.sched, a.c, a.scale, a.err);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

@@ -39,6 +39,7 @@ struct BwdLaunch {
     void* folds;                          // workspace: per query row, 32-byte records of
                                           // -LSE/scale then of -D ([B*Hq, Npad] each)
     float* dq_acc;                        // workspace: fp32 [B*Hq, Npad, d]
+    unsigned* sched;                      // workspace: the main kernel's unit counter
     int Tq, Tk, Npad, Hq, Hkv, BHq, BHkv, d, window;
     float scale;
     float c;                              // scale * log2(e)

@@ -86,9 +86,9 @@ def test_backward_empty_is_ok(lib):
 def test_workspace_bytes(lib):
     from exact_io_aware_fa_gb300 import api
     # two 16-byte fold records and d fp32 dQ partial sums per padded query row
-    assert api.backward_workspace_bytes(1, 1, 128, 64) == 128 * (32 + 4 * 64)
+    assert api.backward_workspace_bytes(1, 1, 128, 64) == 128 * (32 + 4 * 64) + 256
     # N is padded to a multiple of 128
-    assert api.backward_workspace_bytes(2, 3, 129, 128) == 6 * 256 * (32 + 4 * 128)
+    assert api.backward_workspace_bytes(2, 3, 129, 128) == 6 * 256 * (32 + 4 * 128) + 256
     assert api.backward_workspace_bytes(0, 1, 128, 64) == 0
     assert api.backward_workspace_bytes(1, 1, 128, 48) == 0
 

@@ -113,3 +113,15 @@ def test_config5_sampled(env):
     assert_close_grad(dv[:, :, rk], ref_v, "dV", "config 5")
     for g in (dq, dk, dv):
         assert np.all(np.isfinite(g))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_persistent_many_units_per_cta(env, d, causal):
+    """B*H*ceil(N/128) key tiles far above the SM count: every CTA of the persistent backward
+    walks several units, carrying its barrier phases, Q/dO ring and dV/dK epilogues across
+    them."""
+    from exact_io_aware_fa_gb300 import synthetic
+    api, orc = env
+    bits = synthetic.attention_inputs(2, 200, 300, d, seed=310 + d, with_dout=True)
+    check_full(api, orc, bits, causal, default_scale(d), f"many units d={d} causal={causal}")

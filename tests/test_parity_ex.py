@@ -203,3 +203,23 @@ def test_calls_from_a_new_host_thread(env):
     assert torch.equal(out["o"], ref_o)
     for a, b in zip(out["g"], ref_g):
         assert torch.equal(a, b)
+
+
+def test_backward_many_units_with_empty_tiles(env):
+    """Persistent backward over more units than SMs where most key tiles see no query (window
+    far behind a short query block): zero-step units interleave with working ones in every
+    CTA's walk."""
+    import torch
+    from exact_io_aware_fa_gb300 import synthetic
+    api, orc = env
+    B, Hq, Hkv, Tq, Tk, d, window = 1, 32, 16, 150, 1400, 64, 90
+    bits = synthetic.attention_inputs_ex(B, Hq, Hkv, Tq, Tk, d, seed=77, with_dout=True)
+    scale = default_scale(d)
+    q, k, v, o, lse = run_fwd(api, bits, True, window, scale)
+    do = to_dev(bits["do"])
+    dq, dk, dv = api.backward(q, k, v, o, lse, do, causal=True, scale=scale, window=window)
+    torch.cuda.synchronize()
+    assert api.device_error() == 0
+    ref = orc.backward_ex(bits["q"], bits["k"], bits["v"], bits["do"], True, scale, window)
+    for name, a, b in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
+        assert_close_grad(to_f64(a), b, name, "many units, empty tiles")
