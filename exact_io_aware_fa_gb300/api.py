@@ -25,8 +25,9 @@ FA_ERR_TIMEOUT = 5
 # Every symbol include/fa.h declares.
 EXPORTS = ("fa_forward", "fa_forward_ex", "fa_forward_splitkv_workspace_bytes",
            "fa_forward_splitkv", "fa_backward_workspace_bytes", "fa_backward",
-           "fa_backward_ex", "fa_backward_noalloc", "fa_selftest_wait_timeout",
-           "fa_status_string", "fa_last_cuda_error", "fa_device_error")
+           "fa_backward_ex", "fa_backward_noalloc", "fa_forward_backward_host_device_bytes",
+           "fa_forward_backward_host", "fa_selftest_wait_timeout", "fa_status_string",
+           "fa_last_cuda_error", "fa_device_error")
 
 # Size of the library's own backward workspace (FA_NOALLOC_SCRATCH_BYTES in include/fa.h).
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
@@ -77,6 +78,11 @@ def library(path: str | None = None):
         lib.fa_backward_ex.restype = I
         lib.fa_backward_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, P]
         lib.fa_backward_noalloc.restype = I
+        lib.fa_forward_backward_host_device_bytes.argtypes = [I, I, I, I, I, I, I]
+        lib.fa_forward_backward_host_device_bytes.restype = Z
+        lib.fa_forward_backward_host.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I,
+                                                 I, F, I, P, P]
+        lib.fa_forward_backward_host.restype = I
         lib.fa_selftest_wait_timeout.argtypes = [ctypes.c_uint, P]
         lib.fa_selftest_wait_timeout.restype = I
         lib.fa_status_string.argtypes = [I]
@@ -147,6 +153,22 @@ def backward_noalloc_raw(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, causal, 
 
 def backward_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
     return int(library().fa_backward_workspace_bytes(B, H, N, d))
+
+
+MAX_HOST_CHUNKS = 16  # FA_MAX_HOST_CHUNKS in include/fa.h
+
+
+def host_step_device_bytes(B: int, Hq: int, Hkv: int, Tq: int, Tk: int, d: int,
+                           nchunks: int = 0) -> int:
+    return int(library().fa_forward_backward_host_device_bytes(B, Hq, Hkv, Tq, Tk, d, nchunks))
+
+
+def forward_backward_host_raw(q, k, v, dout, o, lse, dq, dk, dv, B, Hq, Hkv, Tq, Tk, d, causal,
+                              window, scale, nchunks, device_buffer, stream) -> int:
+    """fa_forward_backward_host: one forward + backward step on host buffers."""
+    return library().fa_forward_backward_host(q, k, v, dout, o, lse, dq, dk, dv, B, Hq, Hkv, Tq,
+                                              Tk, d, causal, window, scale, nchunks,
+                                              device_buffer, stream)
 
 
 def selftest_wait_timeout(limit_us: int, stream: int | None = None) -> None:
@@ -292,6 +314,72 @@ def backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = 
                              float(scale), ws_ptr, s)
     _check(st, "fa_backward_ex")
     return dq, dk, dv
+
+
+def _check_host(name, t, shape=None, dtype=None):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cpu":
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}")
+
+
+def forward_backward_host(q, k, v, dout, causal: bool = False, scale: float | None = None,
+                          window: int = -1, nchunks: int = 0, out=None, device_buffer=None,
+                          device=None, stream=None):
+    """One forward + backward step on host tensors (pinned for overlap): returns host
+    (O, LSE, dQ, dK, dV). Shapes as ``forward``; ``out`` = optional tuple of the five output
+    tensors; ``device_buffer`` = optional uint8 CUDA tensor of ``host_step_device_bytes`` bytes.
+    The call is asynchronous on ``stream`` (synchronise before reading the outputs)."""
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v), ("dout", dout)):
+        _check_host(name, t, dtype=torch.bfloat16)
+        if t.dim() != 4:
+            raise ValueError(f"{name} must be 4-D")
+    B, Hq, Tq, d = q.shape
+    _, Hkv, Tk, _ = k.shape
+    if tuple(k.shape) != (B, Hkv, Tk, d) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError(f"k, v must both be [B, Hkv, Tk, d] = {(B, Hkv, Tk, d)}")
+    _check_host("dout", dout, q.shape)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        pin = q.is_pinned()
+        def alloc(shape, dt):
+            return torch.empty(shape, dtype=dt, pin_memory=pin)
+        out = (alloc(q.shape, torch.bfloat16), alloc((B, Hq, Tq), torch.float32),
+               alloc(q.shape, torch.bfloat16), alloc(k.shape, torch.bfloat16),
+               alloc(k.shape, torch.bfloat16))
+    o, lse, dq, dk, dv = out
+    _check_host("o", o, q.shape, torch.bfloat16)
+    _check_host("lse", lse, (B, Hq, Tq), torch.float32)
+    _check_host("dq", dq, q.shape, torch.bfloat16)
+    _check_host("dk", dk, k.shape, torch.bfloat16)
+    _check_host("dv", dv, k.shape, torch.bfloat16)
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    need = host_step_device_bytes(B, Hq, Hkv, Tq, Tk, d, nchunks)
+    if device_buffer is None and need > 0:
+        device_buffer = torch.empty(need, dtype=torch.uint8, device=dev)
+    buf_ptr = 0
+    if device_buffer is not None:
+        _check_tensor("device_buffer", device_buffer)
+        if device_buffer.numel() * device_buffer.element_size() < need:
+            raise ValueError(f"device_buffer needs {need} bytes")
+        buf_ptr = device_buffer.data_ptr()
+    s = stream if stream is not None else torch.cuda.current_stream(dev).cuda_stream
+    with torch.cuda.device(dev):
+        st = forward_backward_host_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), dout.data_ptr(),
+                                       o.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                       dv.data_ptr(), B, Hq, Hkv, Tq, Tk, d, int(bool(causal)),
+                                       int(window), float(scale), int(nchunks), buf_ptr, s)
+    _check(st, "fa_forward_backward_host")
+    return o, lse, dq, dk, dv
 
 
 # ---- autograd -----------------------------------------------------------------------------

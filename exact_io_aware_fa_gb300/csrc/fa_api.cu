@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <climits>
 #include <cmath>
 #include <cstdint>
@@ -220,6 +221,94 @@ __global__ void fa_wait_selftest_kernel(int* err, unsigned long long limit_ns) {
     }
     __syncthreads();
     fa::warp_wait(fa::ptx::smem_addr(&bar), 0, &abort_flag, err, fa::kDevTimeoutLoad, limit_ns);
+}
+
+// ---- host-buffer step (fa_forward_backward_host) ----------------------------------------
+
+// Streams and events of the host-buffer step, created once per device and reused; g_host_mu is
+// held while a step is enqueued, so reusing the events is safe (a stream wait takes the state of
+// the event's latest record at the time of the wait call).
+struct HostStepRes {
+    bool ready = false;
+    cudaStream_t in = nullptr, out = nullptr, comp[2] = {nullptr, nullptr};
+    cudaEvent_t entry = nullptr, done = nullptr;
+    cudaEvent_t in_done[FA_MAX_HOST_CHUNKS] = {};
+    cudaEvent_t fwd_done[FA_MAX_HOST_CHUNKS] = {};
+    cudaEvent_t comp_done[FA_MAX_HOST_CHUNKS] = {};
+};
+std::mutex g_host_mu;
+HostStepRes g_host_res[kMaxDevices];
+
+fa_status host_step_resources(HostStepRes** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+    HostStepRes& r = g_host_res[dev];
+    if (!r.ready) {
+        cudaStream_t* ss[4] = {&r.in, &r.out, &r.comp[0], &r.comp[1]};
+        for (cudaStream_t* sp : ss)
+            if ((e = cudaStreamCreateWithFlags(sp, cudaStreamNonBlocking)) != cudaSuccess) return cuda_fail(e);
+        if ((e = cudaEventCreateWithFlags(&r.entry, cudaEventDisableTiming)) != cudaSuccess) return cuda_fail(e);
+        if ((e = cudaEventCreateWithFlags(&r.done, cudaEventDisableTiming)) != cudaSuccess) return cuda_fail(e);
+        for (int c = 0; c < FA_MAX_HOST_CHUNKS; ++c) {
+            if ((e = cudaEventCreateWithFlags(&r.in_done[c], cudaEventDisableTiming)) != cudaSuccess)
+                return cuda_fail(e);
+            if ((e = cudaEventCreateWithFlags(&r.fwd_done[c], cudaEventDisableTiming)) != cudaSuccess)
+                return cuda_fail(e);
+            if ((e = cudaEventCreateWithFlags(&r.comp_done[c], cudaEventDisableTiming)) != cudaSuccess)
+                return cuda_fail(e);
+        }
+        r.ready = true;
+    }
+    *out = &r;
+    return FA_OK;
+}
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+// First KV head of chunk c (of nch, nearly equal shares) over nkv heads.
+int chunk_start(int c, int nch, int nkv) { return (int)((long long)nkv * c / nch); }
+
+// Chunks of the host-buffer step and its device layout: the device copies of every tensor at
+// full size, then one backward workspace per compute stream, sized for the largest chunk.
+struct HostPlan {
+    int nch, group, kv_per_chunk_max;
+    size_t q_bytes, kv_bytes, lse_bytes, ws_bytes;
+    size_t off_q, off_k, off_v, off_do, off_o, off_lse, off_dq, off_dk, off_dv, off_ws, total;
+};
+
+HostPlan host_plan(const Shape& sh, int nchunks) {
+    HostPlan p;
+    const int nkv = sh.BHkv;
+    int n = nchunks == 0 ? 4 : nchunks;
+    p.nch = std::max(1, std::min(n, std::max(1, nkv)));
+    p.group = sh.Hkv > 0 ? sh.Hq / sh.Hkv : 1;
+    p.kv_per_chunk_max = 0;
+    for (int c = 0; c < p.nch; ++c)
+        p.kv_per_chunk_max = std::max(p.kv_per_chunk_max, chunk_start(c + 1, p.nch, nkv) - chunk_start(c, p.nch, nkv));
+    p.q_bytes = (size_t)sh.BHq * (size_t)sh.Tq * (size_t)sh.d * 2u;
+    p.kv_bytes = (size_t)sh.BHkv * (size_t)sh.Tk * (size_t)sh.d * 2u;
+    p.lse_bytes = (size_t)sh.BHq * (size_t)sh.Tq * sizeof(float);
+    p.ws_bytes = workspace_bytes((long long)p.kv_per_chunk_max * p.group, sh.Tq, sh.d);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off += round256(bytes);
+        return o;
+    };
+    p.off_q = take(p.q_bytes);
+    p.off_k = take(p.kv_bytes);
+    p.off_v = take(p.kv_bytes);
+    p.off_do = take(p.q_bytes);
+    p.off_o = take(p.q_bytes);
+    p.off_lse = take(p.lse_bytes);
+    p.off_dq = take(p.q_bytes);
+    p.off_dk = take(p.kv_bytes);
+    p.off_dv = take(p.kv_bytes);
+    p.off_ws = take(2 * round256(p.ws_bytes));
+    p.total = off;
+    return p;
 }
 
 }  // namespace
@@ -440,6 +529,151 @@ fa_status fa_selftest_wait_timeout(unsigned int limit_us, struct CUstream_st* st
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
     return FA_OK;
+}
+
+size_t fa_forward_backward_host_device_bytes(int B, int Hq, int Hkv, int Tq, int Tk, int d,
+                                             int nchunks) {
+    if (nchunks < 0 || nchunks > FA_MAX_HOST_CHUNKS) return 0;
+    Shape sh;
+    bool empty = false;
+    // the shape rules of the device calls (causal = 0 accepts every Tq / Tk pairing)
+    if (check_shape(B, Hq, Hkv, Tq, Tk, d, 0, -1, 1.0f, &sh, &empty) != FA_OK) return 0;
+    return host_plan(sh, nchunks).total;
+}
+
+fa_status fa_forward_backward_host(const void* q, const void* k, const void* v, const void* dout,
+                                   void* o, float* lse, void* dq, void* dk, void* dv, int B,
+                                   int Hq, int Hkv, int Tq, int Tk, int d, int causal, int window,
+                                   float scale, int nchunks, void* device_buffer,
+                                   struct CUstream_st* stream) {
+    if (nchunks < 0 || nchunks > FA_MAX_HOST_CHUNKS) return FA_ERR_INVALID_ARG;
+    Shape sh;
+    bool empty = false;
+    fa_status st = check_shape(B, Hq, Hkv, Tq, Tk, d, causal, window, scale, &sh, &empty);
+    if (st != FA_OK) return st;
+    const HostPlan p = host_plan(sh, nchunks);
+    if (p.q_bytes > 0 && (!q || !dout || !o || !lse || !dq)) return FA_ERR_INVALID_ARG;
+    if (p.kv_bytes > 0 && (!k || !v || !dk || !dv)) return FA_ERR_INVALID_ARG;
+    if (p.q_bytes == 0 && p.kv_bytes == 0) return FA_OK;
+    if (device_buffer && !aligned(device_buffer, 256)) return FA_ERR_INVALID_ARG;
+    if ((st = bind_context()) != FA_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    std::lock_guard<std::mutex> lk(g_host_mu);
+    HostStepRes* r = nullptr;
+    if ((st = host_step_resources(&r)) != FA_OK) return st;
+    uint8_t* buf = static_cast<uint8_t*>(device_buffer);
+    bool owned = false;
+    cudaError_t e = cudaSuccess;
+    if (!buf) {
+        void* m = nullptr;
+        if ((e = cudaMallocAsync(&m, p.total, s)) != cudaSuccess) return cuda_fail(e);
+        buf = static_cast<uint8_t*>(m);
+        owned = true;
+    }
+    // Every failure past this point still joins the internal streams back into `stream`, so
+    // that nothing queued here outlives a buffer the caller or the library frees afterwards.
+    fa_status result = FA_OK;
+    auto fail = [&](cudaError_t err) {
+        if (result == FA_OK) result = cuda_fail(err);
+    };
+    if ((e = cudaEventRecord(r->entry, s)) != cudaSuccess) {
+        if (owned) cudaFreeAsync(buf, s);
+        return cuda_fail(e);
+    }
+    cudaStream_t all[4] = {r->in, r->out, r->comp[0], r->comp[1]};
+    for (cudaStream_t x : all)
+        if ((e = cudaStreamWaitEvent(x, r->entry, 0)) != cudaSuccess) fail(e);
+
+    const size_t qrow = (size_t)Tq * d * 2u, krow = (size_t)Tk * d * 2u, lrow = (size_t)Tq * 4u;
+    const uint8_t* hq = static_cast<const uint8_t*>(q);
+    const uint8_t* hk = static_cast<const uint8_t*>(k);
+    const uint8_t* hv = static_cast<const uint8_t*>(v);
+    const uint8_t* hdo = static_cast<const uint8_t*>(dout);
+    auto kv0_of = [&](int c) { return chunk_start(c, p.nch, sh.BHkv); };
+    // copies in
+    for (int c = 0; c < p.nch && result == FA_OK; ++c) {
+        const size_t h0 = (size_t)kv0_of(c), h1 = (size_t)kv0_of(c + 1);
+        const size_t g0 = h0 * p.group, g1 = h1 * p.group;
+        const struct { size_t off; const uint8_t* src; size_t row, a, b; } cp[4] = {
+            {p.off_q, hq, qrow, g0, g1}, {p.off_k, hk, krow, h0, h1},
+            {p.off_v, hv, krow, h0, h1}, {p.off_do, hdo, qrow, g0, g1}};
+        for (const auto& x : cp) {
+            const size_t bytes = (x.b - x.a) * x.row;
+            if (bytes == 0) continue;
+            e = cudaMemcpyAsync(buf + x.off + x.a * x.row, x.src + x.a * x.row, bytes,
+                                cudaMemcpyHostToDevice, r->in);
+            if (e != cudaSuccess) fail(e);
+        }
+        if ((e = cudaEventRecord(r->in_done[c], r->in)) != cudaSuccess) fail(e);
+    }
+    // kernels: chunk c on compute stream c % 2, with that stream's workspace
+    for (int c = 0; c < p.nch && result == FA_OK; ++c) {
+        const int h0 = kv0_of(c), h1 = kv0_of(c + 1);
+        const int nkv = h1 - h0, nq = nkv * p.group;
+        cudaStream_t cs = r->comp[c & 1];
+        if ((e = cudaStreamWaitEvent(cs, r->in_done[c], 0)) != cudaSuccess) {
+            fail(e);
+            break;
+        }
+        const size_t g0 = (size_t)h0 * p.group;
+        uint8_t* ws = buf + p.off_ws + (size_t)(c & 1) * round256(p.ws_bytes);
+        CUstream_st* csx = reinterpret_cast<CUstream_st*>(cs);
+        // A chunk is the flattened [B*H] layout cut along heads: batch 1 with nq query heads
+        // over nkv KV heads keeps query head j on KV head j / group.
+        fa_status st2 = fa_forward_ex(buf + p.off_q + g0 * qrow, buf + p.off_k + h0 * krow,
+                                      buf + p.off_v + h0 * krow, buf + p.off_o + g0 * qrow,
+                                      reinterpret_cast<float*>(buf + p.off_lse + g0 * lrow), 1, nq,
+                                      nkv, Tq, Tk, d, causal, window, scale, csx);
+        if (st2 == FA_OK && (e = cudaEventRecord(r->fwd_done[c], cs)) != cudaSuccess) fail(e);
+        if (st2 == FA_OK && result == FA_OK)
+            st2 = fa_backward_ex(buf + p.off_q + g0 * qrow, buf + p.off_k + h0 * krow,
+                                 buf + p.off_v + h0 * krow, buf + p.off_o + g0 * qrow,
+                                 reinterpret_cast<const float*>(buf + p.off_lse + g0 * lrow),
+                                 buf + p.off_do + g0 * qrow, buf + p.off_dq + g0 * qrow,
+                                 buf + p.off_dk + h0 * krow, buf + p.off_dv + h0 * krow, 1, nq, nkv,
+                                 Tq, Tk, d, causal, window, scale, ws, csx);
+        if (st2 != FA_OK) {
+            result = st2;
+            break;
+        }
+        if ((e = cudaEventRecord(r->comp_done[c], cs)) != cudaSuccess) fail(e);
+    }
+    // copies out: O and LSE once the chunk's forward is done, the gradients after its backward
+    uint8_t* ho = static_cast<uint8_t*>(o);
+    uint8_t* hl = reinterpret_cast<uint8_t*>(lse);
+    uint8_t* hdq = static_cast<uint8_t*>(dq);
+    uint8_t* hdk = static_cast<uint8_t*>(dk);
+    uint8_t* hdv = static_cast<uint8_t*>(dv);
+    for (int c = 0; c < p.nch && result == FA_OK; ++c) {
+        const size_t h0 = (size_t)kv0_of(c), h1 = (size_t)kv0_of(c + 1);
+        const size_t g0 = h0 * p.group, g1 = h1 * p.group;
+        const struct { size_t off; uint8_t* dst; size_t row, a, b; } cp[5] = {
+            {p.off_o, ho, qrow, g0, g1}, {p.off_lse, hl, lrow, g0, g1}, {p.off_dq, hdq, qrow, g0, g1},
+            {p.off_dk, hdk, krow, h0, h1}, {p.off_dv, hdv, krow, h0, h1}};
+        for (int i = 0; i < 5 && result == FA_OK; ++i) {
+            if (i == 0 || i == 2) {
+                cudaEvent_t ev = (i == 0) ? r->fwd_done[c] : r->comp_done[c];
+                if ((e = cudaStreamWaitEvent(r->out, ev, 0)) != cudaSuccess) {
+                    fail(e);
+                    break;
+                }
+            }
+            const auto& x = cp[i];
+            const size_t bytes = (x.b - x.a) * x.row;
+            if (bytes == 0) continue;
+            e = cudaMemcpyAsync(x.dst + x.a * x.row, buf + x.off + x.a * x.row, bytes,
+                                cudaMemcpyDeviceToHost, r->out);
+            if (e != cudaSuccess) fail(e);
+        }
+    }
+    // join: every internal stream's work is done before later work on `stream`
+    for (cudaStream_t x : all) {
+        if ((e = cudaEventRecord(r->done, x)) != cudaSuccess) fail(e);
+        if ((e = cudaStreamWaitEvent(s, r->done, 0)) != cudaSuccess) fail(e);
+    }
+    if (owned && (e = cudaFreeAsync(buf, s)) != cudaSuccess) fail(e);
+    return result;
 }
 
 fa_status fa_device_error(struct CUstream_st* stream, int* code) {

@@ -186,6 +186,47 @@ fa_status fa_backward_noalloc(const void* q, const void* k, const void* v, const
                               struct CUstream_st* stream);
 
 /*
+ * One forward + backward step on host-resident tensors (no counterpart in the pages: an
+ * integration convenience for callers whose activations live in host memory). Copies Q, K, V
+ * and dO to the device, runs fa_forward_ex and then fa_backward_ex on them, and copies O, LSE,
+ * dQ, dK and dV back. The KV heads, flattened over the batch, are cut into `nchunks` chunks
+ * of nearly equal size, each with the query heads that read them. Every chunk's copies in, its
+ * two kernels and its copies out (O and LSE once its forward is done, the gradients after its
+ * backward) go to internal streams -- one for copies in, two for kernels, one for copies out --
+ * so that one chunk's copies overlap other chunks' kernels. Results equal those of
+ * fa_forward_ex and fa_backward_ex on the same inputs (dQ up to the order in which its fp32
+ * partial sums are added).
+ *   q, dout in : host bf16 [B,Hq,Tq,d];  k, v in : host bf16 [B,Hkv,Tk,d]
+ *   o out : host bf16 [B,Hq,Tq,d];  lse out : host fp32 [B,Hq,Tq]
+ *   dq out: host bf16 [B,Hq,Tq,d];  dk, dv out: host bf16 [B,Hkv,Tk,d]
+ *   Host buffers should be page-locked (cudaHostAlloc or cudaHostRegister) for the copies to
+ *   overlap with the kernels; pageable memory gives the same results without the overlap.
+ *   nchunks: 1 .. FA_MAX_HOST_CHUNKS, or 0 for the library's choice (4); a value above B*Hkv
+ *            is reduced to B*Hkv.
+ *   device_buffer: >= fa_forward_backward_host_device_bytes(B, Hq, Hkv, Tq, Tk, d, nchunks)
+ *            bytes of device memory, 256-byte aligned, used until the step is done on
+ *            `stream`; or NULL, in which case the library allocates and frees it on `stream`
+ *            (cudaMallocAsync).
+ *   stream: the step starts after the work queued on `stream` before the call, and work
+ *           queued on `stream` after the call starts once the step, copies out included, is
+ *           done. As with cudaMemcpyAsync, the host buffers must stay valid and unmodified
+ *           until then. Calls from several host threads are serialised while they enqueue.
+ * Errors as fa_forward_ex and fa_backward_ex; FA_ERR_INVALID_ARG for a NULL tensor pointer
+ * where that tensor has elements, or nchunks outside 0 .. FA_MAX_HOST_CHUNKS.
+ */
+#define FA_MAX_HOST_CHUNKS 16
+
+/* Device bytes fa_forward_backward_host needs (0 for invalid arguments). */
+size_t fa_forward_backward_host_device_bytes(int B, int Hq, int Hkv, int Tq, int Tk, int d,
+                                             int nchunks);
+
+fa_status fa_forward_backward_host(const void* q, const void* k, const void* v, const void* dout,
+                                   void* o, float* lse, void* dq, void* dk, void* dv, int B,
+                                   int Hq, int Hkv, int Tq, int Tk, int d, int causal, int window,
+                                   float scale, int nchunks, void* device_buffer,
+                                   struct CUstream_st* stream);
+
+/*
  * Diagnostic of the failure path (no counterpart in the pages). Launches one warp that waits,
  * through the same bounded mbarrier wait the attention kernels use, on a barrier nothing ever
  * arrives on; after `limit_us` microseconds (1 .. 1000000) the wait gives up, records code 1

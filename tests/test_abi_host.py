@@ -184,3 +184,47 @@ def test_split_choice():
     assert api.choose_splits(1, 8, 1, 16384, 152) == 32          # 8 rows, 128 key tiles
     assert api.choose_splits(1, 8, 1, 300, 152) == 1             # too few key tiles to split
     assert api.choose_splits(1, 1, 1, 1 << 20, 152) == api.MAX_SPLITS
+
+
+def host_step(lib, q=A, k=A, v=A, do=A, o=A, lse=A, dq=A, dk=A, dv=A, B=1, Hq=2, Hkv=1, Tq=128,
+              Tk=256, d=64, causal=1, window=-1, scale=0.125, nchunks=0, buf=None):
+    return lib.fa_forward_backward_host(q, k, v, do, o, lse, dq, dk, dv, B, Hq, Hkv, Tq, Tk, d,
+                                        causal, window, scale, nchunks, buf, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(nchunks=-1), 1), (dict(nchunks=17), 1), (dict(q=0), 1), (dict(do=0), 1),
+    (dict(lse=0), 1), (dict(dq=0), 1), (dict(k=0), 1), (dict(dv=0), 1),
+    (dict(buf=A + 16), 1), (dict(Hq=3, Hkv=2), 1), (dict(Tq=300), 1), (dict(window=5, causal=0), 1),
+    (dict(d=96), 2),
+])
+def test_host_step_rejects(lib, kw, status):
+    # every one of these is refused before any CUDA call (no GPU here)
+    assert host_step(lib, **kw) == status
+
+
+def test_host_step_empty_is_ok(lib):
+    assert host_step(lib, B=0) == 0
+    assert host_step(lib, Hq=0, Hkv=0, q=0, k=0, v=0, do=0, o=0, lse=0, dq=0, dk=0, dv=0) == 0
+
+
+def test_host_step_device_bytes():
+    from exact_io_aware_fa_gb300 import api
+    r = lambda x: (x + 255) // 256 * 256
+
+    def expect(B, Hq, Hkv, Tq, Tk, d, nch):
+        nkv = B * Hkv
+        nch = min(nch or 4, nkv)
+        starts = [nkv * c // nch for c in range(nch + 1)]
+        per = max(b - a for a, b in zip(starts, starts[1:])) * (Hq // Hkv)  # largest chunk
+        ws = api.backward_workspace_bytes(1, per, Tq, d)
+        q = B * Hq * Tq * d * 2
+        kv = B * Hkv * Tk * d * 2
+        return 4 * r(q) + 4 * r(kv) + r(B * Hq * Tq * 4) + 2 * r(ws)
+
+    for args in [(1, 2, 1, 128, 256, 64, 0), (4, 16, 16, 2048, 2048, 64, 0),
+                 (2, 8, 2, 100, 300, 128, 3), (1, 4, 4, 1, 777, 64, 16), (3, 6, 3, 50, 50, 128, 1)]:
+        assert api.host_step_device_bytes(*args) == expect(*args), args
+    assert api.host_step_device_bytes(1, 2, 1, 128, 256, 64, 0) == 411136
+    assert api.host_step_device_bytes(1, 2, 1, 128, 256, 64, 17) == 0
+    assert api.host_step_device_bytes(1, 2, 1, 128, 256, 96, 0) == 0
