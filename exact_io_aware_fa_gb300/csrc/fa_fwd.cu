@@ -111,12 +111,17 @@ struct FwdShape {
     int Tq, Tk, Hq, Hkv, group, offset, window, nqb;
     int nsplit;  // key-range splits per unit (flash-decoding); 1 = whole range, final output
     int BHq;     // B * Hq (partial-result indexing)
+    // Units numbered from full_units on are half units (non-causal, unsplit launches): the
+    // 256-row block full_units + (h >> 1) cut into its two Q tiles, h & 1 selecting one. They
+    // fill a last round that would otherwise leave most SMs idle.
+    int full_units;
 };
 
 // One work unit: (query head bh_q, 256-row block qb) and, per Q tile t, its range of key
 // tiles [jb_t, je_t) (empty when the tile lies past Tq).
 struct FwdUnit {
     int bh_q, bh_kv, qb, split;
+    int row0;  // first query row of Q tile 0
     int jb0, je0, jb1, je1;
     int jb_all, je_all;
     __device__ __forceinline__ int jb(int t) const { return t ? jb1 : jb0; }
@@ -140,6 +145,12 @@ __device__ __forceinline__ FwdUnit fwd_unit(int u, const FwdShape& sh) {
     using C = FwdCfg<D>;
     FwdUnit w;
     w.split = 0;
+    int half = -1;  // a half unit's Q tile (0 or 1); -1 for a full unit
+    if (!CAUSAL && !SPLIT && u >= sh.full_units) {
+        const int h = u - sh.full_units;
+        u = sh.full_units + (h >> 1);
+        half = h & 1;
+    }
     if (SPLIT) {
         w.split = u % sh.nsplit;  // the splits of one query block are consecutive units
         u /= sh.nsplit;
@@ -173,8 +184,12 @@ __device__ __forceinline__ FwdUnit fwd_unit(int u, const FwdShape& sh) {
             je = min(je, b0 + c);
         }
     };
-    range(w.qb * C::ROWS, w.jb0, w.je0);
-    range(w.qb * C::ROWS + C::BM, w.jb1, w.je1);
+    w.row0 = w.qb * C::ROWS + (half > 0 ? C::BM : 0);
+    range(w.row0, w.jb0, w.je0);
+    if (half >= 0)
+        w.jb1 = w.je1 = 0;  // a half unit is its one Q tile, run as tile 0
+    else
+        range(w.row0 + C::BM, w.jb1, w.je1);
     if (!SPLIT) {
         // tile 0 always has keys without splits
         w.jb_all = w.jb0;
@@ -271,7 +286,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 for (int t = 0; t < ntl; ++t)
                     for (int ch = 0; ch < C::DCH; ++ch)
                         ptx::tma_load_3d_hint(s_q + (b * 2 + t) * C::TILE_BYTES + ch * C::CHUNK_BYTES,
-                                              &tm_q, bq, ch * 64, w.qb * C::ROWS + t * C::BM, w.bh_q,
+                                              &tm_q, bq, ch * 64, w.row0 + t * C::BM, w.bh_q,
                                               pol_q);
                 last_q_use[b] = use;
                 for (int j = w.jb_all; j < w.je_all; ++j, ++kv) {
@@ -429,7 +444,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             const int jb = w.jb(t), je = w.je(t);
             const int n = je - jb;
             const int b = ul % C::NQB;
-            const int row0 = w.qb * C::ROWS + t * C::BM;
+            const int row0 = w.row0 + t * C::BM;
             const int row = row0 + r;
             const int pos = sh.offset + row;               // this row's key position
             const int pos_first = sh.offset + row0;        // first row of the tile
@@ -734,11 +749,23 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
     sh.nqb = (a.Tq + C::ROWS - 1) / C::ROWS;
     sh.nsplit = SPLIT ? a.nsplit : 1;
     sh.BHq = a.BHq;
-    const long long units = (long long)sh.nqb * a.BHq * sh.nsplit;
+    long long units = (long long)sh.nqb * a.BHq * sh.nsplit;
     if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     // Persistent grid: one CTA per SM (the shared-memory footprint admits no more), each
     // walking its units in the order fwd_unit_index gives.
-    const int grid = (int)std::min<long long>(units, (long long)a.num_sms);
+    const long long sms = std::max(1, a.num_sms);
+    sh.full_units = (int)units;
+    if (!CAUSAL && !SPLIT) {
+        // Equal units: a last round at most half full runs as half units (one Q tile each)
+        // on twice as many SMs; a one-tile unit takes ~81 % of a two-tile unit's time.
+        const long long rem = units % sms;
+        if (units > sms && rem > 0 && 2 * rem <= sms) {
+            sh.full_units = (int)(units - rem);
+            units += rem;
+        }
+    }
+    if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const int grid = (int)std::min<long long>(units, sms);
     kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, sh,
                                                       (int)units, a.c, a.lse, a.part_o,
                                                       a.part_lse, a.err);

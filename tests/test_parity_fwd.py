@@ -164,3 +164,25 @@ def test_persistent_many_units_per_cta(env, d, causal, N):
     o_ref, lse_ref = orc.forward_bf16(bits["q"], bits["k"], bits["v"], causal, default_scale(d))
     assert_close_o(o, o_ref, f"many units N={N} d={d} causal={causal}", small_case=True)
     assert_close_lse(lse, lse_ref, f"many units N={N} d={d} causal={causal}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N", [200, 300])
+def test_half_units_in_last_round(env, d, N):
+    """Non-causal launches whose last round of (head, 256-row block) units would fill at most
+    half of the SMs run that round as half units, one 128-row Q tile each. Sizes chosen from
+    the device's SM count so that a few units are left over; with N = 300 the second tile of
+    every block is ragged and one half unit of each leftover block is past the end (empty)."""
+    import torch
+    from exact_io_aware_fa_gb300 import synthetic
+    api, orc = env
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    nqb = -(-N // 256)
+    H = (sms + 8 + nqb - 1) // nqb          # units = H * nqb = sms + (a few)
+    units = H * nqb
+    assert units > sms and 0 < units % sms <= sms // 2
+    bits = synthetic.attention_inputs(1, H, N, d, seed=700 + N + d)
+    o, lse = run_fwd(api, bits, False, default_scale(d))
+    o_ref, lse_ref = orc.forward_bf16(bits["q"], bits["k"], bits["v"], False, default_scale(d))
+    assert_close_o(o, o_ref, f"half units N={N} d={d}", small_case=True)
+    assert_close_lse(lse, lse_ref, f"half units N={N} d={d}")
