@@ -224,15 +224,25 @@ MAX_SPLITS = 64  # FA_MAX_SPLITS in include/fa.h
 
 
 def choose_splits(B: int, Hq: int, Tq: int, Tk: int, num_sms: int) -> int:
-    """Key-range splits for the forward: 1 when the 256-row query blocks alone give every SM
-    two or more work units, else enough splits for about four units per SM, each keeping at
-    least four 128-key tiles."""
+    """Key-range splits for the forward, from a cost model in units of one 128-key tile step
+    (fitted to GB300 timings of decode and chunked-prefill shapes): with n splits the launch
+    runs ceil(units * n / SMs) rounds of units costing ceil(tiles / n) steps plus a fixed cost
+    per unit (Q load, epilogue and partial-result writes: ~2 steps for a single query row, ~5.5
+    for full 256-row blocks), and the merge adds ~2. Splits are used only when they beat the
+    unsplit launch by 10 %; among equal costs the fewest splits win."""
     units = -(-Tq // 256) * B * Hq
-    if units <= 0 or units >= 2 * num_sms:
-        return 1
     tiles = -(-Tk // 128)
-    want = -(-4 * num_sms // units)
-    return max(1, min(MAX_SPLITS, want, tiles // 4))
+    if units <= 0 or tiles <= 1:
+        return 1
+    fixed = 2.0 + 3.5 * min(Tq, 256) / 256.0
+    merge = 2.0
+    unsplit = -(-units // num_sms) * (tiles + fixed)
+    best_n, best = 1, None
+    for n in range(2, min(MAX_SPLITS, tiles) + 1):
+        c = -(-units * n // num_sms) * (-(-tiles // n) + fixed) + merge
+        if best is None or c < best:
+            best_n, best = n, c
+    return best_n if best is not None and best < 0.9 * unsplit else 1
 
 
 def forward(q, k, v, causal: bool = False, scale: float | None = None, window: int = -1,

@@ -115,6 +115,10 @@ struct FwdShape {
     // 256-row block full_units + (h >> 1) cut into its two Q tiles, h & 1 selecting one. They
     // fill a last round that would otherwise leave most SMs idle.
     int full_units;
+    // Causal: 0 for the pairs order, else the sorted order with q_chunk query heads per chunk
+    // (chosen so that a chunk's K/V stays in L2); inside a chunk units go heaviest block first,
+    // head by head (with splits: the key chunks of a block are consecutive units).
+    int q_chunk;
 };
 
 // One work unit: (query head bh_q, 256-row block qb) and, per Q tile t, its range of key
@@ -124,19 +128,31 @@ struct FwdUnit {
     int row0;  // first query row of Q tile 0
     int jb0, je0, jb1, je1;
     int jb_all, je_all;
+    // No key tile for either Q tile (an empty key chunk, or a half unit past Tq): such a unit
+    // takes no part in the Q-buffer protocol (no load, no q_full / q_free phase), and every
+    // role counts Q-buffer uses over the other units only.
+    __device__ __forceinline__ bool empty() const { return je_all <= jb_all; }
     __device__ __forceinline__ int jb(int t) const { return t ? jb1 : jb0; }
     __device__ __forceinline__ int je(int t) const { return t ? je1 : je0; }
 };
 
-// The k-th unit of CTA `cta` (of G), or -1 past the end. Units are numbered head by head.
-// Non-causal: plain round robin. Causal: a head's blocks are ordered heaviest, lightest,
-// second heaviest, second lightest, ... and each CTA takes consecutive pairs, so every pair
-// (and so every CTA's share of a round) costs about the same while concurrently running CTAs
-// still work on a few neighbouring heads (their K/V stays in L2).
+// The k-th unit of CTA `cta` (of G), or -1 past the end.
+// Non-causal: plain round robin over units numbered head by head (all cost the same).
+// Causal, sorted order (sh.q_chunk > 0): units are numbered heaviest first (see fwd_unit) and
+// dealt in snake order -- round k goes to CTAs 0 .. G-1 when k is even and G-1 .. 0 when odd --
+// so every CTA's running sum of cost stays close to the others' and the launch ends on the
+// lightest units. Causal otherwise: a head's blocks are ordered heaviest, lightest, second
+// heaviest, second lightest, ... and each CTA takes consecutive pairs (with cost linear in the
+// block index every pair costs the same, and a round works on a few neighbouring heads).
 template <bool CAUSAL>
-__device__ __forceinline__ int fwd_unit_index(int cta, int k, int G, int U) {
-    const long long u = CAUSAL ? 2LL * (cta + (long long)(k >> 1) * G) + (k & 1)
-                               : cta + (long long)k * G;
+__device__ __forceinline__ int fwd_unit_index(int cta, int k, int G, int U, bool sorted) {
+    long long u;
+    if (!CAUSAL)
+        u = cta + (long long)k * G;
+    else if (sorted)
+        u = (long long)k * G + ((k & 1) ? (G - 1 - cta) : cta);
+    else
+        u = 2LL * (cta + (long long)(k >> 1) * G) + (k & 1);
     return u < U ? (int)u : -1;
 }
 
@@ -155,13 +171,25 @@ __device__ __forceinline__ FwdUnit fwd_unit(int u, const FwdShape& sh) {
         w.split = u % sh.nsplit;  // the splits of one query block are consecutive units
         u /= sh.nsplit;
     }
-    w.bh_q = u / sh.nqb;
-    const int i = u % sh.nqb;
-    if (CAUSAL) {
-        const int q = (i & 1) ? sh.nqb - 1 - (i >> 1) : (i >> 1);  // rank by cost, 0 = heaviest
-        w.qb = sh.nqb - 1 - q;
+    if (CAUSAL && sh.q_chunk > 0) {
+        // chunk of q_chunk query heads (the last may be smaller); inside it, rank-major: all
+        // heads' heaviest block (the last one), then all heads' next, ...
+        const uint32_t per_chunk = (uint32_t)sh.q_chunk * (uint32_t)sh.nqb;
+        const uint32_t chunk = (uint32_t)u / per_chunk;
+        const uint32_t r = (uint32_t)u - chunk * per_chunk;
+        const uint32_t h0 = chunk * (uint32_t)sh.q_chunk;
+        const uint32_t hc = min((uint32_t)sh.q_chunk, (uint32_t)sh.BHq - h0);
+        w.bh_q = (int)(h0 + r % hc);
+        w.qb = sh.nqb - 1 - (int)(r / hc);
     } else {
-        w.qb = i;
+        w.bh_q = u / sh.nqb;
+        const int i = u % sh.nqb;
+        if (CAUSAL) {
+            const int q = (i & 1) ? sh.nqb - 1 - (i >> 1) : (i >> 1);  // rank by cost, 0 = heaviest
+            w.qb = sh.nqb - 1 - q;
+        } else {
+            w.qb = i;
+        }
     }
     w.bh_kv = (w.bh_q / sh.Hq) * sh.Hkv + (w.bh_q % sh.Hq) / sh.group;
     const int nk = (sh.Tk + C::BN - 1) / C::BN;
@@ -268,14 +296,17 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             const uint64_t pol_q = ptx::l2_policy_evict_first();
             int kv = 0;   // K/V tiles loaded so far (ring position)
             int ul = 0;   // units started by this CTA
+            int qn = 0;   // non-empty units started (Q-buffer uses)
             int last_q_use[2] = {-1, -1};
             bool ok = true;
-            for (int u; ok && (u = fwd_unit_index<CAUSAL>(blockIdx.x, ul, G, num_units)) >= 0; ++ul) {
+            for (int u; ok && (u = fwd_unit_index<CAUSAL>(blockIdx.x, ul, G, num_units, sh.q_chunk > 0)) >= 0; ++ul) {
                 const FwdUnit w = fwd_unit<D, CAUSAL, WINDOW, SPLIT>(u, sh);
-                const int b = ul % C::NQB;
-                const int use = ul / C::NQB;  // earlier uses of Q buffer b
+                if (w.empty()) continue;
+                const int b = qn % C::NQB;
+                const int use = qn / C::NQB;  // earlier uses of Q buffer b
+                ++qn;
                 if (use > 0) {
-                    // the epilogues of unit (ul - NQB) staged O in this buffer and stored it
+                    // the epilogues of the unit NQB uses back staged O in this buffer and stored it
                     ok = wait_phase(ptx::smem_addr(&bars->q_free[b]), (uint32_t)(use - 1) & 1u,
                                     abort_flag, err, kDevTimeoutSoftmax);
                     if (!ok) break;
@@ -342,13 +373,17 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         int uo[2] = {0, 0};  // units in which each Q tile ran (PV issuer: o_free phases)
         int kv = 0;
         int ul = 0;
+        int qn = 0;  // non-empty units (Q-buffer uses)
         bool ok = true;
-        for (int u; ok && (u = fwd_unit_index<CAUSAL>(blockIdx.x, ul, G, num_units)) >= 0; ++ul) {
+        for (int u; ok && (u = fwd_unit_index<CAUSAL>(blockIdx.x, ul, G, num_units, sh.q_chunk > 0)) >= 0; ++ul) {
             const FwdUnit w = fwd_unit<D, CAUSAL, WINDOW, SPLIT>(u, sh);
-            const int b = ul % C::NQB;
+            if (w.empty()) continue;
+            const int b = qn % C::NQB;
+            const uint32_t qph = (uint32_t)(qn / C::NQB) & 1u;
+            ++qn;
             if (warp == 1) {
-                ok = warp_wait(ptx::smem_addr(&bars->q_full[b]), (uint32_t)(ul / C::NQB) & 1u,
-                               abort_flag, err, kDevTimeoutLoad);
+                ok = warp_wait(ptx::smem_addr(&bars->q_full[b]), qph, abort_flag, err,
+                               kDevTimeoutLoad);
                 for (int j = w.jb_all; ok && j < w.je_all; ++j, ++kv) {
                     const int s = kv % C::NS;
                     ok = warp_wait(ptx::smem_addr(&bars->k_full[s]), (uint32_t)(kv / C::NS) & 1u,
@@ -438,12 +473,16 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const uint32_t b_o_done = ptx::smem_addr(&bars->o_done[t]);
         int it = 0;  // score tiles of this Q tile processed so far (all units)
         int ul = 0;
+        int qn = 0;  // non-empty units (Q-buffer uses)
         bool ok = true;
-        for (int u; ok && (u = fwd_unit_index<CAUSAL>(blockIdx.x, ul, G, num_units)) >= 0; ++ul) {
+        for (int u; ok && (u = fwd_unit_index<CAUSAL>(blockIdx.x, ul, G, num_units, sh.q_chunk > 0)) >= 0; ++ul) {
             const FwdUnit w = fwd_unit<D, CAUSAL, WINDOW, SPLIT>(u, sh);
             const int jb = w.jb(t), je = w.je(t);
             const int n = je - jb;
-            const int b = ul % C::NQB;
+            const bool unit_empty = w.empty();
+            const int b = qn % C::NQB;
+            const uint32_t qph = (uint32_t)(qn / C::NQB) & 1u;
+            qn += unit_empty ? 0 : 1;
             const int row0 = w.row0 + t * C::BM;
             const int row = row0 + r;
             const int pos = sh.offset + row;               // this row's key position
@@ -459,14 +498,15 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             const size_t prow = ((size_t)w.split * sh.BHq + w.bh_q) * (size_t)sh.Tq + row;
             if (n == 0) {
                 // No key tile of this Q tile in this unit (rows past Tq, or an empty split
-                // chunk): release its share of the Q buffer. It first waits for this unit's Q
-                // load, so that its arrival counts towards this use of the buffer and cannot
-                // complete an earlier use's phase ahead of the other tile's epilogue (an
-                // mbarrier counts arrivals, not arrivers).
+                // chunk). A unit empty for both tiles has no Q-buffer use. Otherwise release
+                // this tile's share of the buffer: first wait for this use's Q load, so that
+                // the arrival counts towards this use and cannot complete an earlier use's
+                // phase ahead of the other tile's epilogue (an mbarrier counts arrivals, not
+                // arrivers).
                 if (SPLIT && row < sh.Tq) part_lse[prow] = -INFINITY;  // merge skips it
-                ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->q_full[b]),
-                                                        (uint32_t)(ul / C::NQB) & 1u, abort_flag,
-                                                        err, kDevTimeoutLoad));
+                if (unit_empty) continue;
+                ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->q_full[b]), qph,
+                                                        abort_flag, err, kDevTimeoutLoad));
                 if (!ok) break;
                 if (r == 0) ptx::mbar_arrive(ptx::smem_addr(&bars->q_free[b]));
                 continue;
@@ -730,6 +770,13 @@ fa_fwd_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ 
     if (lane == 0) lse[row] = (sum > 0.f) ? mx + logf(sum) : -INFINITY;
 }
 
+// Causal sorted order: L2 budget for the K/V of one chunk, and the largest launch (in units
+// per SM) that uses it without a window. Measured: up to 16 units per SM the sorted order wins
+// by 10-90 % (the pairs order leaves SMs idle in its last round); at 27 and 54 units per SM
+// (B1 H64 N16384, B8 H32 N8192, d=128) it is even or up to 2 % slower (L2 reuse).
+constexpr long long kFwdChunkL2Bytes = 128LL << 20;
+constexpr long long kSortedMaxRounds = 16;
+
 template <int D, bool CAUSAL, bool WINDOW, bool SPLIT>
 cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
     static_assert(CAUSAL || !WINDOW, "a window hangs off the causal diagonal");
@@ -755,6 +802,15 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
     // walking its units in the order fwd_unit_index gives.
     const long long sms = std::max(1, a.num_sms);
     sh.full_units = (int)units;
+    sh.q_chunk = 0;
+    if (CAUSAL && (SPLIT || WINDOW || units <= kSortedMaxRounds * sms)) {
+        // Sorted order: few rounds (the tail of the pairs order costs up to a round), a window
+        // (block costs are not linear in the block index, so pairs are unequal) or key splits
+        // (a block's equal chunks must go to different SMs).
+        // K and V bytes a query head reads (its KV head's, shared by the group):
+        const long long per_head = std::max(1LL, 2LL * a.Tk * D * 2 / std::max(1, sh.group));
+        sh.q_chunk = (int)std::max(1LL, std::min<long long>(a.BHq, kFwdChunkL2Bytes / per_head));
+    }
     if (!CAUSAL && !SPLIT) {
         // Equal units: a last round at most half full runs as half units (one Q tile each)
         // on twice as many SMs; a one-tile unit takes ~81 % of a two-tile unit's time.

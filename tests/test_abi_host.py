@@ -180,8 +180,11 @@ def test_splitkv_workspace_bytes(lib):
 def test_split_choice():
     from exact_io_aware_fa_gb300 import api
     assert api.choose_splits(4, 16, 2048, 2048, 152) == 1        # 512 blocks fill the GPU
-    assert api.choose_splits(8, 32, 1, 16384, 152) == 3          # 256 decode rows: ~4 units/SM
-    assert api.choose_splits(1, 8, 1, 16384, 152) == 32          # 8 rows, 128 key tiles
+    assert api.choose_splits(8, 32, 1, 16384, 152) == 1          # 256 decode rows fill it too
+    assert api.choose_splits(1, 8, 1, 16384, 152) == 19          # 8 rows x 19 chunks = 152 SMs
+    assert api.choose_splits(1, 32, 1, 16384, 152) == 4          # 32 rows x 4 chunks, one round
+    assert api.choose_splits(1, 32, 512, 16384, 152) == 2        # chunked prefill, 64 blocks
+    assert api.choose_splits(1, 32, 1024, 16384, 152) == 1       # 128 blocks: no split
     assert api.choose_splits(1, 8, 1, 300, 152) == 1             # too few key tiles to split
     assert api.choose_splits(1, 1, 1, 1 << 20, 152) == api.MAX_SPLITS
 

@@ -57,6 +57,26 @@ def test_splitkv_matches_oracle(env, case):
     assert_close_lse(to_f64(lse), lse_ref, ids(case))
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_runs_of_empty_key_chunks(env, d):
+    """Many more key splits than key tiles, and several units per SM: most units of every SM
+    are key chunks with no tile for either Q tile, often several in a row. Such units release
+    their Q buffer at once; the kernel must not lose track of the buffer's phases."""
+    import torch
+    from exact_io_aware_fa_gb300 import synthetic
+    api, orc = env
+    B, Hq, Hkv, Tq, Tk, nsplit = 2, 40, 8, 256, 640, 16   # 5 key tiles, 16 splits
+    bits = synthetic.attention_inputs_ex(B, Hq, Hkv, Tq, Tk, d, seed=77 + d)
+    q, k, v = (to_dev(bits[n]) for n in ("q", "k", "v"))
+    scale = default_scale(d)
+    o, lse = api.forward(q, k, v, causal=True, scale=scale, nsplit=nsplit)
+    torch.cuda.synchronize()
+    assert api.device_error() == 0
+    o_ref, lse_ref = orc.forward_ex(bits["q"], bits["k"], bits["v"], True, scale)
+    assert_close_o(to_f64(o), o_ref, f"empty chunks d={d}")
+    assert_close_lse(to_f64(lse), lse_ref, f"empty chunks d={d}")
+
+
 def test_one_split_is_the_plain_forward(env):
     """nsplit = 1 runs fa_forward_ex: bit-identical output."""
     import torch
