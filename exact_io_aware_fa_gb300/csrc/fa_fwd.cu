@@ -115,9 +115,9 @@ struct FwdShape {
     // 256-row block full_units + (h >> 1) cut into its two Q tiles, h & 1 selecting one. They
     // fill a last round that would otherwise leave most SMs idle.
     int full_units;
-    // Causal: 0 for the pairs order, else the sorted order with q_chunk query heads per chunk
-    // (chosen so that a chunk's K/V stays in L2); inside a chunk units go heaviest block first,
-    // head by head (with splits: the key chunks of a block are consecutive units).
+    // Causal, sorted order: query heads per chunk (chosen so that a chunk's K/V stays in L2);
+    // inside a chunk units go heaviest block first, head by head (with splits: the key chunks
+    // of a block are consecutive units).
     int q_chunk;
 };
 
@@ -138,25 +138,25 @@ struct FwdUnit {
 
 // The k-th unit of CTA `cta` (of G), or -1 past the end.
 // Non-causal: plain round robin over units numbered head by head (all cost the same).
-// Causal, sorted order (sh.q_chunk > 0): units are numbered heaviest first (see fwd_unit) and
+// Causal, SORTED: units are numbered heaviest first (see fwd_unit) and
 // dealt in snake order -- round k goes to CTAs 0 .. G-1 when k is even and G-1 .. 0 when odd --
 // so every CTA's running sum of cost stays close to the others' and the launch ends on the
 // lightest units. Causal otherwise: a head's blocks are ordered heaviest, lightest, second
 // heaviest, second lightest, ... and each CTA takes consecutive pairs (with cost linear in the
 // block index every pair costs the same, and a round works on a few neighbouring heads).
-template <bool CAUSAL>
-__device__ __forceinline__ int fwd_unit_index(int cta, int k, int G, int U, bool sorted) {
+template <bool CAUSAL, bool SORTED>
+__device__ __forceinline__ int fwd_unit_index(int cta, int k, int G, int U) {
     long long u;
     if (!CAUSAL)
         u = cta + (long long)k * G;
-    else if (sorted)
+    else if (SORTED)
         u = (long long)k * G + ((k & 1) ? (G - 1 - cta) : cta);
     else
         u = 2LL * (cta + (long long)(k >> 1) * G) + (k & 1);
     return u < U ? (int)u : -1;
 }
 
-template <int D, bool CAUSAL, bool WINDOW, bool SPLIT>
+template <int D, bool CAUSAL, bool WINDOW, bool SPLIT, bool SORTED>
 __device__ __forceinline__ FwdUnit fwd_unit(int u, const FwdShape& sh) {
     using C = FwdCfg<D>;
     FwdUnit w;
@@ -171,7 +171,7 @@ __device__ __forceinline__ FwdUnit fwd_unit(int u, const FwdShape& sh) {
         w.split = u % sh.nsplit;  // the splits of one query block are consecutive units
         u /= sh.nsplit;
     }
-    if (CAUSAL && sh.q_chunk > 0) {
+    if (CAUSAL && SORTED) {
         // chunk of q_chunk query heads (the last may be smaller); inside it, rank-major: all
         // heads' heaviest block (the last one), then all heads' next, ...
         const uint32_t per_chunk = (uint32_t)sh.q_chunk * (uint32_t)sh.nqb;
@@ -234,7 +234,7 @@ __device__ __forceinline__ FwdUnit fwd_unit(int u, const FwdShape& sh) {
 
 // WINDOW (causal only): keys before position - window are not visible. SPLIT: every unit is
 // one key chunk of a query block and writes a partial result for the merge kernel.
-template <int D, bool CAUSAL, bool WINDOW, bool SPLIT>
+template <int D, bool CAUSAL, bool WINDOW, bool SPLIT, bool SORTED>
 __global__ void __launch_bounds__(384, 1)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -299,8 +299,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             int qn = 0;   // non-empty units started (Q-buffer uses)
             int last_q_use[2] = {-1, -1};
             bool ok = true;
-            for (int u; ok && (u = fwd_unit_index<CAUSAL>(blockIdx.x, ul, G, num_units, sh.q_chunk > 0)) >= 0; ++ul) {
-                const FwdUnit w = fwd_unit<D, CAUSAL, WINDOW, SPLIT>(u, sh);
+            for (int u; ok && (u = fwd_unit_index<CAUSAL, SORTED>(blockIdx.x, ul, G, num_units)) >= 0; ++ul) {
+                const FwdUnit w = fwd_unit<D, CAUSAL, WINDOW, SPLIT, SORTED>(u, sh);
                 if (w.empty()) continue;
                 const int b = qn % C::NQB;
                 const int use = qn / C::NQB;  // earlier uses of Q buffer b
@@ -375,8 +375,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         int ul = 0;
         int qn = 0;  // non-empty units (Q-buffer uses)
         bool ok = true;
-        for (int u; ok && (u = fwd_unit_index<CAUSAL>(blockIdx.x, ul, G, num_units, sh.q_chunk > 0)) >= 0; ++ul) {
-            const FwdUnit w = fwd_unit<D, CAUSAL, WINDOW, SPLIT>(u, sh);
+        for (int u; ok && (u = fwd_unit_index<CAUSAL, SORTED>(blockIdx.x, ul, G, num_units)) >= 0; ++ul) {
+            const FwdUnit w = fwd_unit<D, CAUSAL, WINDOW, SPLIT, SORTED>(u, sh);
             if (w.empty()) continue;
             const int b = qn % C::NQB;
             const uint32_t qph = (uint32_t)(qn / C::NQB) & 1u;
@@ -475,8 +475,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         int ul = 0;
         int qn = 0;  // non-empty units (Q-buffer uses)
         bool ok = true;
-        for (int u; ok && (u = fwd_unit_index<CAUSAL>(blockIdx.x, ul, G, num_units, sh.q_chunk > 0)) >= 0; ++ul) {
-            const FwdUnit w = fwd_unit<D, CAUSAL, WINDOW, SPLIT>(u, sh);
+        for (int u; ok && (u = fwd_unit_index<CAUSAL, SORTED>(blockIdx.x, ul, G, num_units)) >= 0; ++ul) {
+            const FwdUnit w = fwd_unit<D, CAUSAL, WINDOW, SPLIT, SORTED>(u, sh);
             const int jb = w.jb(t), je = w.je(t);
             const int n = je - jb;
             const bool unit_empty = w.empty();
@@ -777,14 +777,24 @@ fa_fwd_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ 
 constexpr long long kFwdChunkL2Bytes = 128LL << 20;
 constexpr long long kSortedMaxRounds = 16;
 
+template <int D, bool CAUSAL, bool WINDOW, bool SPLIT, bool SORTED>
+cudaError_t run_fwd_kernel(const FwdLaunch& a, const FwdShape& sh, int units, cudaStream_t stream) {
+    using C = FwdCfg<D>;
+    auto kern = fa_fwd_kernel<D, CAUSAL, WINDOW, SPLIT, SORTED>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int grid = std::min(units, std::max(1, a.num_sms));
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, sh, units,
+                                                      a.c, a.lse, a.part_o, a.part_lse, a.err);
+    return cudaGetLastError();
+}
+
 template <int D, bool CAUSAL, bool WINDOW, bool SPLIT>
 cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
     static_assert(CAUSAL || !WINDOW, "a window hangs off the causal diagonal");
     using C = FwdCfg<D>;
-    auto kern = fa_fwd_kernel<D, CAUSAL, WINDOW, SPLIT>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
+    cudaError_t e = cudaSuccess;
     FwdShape sh;
     sh.Tq = a.Tq;
     sh.Tk = a.Tk;
@@ -802,8 +812,9 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
     // walking its units in the order fwd_unit_index gives.
     const long long sms = std::max(1, a.num_sms);
     sh.full_units = (int)units;
-    sh.q_chunk = 0;
-    if (CAUSAL && (SPLIT || WINDOW || units <= kSortedMaxRounds * sms)) {
+    sh.q_chunk = 1;
+    const bool sorted = CAUSAL && (SPLIT || WINDOW || units <= kSortedMaxRounds * sms);
+    if (sorted) {
         // Sorted order: few rounds (the tail of the pairs order costs up to a round), a window
         // (block costs are not linear in the block index, so pairs are unequal) or key splits
         // (a block's equal chunks must go to different SMs).
@@ -821,11 +832,15 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
         }
     }
     if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    const int grid = (int)std::min<long long>(units, sms);
-    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, sh,
-                                                      (int)units, a.c, a.lse, a.part_o,
-                                                      a.part_lse, a.err);
-    e = cudaGetLastError();
+    // Kernel variants: non-causal launches use the round robin; windowed and split causal
+    // launches always use the sorted order; plain causal launches use either.
+    if constexpr (!CAUSAL)
+        e = run_fwd_kernel<D, CAUSAL, WINDOW, SPLIT, false>(a, sh, (int)units, stream);
+    else if constexpr (WINDOW || SPLIT)
+        e = run_fwd_kernel<D, CAUSAL, WINDOW, SPLIT, true>(a, sh, (int)units, stream);
+    else
+        e = sorted ? run_fwd_kernel<D, CAUSAL, WINDOW, SPLIT, true>(a, sh, (int)units, stream)
+                   : run_fwd_kernel<D, CAUSAL, WINDOW, SPLIT, false>(a, sh, (int)units, stream);
     if (e != cudaSuccess || !SPLIT) return e;
     const long long rows = (long long)a.BHq * a.Tq;
     const long long blocks = (rows + 7) / 8;
