@@ -125,3 +125,21 @@ def test_persistent_many_units_per_cta(env, d, causal):
     api, orc = env
     bits = synthetic.attention_inputs(2, 200, 300, d, seed=310 + d, with_dout=True)
     check_full(api, orc, bits, causal, default_scale(d), f"many units d={d} causal={causal}")
+
+
+def test_causal_unit_order_in_several_head_chunks(env):
+    """Causal launches order their units key tile by key tile inside chunks of KV heads whose
+    Q/dO fit in 128 MB of L2. B1 H40 N8192 d128 needs 4 MB per head: chunks of 32 and 8 heads
+    (the last one ragged). dQ on seeded query rows, dK/dV on seeded key rows."""
+    from exact_io_aware_fa_gb300 import synthetic
+    api, orc = env
+    B, H, N, d = 1, 40, 8192, 128
+    bits = synthetic.attention_inputs(B, H, N, d, seed=4040, with_dout=True)
+    dq, dk, dv = run_fwd_bwd(api, bits, True, default_scale(d))
+    rq = synthetic.sample_rows(N, 16, 4040)
+    rk = synthetic.sample_rows(N, 16, 5040)
+    ref_q, ref_k, ref_v = orc.backward_rows_bf16(bits["q"], bits["k"], bits["v"], bits["do"], True,
+                                                 default_scale(d), rq, rk)
+    assert_close_grad(dq[:, :, rq], ref_q, "dQ", "head chunks")
+    assert_close_grad(dk[:, :, rk], ref_k, "dK", "head chunks")
+    assert_close_grad(dv[:, :, rk], ref_v, "dV", "head chunks")

@@ -186,3 +186,10 @@ def test_half_units_in_last_round(env, d, N):
     o_ref, lse_ref = orc.forward_bf16(bits["q"], bits["k"], bits["v"], False, default_scale(d))
     assert_close_o(o, o_ref, f"half units N={N} d={d}", small_case=True)
     assert_close_lse(lse, lse_ref, f"half units N={N} d={d}")
+
+
+def test_sorted_causal_order_in_several_head_chunks(env):
+    """A causal launch of at most 16 units per SM deals its units heaviest first inside chunks
+    of heads whose K/V fits in 128 MB of L2. B1 H36 N16384 d128 reads 8 MB of K/V per head:
+    chunks of 16, 16 and 4 heads (the last one ragged); 2304 units, under 16 per SM on 152."""
+    _sampled(env, 1, 36, 16384, 128, True, 4041, 1.0)

@@ -130,3 +130,21 @@ def test_automatic_split_choice_for_decode(env):
     o_ref, lse_ref = orc.forward_ex(bits["q"], bits["k"], bits["v"], True, default_scale(d))
     assert_close_o(to_f64(o), o_ref, "auto", small_case=True)
     assert_close_lse(to_f64(lse), lse_ref, "auto")
+
+
+def test_split_decode_in_several_head_chunks(env):
+    """Split launches use the sorted order over chunks of heads: one query row against 65536
+    keys reads 32 MB of K/V per head, so 10 heads form chunks of 4, 4 and 2."""
+    import torch
+    from exact_io_aware_fa_gb300 import synthetic
+    api, orc = env
+    B, Hq, Hkv, Tq, Tk, d = 1, 10, 10, 1, 65536, 128
+    bits = synthetic.attention_inputs_ex(B, Hq, Hkv, Tq, Tk, d, seed=65)
+    q, k, v = (to_dev(bits[n]) for n in ("q", "k", "v"))
+    scale = default_scale(d)
+    o, lse = api.forward(q, k, v, causal=True, scale=scale, nsplit=8)
+    torch.cuda.synchronize()
+    assert api.device_error() == 0
+    o_ref, lse_ref = orc.forward_ex(bits["q"], bits["k"], bits["v"], True, scale)
+    assert_close_o(to_f64(o), o_ref, "decode head chunks", small_case=True)
+    assert_close_lse(to_f64(lse), lse_ref, "decode head chunks")
