@@ -91,6 +91,12 @@ fa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __re
                   float inv_scale) {
     constexpr int TPR = D / 8;            // threads per row
     constexpr int RPB = 256 / TPR;        // rows per block
+    // Launched as a dependent of whatever kernel precedes it (typically the forward): wait for
+    // it before reading O, LSE, dO or touching the workspace. The main kernel may launch (and
+    // run its prologue) once every block of this one has started; it waits for this kernel's
+    // completion before reading anything it writes.
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
     if (blockIdx.x == 0 && threadIdx.x == 0) *sched = 0u;  // the main kernel's unit counter
     const int sub = threadIdx.x % TPR;
     const long long row_global = (long long)blockIdx.x * RPB + threadIdx.x / TPR;  // over BH*Npad
@@ -137,6 +143,7 @@ template <int D>
 __global__ void __launch_bounds__(256)
 fa_bwd_dq_kernel(const float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dq, int N, int Npad,
                  int BH, float scale) {
+    ptx::griddep_wait();  // the main kernel's dQ sums (this kernel may launch during its tail)
     const long long idx8 = (long long)blockIdx.x * blockDim.x + threadIdx.x;  // 8 elements each
     const long long total8 = (long long)BH * N * (D / 8);
     if (idx8 >= total8) return;
@@ -338,6 +345,11 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         *reinterpret_cast<uint4*>(row + 128) = make_uint4(0u, 0u, 0u, 0u);
         ptx::fence_proxy_async_smem();
     }
+    // The prologue above overlaps the preprocess kernel's last blocks (programmatic dependent
+    // launch); the fold records, the zeroed dQ accumulator and the unit counter it writes are
+    // read only after this wait. The dQ conversion may launch during this kernel's tail.
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
@@ -848,10 +860,10 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t stream) {
         const long long rpb = 256 / (D / 8);
         const long long blocks = (rows + rpb - 1) / rpb;
         if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-        fa_bwd_pre_kernel<D><<<(unsigned)blocks, 256, 0, stream>>>(
+        cudaError_t e = launch_dependent(
+            fa_bwd_pre_kernel<D>, dim3((unsigned)blocks), dim3(256), 0, stream,
             static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.lse,
             static_cast<uint8_t*>(a.folds), a.dq_acc, a.sched, a.Tq, a.Npad, a.BHq, 1.0f / a.scale);
-        cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     // 2. main (persistent; a work unit is one KV head and 128-key tile)
@@ -883,10 +895,10 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t stream) {
         }
         // Persistent grid: one CTA per SM walking units (the shared memory admits one CTA).
         const int grid = (int)std::min<long long>(units, (long long)std::max(1, a.num_sms));
-        kern<<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, stream>>>(
-            a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dk, a.tm_dv, a.tm_dqacc,
-            static_cast<const uint8_t*>(a.folds), sh, (int)units, a.sched, a.c, a.scale, a.err);
-        e = cudaGetLastError();
+        e = launch_dependent(kern, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM_BYTES, stream,
+                             a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dk, a.tm_dv, a.tm_dqacc,
+                             static_cast<const uint8_t*>(a.folds), sh, (int)units, a.sched, a.c,
+                             a.scale, a.err);
         if (e != cudaSuccess) return e;
     }
     // 3. dQ convert (query heads)
@@ -894,9 +906,9 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t stream) {
         const long long total8 = (long long)a.BHq * a.Tq * (D / 8);
         const long long blocks = (total8 + 255) / 256;
         if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-        fa_bwd_dq_kernel<D><<<(unsigned)blocks, 256, 0, stream>>>(
-            a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), a.Tq, a.Npad, a.BHq, a.scale);
-        return cudaGetLastError();
+        return launch_dependent(fa_bwd_dq_kernel<D>, dim3((unsigned)blocks), dim3(256), 0, stream,
+                                static_cast<const float*>(a.dq_acc),
+                                static_cast<__nv_bfloat16*>(a.dq), a.Tq, a.Npad, a.BHq, a.scale);
     }
 }
 

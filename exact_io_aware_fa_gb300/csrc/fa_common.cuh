@@ -1,6 +1,6 @@
 // fa_common.cuh -- pieces shared by the forward and backward attention kernels:
-// bounded mbarrier waits with a CTA-wide abort path, the device error codes, and the
-// 128-byte swizzle used by TMA tiles and tcgen05 operands.
+// bounded mbarrier waits with a CTA-wide abort path, the device error codes, the
+// 128-byte swizzle used by TMA tiles and tcgen05 operands, and dependent launches.
 #pragma once
 
 #include "sm100_ptx.cuh"
@@ -49,6 +49,26 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 // tcgen05 descriptors read with layout type 2). The tile base must be 1024-byte aligned.
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t r, uint32_t u) {
     return r * 128u + ((u ^ (r & 7u)) << 4);
+}
+
+// Launch with programmatic stream serialization: the kernel may start while the one before it
+// in the stream finishes; it calls griddep_wait before using that kernel's results (or any
+// buffer that kernel may still read). Without a programmatic trigger in the kernel before it,
+// the launch behaves like an ordinary one.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
 }  // namespace fa

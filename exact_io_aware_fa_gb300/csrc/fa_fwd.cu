@@ -279,6 +279,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         ptx::tmem_alloc(ptx::smem_addr(&bars->tmem_base), C::TMEM_COLS);
         ptx::tmem_relinquish();
     }
+    // The next kernel in the stream (the split merge, or a backward's preprocess) may start
+    // launching now; it waits for this kernel's completion before using its results.
+    ptx::griddep_launch_dependents();
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
@@ -744,6 +747,7 @@ fa_fwd_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ 
     constexpr int E = D / 32;
     const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
+    ptx::griddep_wait();  // the partials of the attention kernel (this one may launch early)
     if (row >= rows) return;
     float mx = -INFINITY;
     for (int sp = 0; sp < nsplit; ++sp) mx = fmaxf(mx, part_lse[(size_t)sp * rows + row]);
@@ -845,9 +849,9 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
     const long long rows = (long long)a.BHq * a.Tq;
     const long long blocks = (rows + 7) / 8;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    fa_fwd_merge_kernel<D><<<(unsigned)blocks, 256, 0, stream>>>(
-        a.part_o, a.part_lse, static_cast<__nv_bfloat16*>(a.o), a.lse, rows, sh.nsplit);
-    return cudaGetLastError();
+    return launch_dependent(fa_fwd_merge_kernel<D>, dim3((unsigned)blocks), dim3(256), 0, stream,
+                            static_cast<const float*>(a.part_o), static_cast<const float*>(a.part_lse),
+                            static_cast<__nv_bfloat16*>(a.o), a.lse, rows, sh.nsplit);
 }
 
 }  // namespace
