@@ -71,3 +71,14 @@ def assert_close_grad(g, g_ref, name, what=""):
 
 def default_scale(d: int) -> float:
     return 1.0 / math.sqrt(d)
+
+
+def same_up_to_summation_order(a, b) -> bool:
+    """dQ of two runs (torch tensors): its fp32 partial sums from different key tiles are added
+    by atomic reductions in whatever order the tiles finish. That moves a result by about 2^-24
+    of the partials' size, which after bf16 rounding is at most one unit in the last place -- or,
+    where partials cancel to near zero, a small absolute amount (bounded here by 2^-16 of the
+    largest |dQ|). Everything else the kernels compute is deterministic and compared exactly."""
+    a, b = a.float(), b.float()
+    floor = 2.0 ** -16 * float(b.abs().max())
+    return bool(((a - b).abs() <= 2.0 ** -7 * b.abs() + floor).all())

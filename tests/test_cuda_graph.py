@@ -3,8 +3,9 @@ new inputs copied into the captured buffers must give the eager calls' results (
 dV bit for bit; dQ up to the order of its fp32 partial sums). Capture includes the dependent
 launches between the backward's kernels (programmatic graph edges) and, for the host-buffer
 step, the copies and the library's internal streams joined back into the captured stream."""
-import numpy as np
 import pytest
+
+from parity_util import same_up_to_summation_order
 
 pytestmark = pytest.mark.gpu
 
@@ -18,11 +19,6 @@ def api():
     __graft_entry__.build()
     from exact_io_aware_fa_gb300 import api as a
     return a
-
-
-def same_up_to_one_ulp(a, b):
-    a, b = a.float(), b.float()
-    return bool(((a - b).abs() <= 2.0 ** -7 * b.abs() + 2.0 ** -30).all())
 
 
 @pytest.mark.parametrize("causal,window,d", [(False, -1, 64), (True, -1, 128), (True, 300, 64)])
@@ -70,7 +66,7 @@ def test_forward_backward_replay(api, causal, window, d):
         torch.cuda.synchronize()
         assert torch.equal(o, o2) and torch.equal(lse, l2)
         assert torch.equal(dk, g2[1]) and torch.equal(dv, g2[2])
-        assert same_up_to_one_ulp(dq, g2[0])
+        assert same_up_to_summation_order(dq, g2[0])
 
 
 def test_host_step_replay(api):
@@ -106,6 +102,6 @@ def test_host_step_replay(api):
         assert api.device_error() == 0
         for name, a, b in zip(("O", "LSE", "dQ", "dK", "dV"), outs, ref):
             if name == "dQ":
-                assert same_up_to_one_ulp(a, b), name
+                assert same_up_to_summation_order(a, b), name
             else:
                 assert torch.equal(a, b), name

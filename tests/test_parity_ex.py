@@ -8,7 +8,7 @@ import pytest
 
 import oracle
 from parity_util import (assert_close_grad, assert_close_lse, assert_close_o, default_scale,
-                         to_dev, to_f64)
+                         same_up_to_summation_order, to_dev, to_f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -112,8 +112,8 @@ def test_mha_call_matches_ex_call(env):
     assert st == api.FA_OK
     g2 = api.backward(q, k, v, o2, l2, do, causal=True, scale=scale)
     torch.cuda.synchronize()
-    for a, b in zip(g1, g2):
-        assert torch.equal(a, b)
+    assert same_up_to_summation_order(g1[0], g2[0])  # dQ
+    assert torch.equal(g1[1], g2[1]) and torch.equal(g1[2], g2[2])
 
 
 def test_no_query_rows_zeroes_kv_gradients(env):
@@ -170,7 +170,8 @@ def test_autograd_wrapper_matches_raw_calls(env):
     dq2, dk2, dv2 = api.backward(q.detach(), k.detach(), v.detach(), o2, lse2, do, causal=True)
     torch.cuda.synchronize()
     assert torch.equal(o.detach(), o2)
-    assert torch.equal(q.grad, dq2) and torch.equal(k.grad, dk2) and torch.equal(v.grad, dv2)
+    assert same_up_to_summation_order(q.grad, dq2)
+    assert torch.equal(k.grad, dk2) and torch.equal(v.grad, dv2)
 
 
 def test_calls_from_a_new_host_thread(env):
@@ -201,8 +202,8 @@ def test_calls_from_a_new_host_thread(env):
     t.join()
     assert "err" not in out, out.get("err")
     assert torch.equal(out["o"], ref_o)
-    for a, b in zip(out["g"], ref_g):
-        assert torch.equal(a, b)
+    assert same_up_to_summation_order(out["g"][0], ref_g[0])  # dQ
+    assert torch.equal(out["g"][1], ref_g[1]) and torch.equal(out["g"][2], ref_g[2])
 
 
 def test_backward_many_units_with_empty_tiles(env):
