@@ -24,7 +24,8 @@ FA_ERR_TIMEOUT = 5
 
 # Every symbol include/fa.h declares.
 EXPORTS = ("fa_forward", "fa_forward_ex", "fa_forward_splitkv_workspace_bytes",
-           "fa_forward_splitkv", "fa_backward_workspace_bytes", "fa_backward",
+           "fa_forward_splitkv", "fa_forward_choose_splits", "fa_backward_workspace_bytes",
+           "fa_backward",
            "fa_backward_ex", "fa_backward_noalloc", "fa_forward_backward_host_device_bytes",
            "fa_forward_backward_host", "fa_selftest_wait_timeout", "fa_status_string",
            "fa_last_cuda_error", "fa_device_error")
@@ -70,6 +71,8 @@ def library(path: str | None = None):
         lib.fa_forward_splitkv_workspace_bytes.restype = Z
         lib.fa_forward_splitkv.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, P, P]
         lib.fa_forward_splitkv.restype = I
+        lib.fa_forward_choose_splits.argtypes = [I, I, I, I, I, I]
+        lib.fa_forward_choose_splits.restype = I
         lib.fa_backward_workspace_bytes.argtypes = [I, I, I, I]
         lib.fa_backward_workspace_bytes.restype = Z
         lib.fa_backward.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, P, P]
@@ -223,26 +226,9 @@ def _shapes(q, k, v):
 MAX_SPLITS = 64  # FA_MAX_SPLITS in include/fa.h
 
 
-def choose_splits(B: int, Hq: int, Tq: int, Tk: int, num_sms: int) -> int:
-    """Key-range splits for the forward, from a cost model in units of one 128-key tile step
-    (fitted to GB300 timings of decode and chunked-prefill shapes): with n splits the launch
-    runs ceil(units * n / SMs) rounds of units costing ceil(tiles / n) steps plus a fixed cost
-    per unit (Q load, epilogue and partial-result writes: ~2 steps for a single query row, ~5.5
-    for full 256-row blocks), and the merge adds ~2. Splits are used only when they beat the
-    unsplit launch by 10 %; among equal costs the fewest splits win."""
-    units = -(-Tq // 256) * B * Hq
-    tiles = -(-Tk // 128)
-    if units <= 0 or tiles <= 1:
-        return 1
-    fixed = 2.0 + 3.5 * min(Tq, 256) / 256.0
-    merge = 2.0
-    unsplit = -(-units // num_sms) * (tiles + fixed)
-    best_n, best = 1, None
-    for n in range(2, min(MAX_SPLITS, tiles) + 1):
-        c = -(-units * n // num_sms) * (-(-tiles // n) + fixed) + merge
-        if best is None or c < best:
-            best_n, best = n, c
-    return best_n if best is not None and best < 0.9 * unsplit else 1
+def choose_splits(B: int, Hq: int, Hkv: int, Tq: int, Tk: int, num_sms: int) -> int:
+    """Key-range splits for the forward: the library's cost model (fa_forward_choose_splits)."""
+    return int(library().fa_forward_choose_splits(B, Hq, Hkv, Tq, Tk, num_sms))
 
 
 def forward(q, k, v, causal: bool = False, scale: float | None = None, window: int = -1,
@@ -267,7 +253,7 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, window: i
     _check_tensor("lse", lse, (B, Hq, Tq))
     if nsplit is None:
         sms = torch.cuda.get_device_properties(q.device).multi_processor_count
-        nsplit = choose_splits(B, Hq, Tq, Tk, sms)
+        nsplit = choose_splits(B, Hq, Hkv, Tq, Tk, sms)
     ws_ptr = 0
     if nsplit > 1:
         need = splitkv_workspace_bytes(B, Hq, Tq, d, nsplit)

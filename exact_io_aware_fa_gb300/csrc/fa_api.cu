@@ -223,6 +223,12 @@ __global__ void fa_wait_selftest_kernel(int* err, unsigned long long limit_ns) {
     fa::warp_wait(fa::ptx::smem_addr(&bar), 0, &abort_flag, err, fa::kDevTimeoutLoad, limit_ns);
 }
 
+// Query heads of a KV head packed into one block of group * Tq query rows (forward only): for
+// short query blocks (decode, short chunks) a 128-row tile would otherwise carry at most Tq
+// live rows, and every query head would stream its KV head's K and V on its own.
+constexpr int kPackMaxTq = 64;
+bool pack_heads(int Hq, int Hkv, int Tq) { return Hkv > 0 && Hq > Hkv && Tq <= kPackMaxTq; }
+
 // ---- host-buffer step (fa_forward_backward_host) ----------------------------------------
 
 // Streams and events of the host-buffer step, created once per device and reused; g_host_mu is
@@ -345,6 +351,38 @@ size_t fa_forward_splitkv_workspace_bytes(int B, int Hq, int Tq, int d, int nspl
     return splitkv_bytes((long long)B * Hq, Tq, d, nsplit, nullptr);
 }
 
+int fa_forward_choose_splits(int B, int Hq, int Hkv, int Tq, int Tk, int num_sms) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Tq <= 0 || Tk <= 0 || num_sms <= 0 || Hq % Hkv != 0)
+        return 1;
+    // Cost model in 128-key tile steps (fitted to GB300 timings of decode and chunked-prefill
+    // shapes): n splits run ceil(units * n / SMs) rounds of units costing ceil(tiles / n)
+    // steps plus a fixed cost per unit (Q load, epilogue, partial writes: ~2 steps for a
+    // single live query row, ~5.5 for a full 256-row block), and the merge adds ~2. A split is
+    // taken only when it beats the unsplit launch by 10 %; among equal costs the fewest win.
+    // Rounds are counted against 85 % of the SMs: on decode shapes the fastest split launch
+    // had ~128 units for 152 SMs (8 packed blocks: 16 splits 31 us, 19 splits 36 us).
+    const long long sms = std::max(1LL, (long long)num_sms * 85 / 100);
+    const bool packed = pack_heads(Hq, Hkv, Tq);
+    const long long rows = packed ? (long long)(Hq / Hkv) * Tq : Tq;
+    const long long units = (rows + 255) / 256 * (long long)B * (packed ? Hkv : Hq);
+    const long long tiles = ((long long)Tk + 127) / 128;
+    if (tiles <= 1) return 1;
+    const double fixed = 2.0 + 3.5 * (double)std::min<long long>(rows, 256) / 256.0;
+    const double merge = 2.0;
+    const double unsplit = (double)((units + sms - 1) / sms) * ((double)tiles + fixed);
+    int best_n = 1;
+    double best = 0.0;
+    for (int n = 2; n <= FA_MAX_SPLITS && n <= tiles; ++n) {
+        const double rounds = (double)((units * n + sms - 1) / sms);
+        const double c = rounds * ((double)((tiles + n - 1) / n) + fixed) + merge;
+        if (best_n == 1 || c < best) {
+            best_n = n;
+            best = c;
+        }
+    }
+    return (best_n > 1 && best < 0.9 * unsplit) ? best_n : 1;
+}
+
 fa_status fa_forward_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
                              int B, int Hq, int Hkv, int Tq, int Tk, int d, int causal,
                              int window, float scale, int nsplit, void* workspace,
@@ -358,22 +396,28 @@ fa_status fa_forward_splitkv(const void* q, const void* k, const void* v, void* 
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
         return FA_ERR_ALIGNMENT;
     if (nsplit > 1 && workspace && !aligned(workspace, 256)) return FA_ERR_ALIGNMENT;
-    if (((long long)Tq + 255) / 256 * sh.BHq * nsplit > INT_MAX) return FA_ERR_UNSUPPORTED;
+    // With packed heads the kernel sees B*Hkv heads of group*Tq rows each: the same memory,
+    // since a KV head's query heads are adjacent in [B*Hq, Tq, d] (and in LSE [B*Hq, Tq]).
+    const bool packed = pack_heads(Hq, Hkv, Tq);
+    const int rows = packed ? (Hq / Hkv) * Tq : Tq;
+    const int heads = packed ? sh.BHkv : sh.BHq;
+    if (((long long)rows + 255) / 256 * heads * nsplit > INT_MAX) return FA_ERR_UNSUPPORTED;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if ((st = bind_context()) != FA_OK) return st;
     fa::FwdLaunch a;
     std::memset(&a, 0, sizeof a);
-    if ((st = make_map(&a.tm_q, q, sh.BHq, Tq, d, 128)) != FA_OK) return st;
-    if ((st = make_map(&a.tm_o, o, sh.BHq, Tq, d, 128)) != FA_OK) return st;
+    if ((st = make_map(&a.tm_q, q, heads, rows, d, 128)) != FA_OK) return st;
+    if ((st = make_map(&a.tm_o, o, heads, rows, d, 128)) != FA_OK) return st;
     if ((st = make_map(&a.tm_k, k, sh.BHkv, Tk, d, 128)) != FA_OK) return st;
     if ((st = make_map(&a.tm_v, v, sh.BHkv, Tk, d, 128)) != FA_OK) return st;
     if ((st = get_err_ptr(&a.err)) != FA_OK) return st;
     if ((st = get_num_sms(&a.num_sms)) != FA_OK) return st;
-    a.Tq = Tq;
+    a.Tq = rows;
+    a.tq_pos = Tq;
     a.Tk = Tk;
-    a.Hq = Hq;
+    a.Hq = packed ? Hkv : Hq;
     a.Hkv = Hkv;
-    a.BHq = sh.BHq;
+    a.BHq = heads;
     a.window = window;
     a.c = scale * kLog2e;
     a.lse = lse;

@@ -109,6 +109,10 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 // keys before position - window are not visible.
 struct FwdShape {
     int Tq, Tk, Hq, Hkv, group, offset, window, nqb;
+    // Query rows per head for positions: row r of a head's block sits at key position
+    // offset + r % tq_pos. Equal to Tq, except with the query heads of a KV head packed into
+    // one block of group * Tq rows (short query blocks), where Tq counts those rows.
+    int tq_pos;
     int nsplit;  // key-range splits per unit (flash-decoding); 1 = whole range, final output
     int BHq;     // B * Hq (partial-result indexing)
     // Units numbered from full_units on are half units (non-causal, unsplit launches): the
@@ -156,7 +160,20 @@ __device__ __forceinline__ int fwd_unit_index(int cta, int k, int G, int U) {
     return u < U ? (int)u : -1;
 }
 
-template <int D, bool CAUSAL, bool WINDOW, bool SPLIT, bool SORTED>
+// Positions (within a head) of rows r0 .. r1 of a block whose rows hold tq positions per head:
+// their smallest and largest, taken over all positions when the rows wrap into the next
+// packed head.
+__device__ __forceinline__ void tile_positions(int r0, int r1, int tq, int& lo, int& hi) {
+    lo = r0 % tq;
+    hi = r1 % tq;
+    if (r1 - r0 >= tq || hi < lo) {
+        lo = 0;
+        hi = tq - 1;
+    }
+}
+
+// PACKED: query heads packed into blocks of group * Tq rows (positions wrap every tq_pos rows).
+template <int D, bool CAUSAL, bool WINDOW, bool SPLIT, bool SORTED, bool PACKED>
 __device__ __forceinline__ FwdUnit fwd_unit(int u, const FwdShape& sh) {
     using C = FwdCfg<D>;
     FwdUnit w;
@@ -199,8 +216,10 @@ __device__ __forceinline__ FwdUnit fwd_unit(int u, const FwdShape& sh) {
             jb = je = 0;
             return;
         }
-        const int p0 = sh.offset + r0;                                // first row's position
-        const int p1 = sh.offset + min(r0 + C::BM, sh.Tq) - 1;       // last row's position
+        int q0 = r0, q1 = min(r0 + C::BM, sh.Tq) - 1;  // smallest and largest row position
+        if (PACKED) tile_positions(r0, q1, sh.tq_pos, q0, q1);
+        const int p0 = sh.offset + q0;
+        const int p1 = sh.offset + q1;
         je = CAUSAL ? min(nk, p1 / C::BN + 1) : nk;
         jb = WINDOW ? max(0, p0 - sh.window) / C::BN : 0;
         if (jb >= je) jb = je = 0;  // (cannot happen for valid shapes)
@@ -234,7 +253,7 @@ __device__ __forceinline__ FwdUnit fwd_unit(int u, const FwdShape& sh) {
 
 // WINDOW (causal only): keys before position - window are not visible. SPLIT: every unit is
 // one key chunk of a query block and writes a partial result for the merge kernel.
-template <int D, bool CAUSAL, bool WINDOW, bool SPLIT, bool SORTED>
+template <int D, bool CAUSAL, bool WINDOW, bool SPLIT, bool SORTED, bool PACKED>
 __global__ void __launch_bounds__(384, 1)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -303,7 +322,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             int last_q_use[2] = {-1, -1};
             bool ok = true;
             for (int u; ok && (u = fwd_unit_index<CAUSAL, SORTED>(blockIdx.x, ul, G, num_units)) >= 0; ++ul) {
-                const FwdUnit w = fwd_unit<D, CAUSAL, WINDOW, SPLIT, SORTED>(u, sh);
+                const FwdUnit w = fwd_unit<D, CAUSAL, WINDOW, SPLIT, SORTED, PACKED>(u, sh);
                 if (w.empty()) continue;
                 const int b = qn % C::NQB;
                 const int use = qn / C::NQB;  // earlier uses of Q buffer b
@@ -379,7 +398,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         int qn = 0;  // non-empty units (Q-buffer uses)
         bool ok = true;
         for (int u; ok && (u = fwd_unit_index<CAUSAL, SORTED>(blockIdx.x, ul, G, num_units)) >= 0; ++ul) {
-            const FwdUnit w = fwd_unit<D, CAUSAL, WINDOW, SPLIT, SORTED>(u, sh);
+            const FwdUnit w = fwd_unit<D, CAUSAL, WINDOW, SPLIT, SORTED, PACKED>(u, sh);
             if (w.empty()) continue;
             const int b = qn % C::NQB;
             const uint32_t qph = (uint32_t)(qn / C::NQB) & 1u;
@@ -479,7 +498,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         int qn = 0;  // non-empty units (Q-buffer uses)
         bool ok = true;
         for (int u; ok && (u = fwd_unit_index<CAUSAL, SORTED>(blockIdx.x, ul, G, num_units)) >= 0; ++ul) {
-            const FwdUnit w = fwd_unit<D, CAUSAL, WINDOW, SPLIT, SORTED>(u, sh);
+            const FwdUnit w = fwd_unit<D, CAUSAL, WINDOW, SPLIT, SORTED, PACKED>(u, sh);
             const int jb = w.jb(t), je = w.je(t);
             const int n = je - jb;
             const bool unit_empty = w.empty();
@@ -488,9 +507,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             qn += unit_empty ? 0 : 1;
             const int row0 = w.row0 + t * C::BM;
             const int row = row0 + r;
-            const int pos = sh.offset + row;               // this row's key position
-            const int pos_first = sh.offset + row0;        // first row of the tile
-            const int pos_last = sh.offset + min(row0 + C::BM, sh.Tq) - 1;
+            const int pos = sh.offset + (PACKED ? row % sh.tq_pos : row);  // this row's key position
+            int tp0 = row0, tp1 = min(row0 + C::BM, sh.Tq) - 1;  // the tile's extreme positions
+            if (PACKED) tile_positions(row0, tp1, sh.tq_pos, tp0, tp1);
+            const int pos_first = sh.offset + tp0;
+            const int pos_last = sh.offset + tp1;
             // Keys [vis_lo, vis_hi] are visible to this row.
             const int vis_lo = WINDOW ? max(0, pos - sh.window) : 0;
             const int vis_hi = CAUSAL ? min(pos, sh.Tk - 1) : sh.Tk - 1;
@@ -781,10 +802,10 @@ fa_fwd_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ 
 constexpr long long kFwdChunkL2Bytes = 128LL << 20;
 constexpr long long kSortedMaxRounds = 16;
 
-template <int D, bool CAUSAL, bool WINDOW, bool SPLIT, bool SORTED>
+template <int D, bool CAUSAL, bool WINDOW, bool SPLIT, bool SORTED, bool PACKED>
 cudaError_t run_fwd_kernel(const FwdLaunch& a, const FwdShape& sh, int units, cudaStream_t stream) {
     using C = FwdCfg<D>;
-    auto kern = fa_fwd_kernel<D, CAUSAL, WINDOW, SPLIT, SORTED>;
+    auto kern = fa_fwd_kernel<D, CAUSAL, WINDOW, SPLIT, SORTED, PACKED>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -805,7 +826,8 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
     sh.Hq = a.Hq;
     sh.Hkv = a.Hkv;
     sh.group = a.Hq / a.Hkv;
-    sh.offset = a.Tk - a.Tq;
+    sh.tq_pos = a.tq_pos;
+    sh.offset = a.Tk - a.tq_pos;
     sh.window = a.window;
     sh.nqb = (a.Tq + C::ROWS - 1) / C::ROWS;
     sh.nsplit = SPLIT ? a.nsplit : 1;
@@ -817,7 +839,8 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
     const long long sms = std::max(1, a.num_sms);
     sh.full_units = (int)units;
     sh.q_chunk = 1;
-    const bool sorted = CAUSAL && (SPLIT || WINDOW || units <= kSortedMaxRounds * sms);
+    const bool packed = a.tq_pos != a.Tq;  // query heads packed (short blocks): few units
+    const bool sorted = CAUSAL && (packed || SPLIT || WINDOW || units <= kSortedMaxRounds * sms);
     if (sorted) {
         // Sorted order: few rounds (the tail of the pairs order costs up to a round), a window
         // (block costs are not linear in the block index, so pairs are unequal) or key splits
@@ -836,15 +859,18 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
         }
     }
     if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    // Kernel variants: non-causal launches use the round robin; windowed and split causal
-    // launches always use the sorted order; plain causal launches use either.
-    if constexpr (!CAUSAL)
-        e = run_fwd_kernel<D, CAUSAL, WINDOW, SPLIT, false>(a, sh, (int)units, stream);
+    // Kernel variants: non-causal launches use the round robin; windowed, split and packed
+    // causal launches always use the sorted order; plain causal launches use either. Packing
+    // is a variant of its own (its row positions cost the other kernels 2-4 % at run time).
+    if (packed)
+        e = run_fwd_kernel<D, CAUSAL, WINDOW, SPLIT, CAUSAL, true>(a, sh, (int)units, stream);
+    else if constexpr (!CAUSAL)
+        e = run_fwd_kernel<D, CAUSAL, WINDOW, SPLIT, false, false>(a, sh, (int)units, stream);
     else if constexpr (WINDOW || SPLIT)
-        e = run_fwd_kernel<D, CAUSAL, WINDOW, SPLIT, true>(a, sh, (int)units, stream);
+        e = run_fwd_kernel<D, CAUSAL, WINDOW, SPLIT, true, false>(a, sh, (int)units, stream);
     else
-        e = sorted ? run_fwd_kernel<D, CAUSAL, WINDOW, SPLIT, true>(a, sh, (int)units, stream)
-                   : run_fwd_kernel<D, CAUSAL, WINDOW, SPLIT, false>(a, sh, (int)units, stream);
+        e = sorted ? run_fwd_kernel<D, CAUSAL, WINDOW, SPLIT, true, false>(a, sh, (int)units, stream)
+                   : run_fwd_kernel<D, CAUSAL, WINDOW, SPLIT, false, false>(a, sh, (int)units, stream);
     if (e != cudaSuccess || !SPLIT) return e;
     const long long rows = (long long)a.BHq * a.Tq;
     const long long blocks = (rows + 7) / 8;

@@ -9,8 +9,10 @@ namespace fa {
 
 struct FwdLaunch {
     CUtensorMap tm_q, tm_o;              // 3-D maps over [B*Hq, Tq, d] bf16, box {64, 128, 1}
+                                         // (packed: [B*Hkv, group*Tq, d], Hq = Hkv, Tq rows)
     CUtensorMap tm_k, tm_v;              // 3-D maps over [B*Hkv, Tk, d] bf16, box {64, 128, 1}
-    int Tq, Tk;                          // query and key sequence lengths
+    int Tq, Tk;                          // query rows per head block, key sequence length
+    int tq_pos;                          // query positions per head (Tq unless heads are packed)
     int Hq, Hkv;                         // query heads, KV heads (Hq % Hkv == 0)
     int BHq;                             // B * Hq
     int window;                          // -1: none; else keys >= position - window (causal)

@@ -85,6 +85,9 @@ fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float
  *   diagonal). Every query row must see a key: Tk >= 1, and with causal Tq <= Tk; otherwise
  *   FA_ERR_INVALID_ARG. Other arguments and errors as fa_forward, which is this call with
  *   Hq = Hkv = H, Tq = Tk = N, window = -1. B*Hq*Tq == 0 launches nothing.
+ *   With grouped heads and Tq <= 64 (decode, short chunks) the query heads of a KV head are
+ *   processed as one block of (Hq / Hkv) * Tq rows, so each KV head's K and V are read once
+ *   for the whole group; the results are the same.
  */
 fa_status fa_forward_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                         int Hq, int Hkv, int Tq, int Tk, int d, int causal, int window,
@@ -108,6 +111,14 @@ fa_status fa_forward_ex(const void* q, const void* k, const void* v, void* o, fl
 #define FA_MAX_SPLITS 64
 
 size_t fa_forward_splitkv_workspace_bytes(int B, int Hq, int Tq, int d, int nsplit);
+
+/*
+ * A key-split count for fa_forward_splitkv on these sizes and `num_sms` SMs (1: no split):
+ * the library's cost model, in 128-key tile steps, of rounds of (key chunk + fixed per-unit
+ * cost) plus the merge; a split is chosen only when it is clearly cheaper than the unsplit
+ * launch. Pure host logic (no device access). Returns 1 for invalid sizes.
+ */
+int fa_forward_choose_splits(int B, int Hq, int Hkv, int Tq, int Tk, int num_sms);
 
 fa_status fa_forward_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
                              int B, int Hq, int Hkv, int Tq, int Tk, int d, int causal,

@@ -179,14 +179,20 @@ def test_splitkv_workspace_bytes(lib):
 
 def test_split_choice():
     from exact_io_aware_fa_gb300 import api
-    assert api.choose_splits(4, 16, 2048, 2048, 152) == 1        # 512 blocks fill the GPU
-    assert api.choose_splits(8, 32, 1, 16384, 152) == 1          # 256 decode rows fill it too
-    assert api.choose_splits(1, 8, 1, 16384, 152) == 19          # 8 rows x 19 chunks = 152 SMs
-    assert api.choose_splits(1, 32, 1, 16384, 152) == 4          # 32 rows x 4 chunks, one round
-    assert api.choose_splits(1, 32, 512, 16384, 152) == 2        # chunked prefill, 64 blocks
-    assert api.choose_splits(1, 32, 1024, 16384, 152) == 1       # 128 blocks: no split
-    assert api.choose_splits(1, 8, 1, 300, 152) == 1             # too few key tiles to split
-    assert api.choose_splits(1, 1, 1, 1 << 20, 152) == api.MAX_SPLITS
+    c = api.choose_splits
+    assert c(4, 16, 16, 2048, 2048, 152) == 1        # 512 blocks fill the GPU
+    assert c(8, 32, 32, 1, 16384, 152) == 1          # 256 decode rows fill it too
+    assert c(1, 8, 8, 1, 16384, 152) == 16           # 8 rows x 16 chunks = 128 units
+    assert c(1, 32, 32, 1, 16384, 152) == 4          # 32 rows x 4 chunks, one round
+    assert c(1, 32, 32, 512, 16384, 152) == 2        # chunked prefill, 64 blocks
+    assert c(1, 32, 32, 1024, 16384, 152) == 1       # 128 blocks: no split
+    assert c(1, 8, 8, 1, 300, 152) == 1              # too few key tiles to split
+    assert c(1, 1, 1, 1, 1 << 20, 152) == api.MAX_SPLITS
+    # grouped heads with short query blocks are packed: one block per KV head
+    assert c(1, 32, 8, 1, 16384, 152) == 16          # 8 packed blocks x 16 chunks
+    assert c(8, 32, 8, 1, 16384, 152) == 2           # 64 packed blocks x 2 chunks
+    assert c(1, 32, 8, 512, 16384, 152) == 2         # Tq > 64: not packed, as MHA
+    assert c(0, 32, 8, 1, 16384, 152) == 1 and c(1, 32, 5, 1, 16384, 152) == 1  # invalid
 
 
 def host_step(lib, q=A, k=A, v=A, do=A, o=A, lse=A, dq=A, dk=A, dv=A, B=1, Hq=2, Hkv=1, Tq=128,

@@ -38,6 +38,11 @@ CASES = [
     (1, 2, 2, 1000, 1000, 128, True, 129),  # window straddling two key tiles
     (2, 4, 4, 384, 1200, 64, True, 300),    # offset and window together
     (1, 8, 1, 257, 257, 128, True, 1000),   # window wider than the sequence
+    # grouped heads with Tq <= 64 run packed (a KV head's query heads as one block of rows)
+    (2, 8, 2, 33, 700, 128, True, 50),      # packed rows 132 straddle the first tile, window
+    (1, 16, 1, 64, 256, 64, True, -1),      # MQA, 1024 packed rows, causal boundary tile
+    (1, 4, 2, 64, 300, 64, False, -1),      # packed exactly one tile per KV head
+    (1, 4, 2, 65, 300, 64, True, -1),       # Tq = 65: not packed
 ]
 
 

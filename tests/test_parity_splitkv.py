@@ -23,7 +23,11 @@ def env():
 
 
 # (B, Hq, Hkv, Tq, Tk, d, causal, window, nsplit)
+# Grouped heads with Tq <= 64 run packed (a KV head's query heads as one block of rows).
 CASES = [
+    (1, 8, 2, 50, 2000, 64, True, -1, 4),     # packed rows 200: tiles straddle packed heads
+    (1, 8, 1, 64, 3000, 128, True, 600, 3),   # MQA packed into 512 rows (two blocks), window
+    (2, 6, 3, 7, 999, 64, False, -1, 2),      # packed, non-causal, ragged keys
     (2, 8, 2, 1, 3000, 128, True, -1, 8),     # decode against a long cache
     (1, 4, 4, 1, 777, 64, False, -1, 3),      # decode, ragged cache, non-causal
     (1, 2, 2, 300, 1000, 64, True, -1, 3),    # chunked prefill
@@ -122,7 +126,7 @@ def test_automatic_split_choice_for_decode(env):
     api, orc = env
     B, Hq, Hkv, Tq, Tk, d = 2, 4, 1, 1, 4000, 64
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    assert api.choose_splits(B, Hq, Tq, Tk, sms) > 1
+    assert api.choose_splits(B, Hq, Hkv, Tq, Tk, sms) > 1
     bits = synthetic.attention_inputs_ex(B, Hq, Hkv, Tq, Tk, d, seed=21)
     q, k, v = (to_dev(bits[n]) for n in ("q", "k", "v"))
     o, lse = api.forward(q, k, v, causal=True)
