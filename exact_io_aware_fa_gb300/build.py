@@ -15,7 +15,11 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfa.so")
-SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_bwd.cu"]
+# (source, object, extra flags): the forward compiles once per head dimension, in parallel
+SOURCES = [("fa_api.cu", "fa_api.o", []),
+           ("fa_fwd.cu", "fa_fwd_d64.o", ["-DFA_FWD_D=64"]),
+           ("fa_fwd.cu", "fa_fwd_d128.o", ["-DFA_FWD_D=128"]),
+           ("fa_bwd.cu", "fa_bwd.o", [])]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2",
                  "-I", os.path.join(ROOT, "include"), "-Xptxas", "-v"]
@@ -44,16 +48,16 @@ def build(verbose: bool = False) -> str:
     deps = _deps()
     jobs = []
     objs = []
-    for src in SOURCES:
+    for src, obj, flags in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
+        o = os.path.join(BUILD, obj)
         objs.append(o)
         if _stale(o, [s] + deps):
-            jobs.append((s, o))
+            jobs.append((s, o, flags))
 
     def compile_one(job):
-        s, o = job
-        cmd = [nvcc] + CFLAGS + ["-c", s, "-o", o]
+        s, o, flags = job
+        cmd = [nvcc] + CFLAGS + flags + ["-c", s, "-o", o]
         r = subprocess.run(cmd, capture_output=True, text=True)
         log = os.path.join(BUILD, os.path.basename(o) + ".log")
         with open(log, "w") as f:

@@ -895,13 +895,19 @@ cudaError_t launch_fwd_mask(const FwdLaunch& a, bool causal, bool window, bool s
                   : launch_fwd_t<D, true, false, false>(a, stream);
 }
 
-cudaError_t launch_forward(const FwdLaunch& a, int d, bool causal, cudaStream_t stream) {
-    const bool window = a.window >= 0;
-    const bool split = a.nsplit > 1;
-    if (window && !causal) return cudaErrorInvalidValue;
-    if (d == 64) return launch_fwd_mask<64>(a, causal, window, split, stream);
-    if (d == 128) return launch_fwd_mask<128>(a, causal, window, split, stream);
-    return cudaErrorInvalidValue;
+// The build compiles this file once per head dimension (FA_FWD_D = 64, 128) so the two sets of
+// kernel variants compile in parallel; without the macro one object carries both.
+#if !defined(FA_FWD_D) || FA_FWD_D == 64
+cudaError_t launch_forward_d64(const FwdLaunch& a, bool causal, cudaStream_t stream) {
+    if (a.window >= 0 && !causal) return cudaErrorInvalidValue;
+    return launch_fwd_mask<64>(a, causal, a.window >= 0, a.nsplit > 1, stream);
 }
+#endif
+#if !defined(FA_FWD_D) || FA_FWD_D == 128
+cudaError_t launch_forward_d128(const FwdLaunch& a, bool causal, cudaStream_t stream) {
+    if (a.window >= 0 && !causal) return cudaErrorInvalidValue;
+    return launch_fwd_mask<128>(a, causal, a.window >= 0, a.nsplit > 1, stream);
+}
+#endif
 
 }  // namespace fa

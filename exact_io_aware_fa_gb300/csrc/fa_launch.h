@@ -27,7 +27,13 @@ struct FwdLaunch {
 };
 
 // Forward: O and LSE. d in {64, 128}.
-cudaError_t launch_forward(const FwdLaunch& a, int d, bool causal, cudaStream_t stream);
+cudaError_t launch_forward_d64(const FwdLaunch& a, bool causal, cudaStream_t stream);
+cudaError_t launch_forward_d128(const FwdLaunch& a, bool causal, cudaStream_t stream);
+inline cudaError_t launch_forward(const FwdLaunch& a, int d, bool causal, cudaStream_t stream) {
+    if (d == 64) return launch_forward_d64(a, causal, stream);
+    if (d == 128) return launch_forward_d128(a, causal, stream);
+    return cudaErrorInvalidValue;
+}
 
 struct BwdLaunch {
     CUtensorMap tm_q, tm_do;              // [B*Hq, Tq, d] loads, box {64, query rows, 1}
