@@ -35,6 +35,7 @@ CASES = [
     (1, 4, 4, 257, 257, 128, False, -1, 0),    # library's chunk count
     (1, 6, 2, 400, 400, 64, True, 100, 16),    # window; more chunks than KV heads
     (3, 2, 1, 130, 700, 128, True, -1, 1),     # one chunk
+    (2, 8, 2, 40, 500, 64, True, -1, 3),       # Tq <= 64: each chunk's forward packs its heads
 ]
 
 
