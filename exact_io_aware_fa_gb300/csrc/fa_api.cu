@@ -238,7 +238,8 @@ struct HostStepRes {
     bool ready = false;
     cudaStream_t in = nullptr, out = nullptr, comp[2] = {nullptr, nullptr};
     cudaEvent_t entry = nullptr, done = nullptr;
-    cudaEvent_t in_done[FA_MAX_HOST_CHUNKS] = {};
+    cudaEvent_t in_fwd[FA_MAX_HOST_CHUNKS] = {};   // a chunk's Q, K, V landed
+    cudaEvent_t in_done[FA_MAX_HOST_CHUNKS] = {};  // and its dO
     cudaEvent_t fwd_done[FA_MAX_HOST_CHUNKS] = {};
     cudaEvent_t comp_done[FA_MAX_HOST_CHUNKS] = {};
 };
@@ -258,6 +259,8 @@ fa_status host_step_resources(HostStepRes** out) {
         if ((e = cudaEventCreateWithFlags(&r.entry, cudaEventDisableTiming)) != cudaSuccess) return cuda_fail(e);
         if ((e = cudaEventCreateWithFlags(&r.done, cudaEventDisableTiming)) != cudaSuccess) return cuda_fail(e);
         for (int c = 0; c < FA_MAX_HOST_CHUNKS; ++c) {
+            if ((e = cudaEventCreateWithFlags(&r.in_fwd[c], cudaEventDisableTiming)) != cudaSuccess)
+                return cuda_fail(e);
             if ((e = cudaEventCreateWithFlags(&r.in_done[c], cudaEventDisableTiming)) != cudaSuccess)
                 return cuda_fail(e);
             if ((e = cudaEventCreateWithFlags(&r.fwd_done[c], cudaEventDisableTiming)) != cudaSuccess)
@@ -642,12 +645,16 @@ fa_status fa_forward_backward_host(const void* q, const void* k, const void* v, 
         const struct { size_t off; const uint8_t* src; size_t row, a, b; } cp[4] = {
             {p.off_q, hq, qrow, g0, g1}, {p.off_k, hk, krow, h0, h1},
             {p.off_v, hv, krow, h0, h1}, {p.off_do, hdo, qrow, g0, g1}};
-        for (const auto& x : cp) {
+        for (int i = 0; i < 4; ++i) {
+            const auto& x = cp[i];
             const size_t bytes = (x.b - x.a) * x.row;
-            if (bytes == 0) continue;
-            e = cudaMemcpyAsync(buf + x.off + x.a * x.row, x.src + x.a * x.row, bytes,
-                                cudaMemcpyHostToDevice, r->in);
-            if (e != cudaSuccess) fail(e);
+            if (bytes > 0) {
+                e = cudaMemcpyAsync(buf + x.off + x.a * x.row, x.src + x.a * x.row, bytes,
+                                    cudaMemcpyHostToDevice, r->in);
+                if (e != cudaSuccess) fail(e);
+            }
+            // the forward needs Q, K, V only; dO (last) is for the backward
+            if (i == 2 && (e = cudaEventRecord(r->in_fwd[c], r->in)) != cudaSuccess) fail(e);
         }
         if ((e = cudaEventRecord(r->in_done[c], r->in)) != cudaSuccess) fail(e);
     }
@@ -656,7 +663,7 @@ fa_status fa_forward_backward_host(const void* q, const void* k, const void* v, 
         const int h0 = kv0_of(c), h1 = kv0_of(c + 1);
         const int nkv = h1 - h0, nq = nkv * p.group;
         cudaStream_t cs = r->comp[c & 1];
-        if ((e = cudaStreamWaitEvent(cs, r->in_done[c], 0)) != cudaSuccess) {
+        if ((e = cudaStreamWaitEvent(cs, r->in_fwd[c], 0)) != cudaSuccess) {
             fail(e);
             break;
         }
@@ -670,6 +677,7 @@ fa_status fa_forward_backward_host(const void* q, const void* k, const void* v, 
                                       reinterpret_cast<float*>(buf + p.off_lse + g0 * lrow), 1, nq,
                                       nkv, Tq, Tk, d, causal, window, scale, csx);
         if (st2 == FA_OK && (e = cudaEventRecord(r->fwd_done[c], cs)) != cudaSuccess) fail(e);
+        if (st2 == FA_OK && (e = cudaStreamWaitEvent(cs, r->in_done[c], 0)) != cudaSuccess) fail(e);
         if (st2 == FA_OK && result == FA_OK)
             st2 = fa_backward_ex(buf + p.off_q + g0 * qrow, buf + p.off_k + h0 * krow,
                                  buf + p.off_v + h0 * krow, buf + p.off_o + g0 * qrow,
