@@ -33,6 +33,11 @@
 //               fp32 partial O and LSE).
 // TMEM (512 columns): d=64: S_0, S_1 [0,256), O_0, O_1 [256,384), P_0, P_1 [384,512);
 // d=128: S_0, S_1 [0,256), O_0, O_1 [256,512), P written over S.
+// Kernel variants (template arguments): CAUSAL, WINDOW, SPLIT as above; SORTED, the causal
+// unit order (heaviest first, snake-dealt, over L2-sized chunks of heads; else a head's blocks
+// in heavy/light pairs); PACKED, a KV head's query heads packed into one block of rows (short
+// query blocks with grouped heads). Non-causal launches whose last round would be at most half
+// full run it as single-tile half units.
 #include <algorithm>
 
 #include <cuda_bf16.h>
