@@ -143,3 +143,20 @@ def test_causal_unit_order_in_several_head_chunks(env):
     assert_close_grad(dq[:, :, rq], ref_q, "dQ", "head chunks")
     assert_close_grad(dk[:, :, rk], ref_k, "dK", "head chunks")
     assert_close_grad(dv[:, :, rk], ref_v, "dV", "head chunks")
+
+
+def test_long_sequence_sampled(env):
+    """N = 32768 (causal, d=64, one head): 256 key-tile units of up to 256 query steps each;
+    dQ on seeded query rows, dK/dV on seeded key rows against the oracle."""
+    from exact_io_aware_fa_gb300 import synthetic
+    api, orc = env
+    B, H, N, d = 1, 1, 32768, 64
+    bits = synthetic.attention_inputs(B, H, N, d, seed=4098, with_dout=True)
+    dq, dk, dv = run_fwd_bwd(api, bits, True, default_scale(d))
+    rq = synthetic.sample_rows(N, 16, 4098)
+    rk = synthetic.sample_rows(N, 16, 5098)
+    ref_q, ref_k, ref_v = orc.backward_rows_bf16(bits["q"], bits["k"], bits["v"], bits["do"], True,
+                                                 default_scale(d), rq, rk)
+    assert_close_grad(dq[:, :, rq], ref_q, "dQ", "N=32768")
+    assert_close_grad(dk[:, :, rk], ref_k, "dK", "N=32768")
+    assert_close_grad(dv[:, :, rk], ref_v, "dV", "N=32768")

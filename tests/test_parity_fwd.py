@@ -193,3 +193,9 @@ def test_sorted_causal_order_in_several_head_chunks(env):
     of heads whose K/V fits in 128 MB of L2. B1 H36 N16384 d128 reads 8 MB of K/V per head:
     chunks of 16, 16 and 4 heads (the last one ragged); 2304 units, under 16 per SM on 152."""
     _sampled(env, 1, 36, 16384, 128, True, 4041, 1.0)
+
+
+def test_long_sequence_sampled(env):
+    """N = 131072 keys and queries (causal, d=64): 1024 key tiles per row block, positions and
+    row offsets well past 2^16; 32 seeded rows plus the tile-boundary rows against the oracle."""
+    _sampled(env, 1, 1, 131072, 64, True, 4099, 1.0)
