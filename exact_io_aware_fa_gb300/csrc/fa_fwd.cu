@@ -382,11 +382,12 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         }
     } else if (warp == 1 || warp == 3) {
         // ================================ MMA issuers =================================
-        // Two issuing warps: warp 1 issues the S MMAs, warp 3 the PV MMAs. A thread that
-        // issues MMAs stalls until the tensor pipe has (almost) drained them, so with one
-        // issuer every barrier wait left the pipe empty; with two, one warp's MMAs run while
-        // the other waits for its next operands. The whole warp runs the loop and one elected
-        // lane issues, which keeps descriptors and TMEM addresses in uniform registers.
+        // d = 64 (P in its own columns): two issuing warps, warp 1 for the S MMAs and warp 3
+        // for the PV MMAs. A thread that issues MMAs stalls until the tensor pipe has (almost)
+        // drained them, so with one issuer every barrier wait left the pipe empty; with two,
+        // one warp's MMAs run while the other waits for its next operands. d = 128 (P over S):
+        // one issuing warp, below. The whole warp runs the loop and one elected lane issues,
+        // which keeps descriptors and TMEM addresses in uniform registers.
         constexpr uint32_t idesc_s = ptx::idesc_bf16(128, C::BN, false, false);
         constexpr uint32_t idesc_o = ptx::idesc_bf16(128, D, false, true);
         const uint64_t dq0 = ptx::sdesc_sw128(s_q, 16, 1024);
@@ -402,6 +403,102 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         int ul = 0;
         int qn = 0;  // non-empty units (Q-buffer uses)
         bool ok = true;
+        if (!C::P_SEPARATE) {
+            // P over S (d = 128): warp 1 issues both products of a tile back to back,
+            // O_t += P_t(j-1) V_(j-1), then S_t(j) = Q_t K_j^T. The MMAs of one thread run in
+            // issue order, so S_t(j) overwrites P_t(j-1) only after the PV MMA has read it and
+            // needs no completion wait in between: the tensor pipe gets PV_0, S_0, PV_1, S_1,
+            // ... with no barrier round trip between a tile's PV and its next S. (A commit
+            // tracks every earlier MMA of the thread, so S_t(j) complete also means PV_t(j-1)
+            // complete.) Warp 3 issues nothing.
+            if (warp == 1) {
+                for (int u; ok && (u = fwd_unit_index<CAUSAL, SORTED>(blockIdx.x, ul, G, num_units)) >= 0; ++ul) {
+                    const FwdUnit w = fwd_unit<D, CAUSAL, WINDOW, SPLIT, SORTED, PACKED>(u, sh);
+                    if (w.empty()) continue;
+                    const int b = qn % C::NQB;
+                    const uint32_t qph = (uint32_t)(qn / C::NQB) & 1u;
+                    ++qn;
+                    ok = warp_wait(ptx::smem_addr(&bars->q_full[b]), qph, abort_flag, err,
+                                   kDevTimeoutLoad);
+                    // iteration j: the PVs of key tile j-1, then the S MMAs of key tile j
+                    for (int j = w.jb_all; ok && j <= w.je_all; ++j) {
+                        const bool has_k = j < w.je_all;
+                        const bool has_v = j > w.jb_all;
+                        const int xk = kv + (j - w.jb_all);  // ring position of key tile j
+                        const int sk = xk % C::NS, sv = (xk - 1 + C::NS) % C::NS;
+                        if (has_v) {
+                            ok = warp_wait(ptx::smem_addr(&bars->v_full[sv]),
+                                           (uint32_t)((xk - 1) / C::NS) & 1u, abort_flag, err,
+                                           kDevTimeoutLoad);
+                            if (!ok) break;
+                        }
+                        bool k_ready = false;
+                        for (int t = 0; ok && t < 2; ++t) {
+                            if (has_v && j - 1 >= w.jb(t) && j - 1 < w.je(t)) {
+                                if (j - 1 == w.jb(t) && uo[t] > 0) {
+                                    // O_t is about to be overwritten: the previous unit's
+                                    // epilogue must have read it.
+                                    ok = warp_wait(ptx::smem_addr(&bars->o_free[t]),
+                                                   (uint32_t)(uo[t] - 1) & 1u, abort_flag, err,
+                                                   kDevTimeoutSoftmax);
+                                    if (!ok) break;
+                                }
+                                ok = warp_wait(ptx::smem_addr(&bars->p_full[t]), (uint32_t)it[t] & 1u,
+                                               abort_flag, err, kDevTimeoutSoftmax);
+                                if (!ok) break;
+                                ptx::tc_fence_after();
+                                const uint32_t d_tmem = tbase + C::o_col(t);
+                                const uint32_t p_tmem = tbase + C::p_col(t);
+                                const uint64_t vd = ptx::sdesc_add(dv0, (uint32_t)sv * C::TILE_BYTES);
+                                if (ptx::elect_one()) {
+#pragma unroll
+                                    for (int kk = 0; kk < C::BN / 16; ++kk)
+                                        ptx::mma_ts(d_tmem, p_tmem + kk * 8, ptx::sdesc_add(vd, kk * 2048),
+                                                    idesc_o, (j - 1 > w.jb(t) || kk > 0) ? 1u : 0u);
+                                    ptx::mma_commit(ptx::smem_addr(&bars->o_done[t]));
+                                }
+                                __syncwarp();
+                                ++it[t];
+                            }
+                            if (has_k && j >= w.jb(t) && j < w.je(t)) {
+                                if (!k_ready) {
+                                    ok = warp_wait(ptx::smem_addr(&bars->k_full[sk]),
+                                                   (uint32_t)(xk / C::NS) & 1u, abort_flag, err,
+                                                   kDevTimeoutLoad);
+                                    if (!ok) break;
+                                    k_ready = true;
+                                }
+                                ptx::tc_fence_after();
+                                const uint32_t d_tmem = tbase + C::s_col(t);
+                                const uint64_t qd = ptx::sdesc_add(dq0, (uint32_t)(b * 2 + t) * C::TILE_BYTES);
+                                const uint64_t kd = ptx::sdesc_add(dk0, (uint32_t)sk * C::TILE_BYTES);
+                                if (ptx::elect_one()) {
+#pragma unroll
+                                    for (int kk = 0; kk < D / 16; ++kk) {
+                                        const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
+                                        ptx::mma_ss(d_tmem, ptx::sdesc_add(qd, off), ptx::sdesc_add(kd, off),
+                                                    idesc_s, kk > 0);
+                                    }
+                                    ptx::mma_commit(ptx::smem_addr(&bars->s_full[t]));
+                                }
+                                __syncwarp();
+                            }
+                        }
+                        if (!ok) break;
+                        if (has_k && !k_ready) {
+                            // (every key tile of the unit belongs to a Q tile; kept for the ring)
+                            ok = warp_wait(ptx::smem_addr(&bars->k_full[sk]), (uint32_t)(xk / C::NS) & 1u,
+                                           abort_flag, err, kDevTimeoutLoad);
+                            if (!ok) break;
+                        }
+                        if (has_v) commit(&bars->v_empty[sv]);
+                        if (has_k) commit(&bars->k_empty[sk]);
+                    }
+                    kv += w.je_all - w.jb_all;
+                    for (int t = 0; t < 2; ++t) uo[t] += (w.je(t) > w.jb(t));
+                }
+            }
+        } else
         for (int u; ok && (u = fwd_unit_index<CAUSAL, SORTED>(blockIdx.x, ul, G, num_units)) >= 0; ++ul) {
             const FwdUnit w = fwd_unit<D, CAUSAL, WINDOW, SPLIT, SORTED, PACKED>(u, sh);
             if (w.empty()) continue;
