@@ -22,8 +22,9 @@
 // them) so that the next unit's loads and first score MMAs overlap the current unit's
 // epilogue. Roles:
 //   warp 0      TMA producer: Q tiles once per unit, then K_j / V_j into separate mbarrier rings
-//   warp 1      MMA issuer for S_t = Q_t K_j^T (tcgen05.mma, fp32 in TMEM)
-//   warp 3      MMA issuer for O_t += P_t V_j (A = P from TMEM)
+//   warp 1      MMA issuer for S_t = Q_t K_j^T (tcgen05.mma, fp32 in TMEM); at d=128 also for
+//               O_t += P_t V_j, issued just before the tile's next S (P is written over S)
+//   warp 3      MMA issuer for O_t += P_t V_j at d=64 (A = P from TMEM)
 //   warp 2      TMEM allocation / release
 //   warps 4-7   softmax for Q tile 0, warps 8-11 softmax for Q tile 1: one thread per row,
 //               the whole row of S read from TMEM into registers (no cross-thread reduction),
