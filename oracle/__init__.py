@@ -64,13 +64,15 @@ def _lib(mutant: int = 0):
         lib.fa_oracle_backward_ex_f64.argtypes = [P, P, P, P, P, P, P, L, L, L, L, L, L, I, L, D, I]
         lib.fa_oracle_backward_ex_bf16.argtypes = [P, P, P, P, P, P, P, L, L, L, L, L, L, I, L, D,
                                                    I]
+        lib.fa_oracle_backward_ex_sens_bf16.argtypes = [P, P, P, P, P, P, P, P, P, P, L, L, L, L,
+                                                        L, L, I, L, D, I]
         lib.fa_oracle_mutant_id.argtypes = []
         for fn in ("fa_oracle_forward_bf16", "fa_oracle_forward_rows_bf16",
                    "fa_oracle_forward_f64", "fa_oracle_probs_f64", "fa_oracle_backward_bf16",
                    "fa_oracle_backward_f64", "fa_oracle_backward_rows_bf16",
                    "fa_oracle_forward_ex_f64", "fa_oracle_forward_ex_bf16",
                    "fa_oracle_backward_ex_f64", "fa_oracle_backward_ex_bf16",
-                   "fa_oracle_mutant_id"):
+                   "fa_oracle_backward_ex_sens_bf16", "fa_oracle_mutant_id"):
             getattr(lib, fn).restype = ctypes.c_int
         _LIBS[mutant] = lib
         return lib
@@ -230,8 +232,28 @@ def _ex_methods():
                   "backward_ex")
         return dq, dk, dv
 
+    def backward_ex_sens(self, q, k, v, dout, causal: bool, scale: float, window: int = -1):
+        """backward_ex on bf16 bits plus the gradients' sensitivities to relative errors in the
+        operands the products consume: (dq, dk, dv), (sq, sk, sv) with
+        sv_je = sum_i P_ij |dO_ie| (over the group's query rows), sk_je = scale sum_i |dS_ij|
+        |q_ie|, sq_ie = scale sum_j |dS_ij| |k_je|. If every P_ij (dS_ij) entering dV (dK, dQ)
+        carries a relative error of at most u, each gradient element moves by at most u times
+        its sensitivity (the triangle inequality on the sums that define it)."""
+        B, Hq, Hkv, Tq, Tk, d = _ex_shapes(q, k)
+        q, k, v, dout = (np.ascontiguousarray(x, dtype=np.uint16) for x in (q, k, v, dout))
+        dq = np.empty((B, Hq, Tq, d), dtype=np.float64)
+        dk = np.empty((B, Hkv, Tk, d), dtype=np.float64)
+        dv = np.empty((B, Hkv, Tk, d), dtype=np.float64)
+        sq, sk, sv = np.empty_like(dq), np.empty_like(dk), np.empty_like(dv)
+        _check_ex(self.lib.fa_oracle_backward_ex_sens_bf16(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(sq), _ptr(sk),
+            _ptr(sv), B, Hq, Hkv, Tq, Tk, d, int(causal), int(window), float(scale), self.threads),
+            "backward_ex_sens")
+        return (dq, dk, dv), (sq, sk, sv)
+
     Oracle.forward_ex = forward_ex
     Oracle.backward_ex = backward_ex
+    Oracle.backward_ex_sens = backward_ex_sens
 
 
 _ex_methods()

@@ -197,6 +197,9 @@ struct job {
     int in_bf16;
     const void *q, *k, *v, *dout;
     double *o, *lse, *dq, *dk, *dv;
+    /* optional (grouped backward): first-order sensitivities of each gradient element to a
+       relative perturbation of every P (dV) or dS (dQ, dK) entry it sums; NULL = not wanted */
+    double *sq, *sk, *sv;
     const long *rows_q, *rows_k;
     long nrows_q, nrows_k;
     /* extension: grouped KV heads, query offset, sliding window */
@@ -607,6 +610,8 @@ static void bwd_ex_slice(const job* jb, long bkv, double* scratch) {
     double* dk = jb->dk + bkv * Tk * d;
     double* dv = jb->dv + bkv * Tk * d;
     for (long x = 0; x < Tk * d; ++x) dk[x] = dv[x] = 0.0;
+    if (jb->sv)
+        for (long x = 0; x < Tk * d; ++x) jb->sk[bkv * Tk * d + x] = jb->sv[bkv * Tk * d + x] = 0.0;
     for (long g = 0; g < group; ++g) {
         long bhq = b * jb->Hq + hk * group + g;
         const double* q = slice_input(jb, jb->q, bhq, Tq, bufq);
@@ -645,11 +650,38 @@ static void bwd_ex_slice(const job* jb, long bkv, double* scratch) {
                 for (long j = 0; j < Tk; ++j) a += dS[i * Tk + j] * k[j * d + e];
                 dq[i * d + e] = jb->scale * a;
             }
+        if (jb->sv) {
+            /* Sensitivities: if every P_ij (resp. dS_ij) is perturbed by a relative amount of
+               at most u, dV_je moves by at most u * sv_je, dK_je by u * sk_je and dQ_ie by
+               u * sq_ie, where sv_je = sum_i P_ij |dO_ie|, sk_je = scale sum_i |dS_ij| |q_ie|,
+               sq_ie = scale sum_j |dS_ij| |k_je| (the triangle inequality on the sums above).
+               Summed over the query heads of the group like dK and dV. */
+            double* sv = jb->sv + bkv * Tk * d;
+            double* sk = jb->sk + bkv * Tk * d;
+            double* sq = jb->sq + bhq * Tq * d;
+            for (long j = 0; j < Tk; ++j)
+                for (long e = 0; e < d; ++e) {
+                    double a = 0.0, c = 0.0;
+                    for (long i = 0; i < Tq; ++i) {
+                        a += P[i * Tk + j] * fabs(dout[i * d + e]);
+                        c += fabs(dS[i * Tk + j]) * fabs(q[i * d + e]);
+                    }
+                    sv[j * d + e] += a;
+                    sk[j * d + e] += jb->scale * c;
+                }
+            for (long i = 0; i < Tq; ++i)
+                for (long e = 0; e < d; ++e) {
+                    double a = 0.0;
+                    for (long j = 0; j < Tk; ++j) a += fabs(dS[i * Tk + j]) * fabs(k[j * d + e]);
+                    sq[i * d + e] = jb->scale * a;
+                }
+        }
     }
 }
 
 static int ex_common(int in_bf16, int backward, const void* q, const void* k, const void* v,
                      const void* dout, double* o, double* lse, double* dq, double* dk, double* dv,
+                     double* sq, double* sk, double* sv,
                      long B, long Hq, long Hkv, long Tq, long Tk, long d, int causal, long window,
                      double scale, int nthreads) {
     if (B < 0 || Hq < 0 || Hkv < 1 || Tq < 0 || Tk < 0 || d < 1) return -2;
@@ -673,6 +705,9 @@ static int ex_common(int in_bf16, int backward, const void* q, const void* k, co
     jb.dq = dq;
     jb.dk = dk;
     jb.dv = dv;
+    jb.sq = sq;
+    jb.sk = sk;
+    jb.sv = sv;
     jb.Hq = Hq;
     jb.Hkv = Hkv;
     jb.Tq = Tq;
@@ -691,14 +726,14 @@ static int ex_common(int in_bf16, int backward, const void* q, const void* k, co
 int fa_oracle_forward_ex_f64(const double* q, const double* k, const double* v, double* o,
                              double* lse, long B, long Hq, long Hkv, long Tq, long Tk, long d,
                              int causal, long window, double scale, int nthreads) {
-    return ex_common(0, 0, q, k, v, NULL, o, lse, NULL, NULL, NULL, B, Hq, Hkv, Tq, Tk, d, causal,
+    return ex_common(0, 0, q, k, v, NULL, o, lse, NULL, NULL, NULL, NULL, NULL, NULL, B, Hq, Hkv, Tq, Tk, d, causal,
                      window, scale, nthreads);
 }
 
 int fa_oracle_forward_ex_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v, double* o,
                               double* lse, long B, long Hq, long Hkv, long Tq, long Tk, long d,
                               int causal, long window, double scale, int nthreads) {
-    return ex_common(1, 0, q, k, v, NULL, o, lse, NULL, NULL, NULL, B, Hq, Hkv, Tq, Tk, d, causal,
+    return ex_common(1, 0, q, k, v, NULL, o, lse, NULL, NULL, NULL, NULL, NULL, NULL, B, Hq, Hkv, Tq, Tk, d, causal,
                      window, scale, nthreads);
 }
 
@@ -706,7 +741,7 @@ int fa_oracle_forward_ex_bf16(const uint16_t* q, const uint16_t* k, const uint16
 int fa_oracle_backward_ex_f64(const double* q, const double* k, const double* v, const double* dout,
                               double* dq, double* dk, double* dv, long B, long Hq, long Hkv, long Tq,
                               long Tk, long d, int causal, long window, double scale, int nthreads) {
-    return ex_common(0, 1, q, k, v, dout, NULL, NULL, dq, dk, dv, B, Hq, Hkv, Tq, Tk, d, causal,
+    return ex_common(0, 1, q, k, v, dout, NULL, NULL, dq, dk, dv, NULL, NULL, NULL, B, Hq, Hkv, Tq, Tk, d, causal,
                      window, scale, nthreads);
 }
 
@@ -714,8 +749,20 @@ int fa_oracle_backward_ex_bf16(const uint16_t* q, const uint16_t* k, const uint1
                                const uint16_t* dout, double* dq, double* dk, double* dv, long B,
                                long Hq, long Hkv, long Tq, long Tk, long d, int causal, long window,
                                double scale, int nthreads) {
-    return ex_common(1, 1, q, k, v, dout, NULL, NULL, dq, dk, dv, B, Hq, Hkv, Tq, Tk, d, causal,
+    return ex_common(1, 1, q, k, v, dout, NULL, NULL, dq, dk, dv, NULL, NULL, NULL, B, Hq, Hkv, Tq, Tk, d, causal,
                      window, scale, nthreads);
+}
+
+/* backward_ex_bf16 plus the sensitivities sq [B,Hq,Tq,d], sk, sv [B,Hkv,Tk,d] (see
+ * bwd_ex_slice): the bound on how far each gradient element can move when every P_ij (dV) or
+ * dS_ij (dQ, dK) it sums carries a relative error of at most u is u times its sensitivity. */
+int fa_oracle_backward_ex_sens_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                    const uint16_t* dout, double* dq, double* dk, double* dv,
+                                    double* sq, double* sk, double* sv, long B, long Hq, long Hkv,
+                                    long Tq, long Tk, long d, int causal, long window, double scale,
+                                    int nthreads) {
+    return ex_common(1, 1, q, k, v, dout, NULL, NULL, dq, dk, dv, sq, sk, sv, B, Hq, Hkv, Tq, Tk,
+                     d, causal, window, scale, nthreads);
 }
 
 int fa_oracle_mutant_id(void) { return ORACLE_MUTANT; }

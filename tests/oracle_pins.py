@@ -499,6 +499,54 @@ def check_ex_backward_finite_differences(orc):
             assert err <= 1e-6, (name, window, err)
 
 
+def check_ex_backward_sensitivities(orc):
+    """The gradient sensitivities (the parity tests' bound for bf16 rounding of P and dS)
+    against a brute-force numpy restatement of the definitions on a tiny GQA + offset + window
+    case, the closed form sum_j sv_je = sum_i |dO_ie| (rows of P sum to 1), and the gradients
+    returned beside them equal backward_ex's."""
+    r = _rng(35)
+    B, Hkv, group, Tq, Tk, d = 2, 2, 3, 5, 9, 4
+    Hq = Hkv * group
+    bits = {}
+    vals = {}
+    for name, shape in (("q", (B, Hq, Tq, d)), ("k", (B, Hkv, Tk, d)), ("v", (B, Hkv, Tk, d)),
+                        ("do", (B, Hq, Tq, d))):
+        x = np.round(r.standard_normal(shape) * 8) / 8  # exact in bf16
+        vals[name], bits[name] = x, _to_bf16_bits(x)
+    scale = 0.6
+    for causal, window in ((False, -1), (True, -1), (True, 3)):
+        (dq, dk, dv), (sq, sk, sv) = orc.backward_ex_sens(bits["q"], bits["k"], bits["v"],
+                                                          bits["do"], causal, scale, window)
+        ref = orc.backward_ex(bits["q"], bits["k"], bits["v"], bits["do"], causal, scale, window)
+        for a, b in zip((dq, dk, dv), ref):
+            assert np.array_equal(a, b), (causal, window)
+        bq, bk, bv = np.zeros_like(sq), np.zeros_like(sk), np.zeros_like(sv)
+        for b_ in range(B):
+            for h in range(Hq):
+                hk = h // group
+                qh, kh, vh, doh = (vals["q"][b_, h], vals["k"][b_, hk], vals["v"][b_, hk],
+                                   vals["do"][b_, h])
+                pos = np.arange(Tq)[:, None] + (Tk - Tq)
+                j = np.arange(Tk)[None, :]
+                vis = np.ones((Tq, Tk), dtype=bool)
+                if causal:
+                    vis &= j <= pos
+                if window >= 0:
+                    vis &= j >= pos - window
+                s = np.where(vis, scale * qh @ kh.T, -np.inf)
+                P = np.exp(s - s.max(axis=1, keepdims=True))
+                P /= P.sum(axis=1, keepdims=True)
+                dP = doh @ vh.T
+                dS = P * (dP - (P * dP).sum(axis=1, keepdims=True))
+                bv[b_, hk] += P.T @ np.abs(doh)
+                bk[b_, hk] += scale * np.abs(dS).T @ np.abs(qh)
+                bq[b_, h] = scale * np.abs(dS) @ np.abs(kh)
+        for name, a, b in (("sq", sq, bq), ("sk", sk, bk), ("sv", sv, bv)):
+            assert np.allclose(a, b, rtol=1e-12, atol=1e-12), (name, causal, window)
+        col = np.abs(vals["do"]).reshape(B, Hkv, group * Tq, d).sum(axis=2)
+        assert np.allclose(sv.sum(axis=2), col, rtol=1e-12, atol=1e-12), (causal, window)
+
+
 def check_split_merge_equals_unsplit(orc):
     """Flash-decoding: partials over any chunking of the keys (including empty chunks and
     chunks some rows cannot see) merge to the unsplit attention ("15. FlashAttention",
@@ -559,6 +607,7 @@ ALL_CHECKS = [
     check_ex_query_offset_bottom_right,
     check_ex_sliding_window,
     check_ex_backward_finite_differences,
+    check_ex_backward_sensitivities,
     check_split_merge_equals_unsplit,
     check_merge_is_associative,
 ]

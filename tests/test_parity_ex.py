@@ -43,6 +43,9 @@ CASES = [
     (1, 16, 1, 64, 256, 64, True, -1),      # MQA, 1024 packed rows, causal boundary tile
     (1, 4, 2, 64, 300, 64, False, -1),      # packed exactly one tile per KV head
     (1, 4, 2, 65, 300, 64, True, -1),       # Tq = 65: not packed
+    # MQA with short causal blocks: every key row sums 16 heads' rows, |dV| reaches ~14
+    (1, 16, 1, 64, 64, 64, True, -1),       # packed forward, 1024 rows
+    (1, 16, 1, 65, 65, 64, True, -1),       # unpacked
 ]
 
 
@@ -88,9 +91,10 @@ def test_backward_ex(env, case):
     dq, dk, dv = api.backward(q, k, v, o, lse, do, causal=causal, scale=scale, window=window)
     torch.cuda.synchronize()
     assert api.device_error() == 0
-    ref = orc.backward_ex(bits["q"], bits["k"], bits["v"], bits["do"], causal, scale, window)
-    for name, a, b in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
-        assert_close_grad(to_f64(a), b, name, ids(case))
+    ref, sens = orc.backward_ex_sens(bits["q"], bits["k"], bits["v"], bits["do"], causal, scale,
+                                     window)
+    for name, a, b, s in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref, sens):
+        assert_close_grad(to_f64(a), b, name, ids(case), sens=s)
 
 
 def test_mha_call_matches_ex_call(env):
