@@ -97,6 +97,15 @@ def test_config2_backward_full(env):
     check_full(api, orc, bits, False, default_scale(64), "config 2 backward")
 
 
+def test_config2_causal_backward_full(env):
+    """B=4 H=16 N=2048 d=64 under the causal mask, in full: every fold record and dQ accumulator
+    row of 64 heads, with units of very unequal cost on the persistent grid."""
+    from exact_io_aware_fa_gb300 import synthetic
+    api, orc = env
+    bits = synthetic.attention_inputs(4, 16, 2048, 64, seed=1012, with_dout=True)
+    check_full(api, orc, bits, True, default_scale(64), "config 2 causal backward")
+
+
 def test_config5_sampled(env):
     """B=4 H=16 N=4096 d=128, causal; dQ on seeded query rows, dK/dV on seeded key rows."""
     from exact_io_aware_fa_gb300 import synthetic
