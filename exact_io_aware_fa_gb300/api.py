@@ -26,12 +26,11 @@ FA_ERR_TIMEOUT = 5
 EXPORTS = ("fa_forward", "fa_forward_ex", "fa_forward_splitkv_workspace_bytes",
            "fa_forward_splitkv", "fa_forward_choose_splits", "fa_backward_workspace_bytes",
            "fa_backward",
-           "fa_backward_ex", "fa_backward_noalloc", "fa_forward_backward_host_device_bytes",
+           "fa_backward_ex", "fa_backward_noalloc", "fa_noalloc_scratch_bytes",
+           "fa_forward_backward_host_device_bytes",
            "fa_forward_backward_host", "fa_selftest_wait_timeout", "fa_status_string",
            "fa_last_cuda_error", "fa_device_error")
 
-# Size of the library's own backward workspace (FA_NOALLOC_SCRATCH_BYTES in include/fa.h).
-NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 
 class FaLibraryMissing(RuntimeError):
@@ -81,6 +80,8 @@ def library(path: str | None = None):
         lib.fa_backward_ex.restype = I
         lib.fa_backward_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, P]
         lib.fa_backward_noalloc.restype = I
+        lib.fa_noalloc_scratch_bytes.argtypes = []
+        lib.fa_noalloc_scratch_bytes.restype = Z
         lib.fa_forward_backward_host_device_bytes.argtypes = [I, I, I, I, I, I, I]
         lib.fa_forward_backward_host_device_bytes.restype = Z
         lib.fa_forward_backward_host.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I,
@@ -152,6 +153,12 @@ def backward_noalloc_raw(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, causal, 
     callers that may not allocate device memory at call time (see include/fa.h)."""
     return library().fa_backward_noalloc(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, causal,
                                          scale, stream)
+
+
+def noalloc_scratch_bytes() -> int:
+    """Size of the library's own backward workspace (FA_NOALLOC_SCRATCH_BYTES), read from
+    libfa.so so that callers never carry a second copy of the constant."""
+    return int(library().fa_noalloc_scratch_bytes())
 
 
 def backward_workspace_bytes(B: int, H: int, N: int, d: int) -> int:

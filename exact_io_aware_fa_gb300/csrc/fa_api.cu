@@ -566,6 +566,8 @@ fa_status fa_backward_noalloc(const void* q, const void* k, const void* v, const
                        stream);
 }
 
+size_t fa_noalloc_scratch_bytes(void) { return (size_t)FA_NOALLOC_SCRATCH_BYTES; }
+
 fa_status fa_selftest_wait_timeout(unsigned int limit_us, struct CUstream_st* stream) {
     if (limit_us == 0 || limit_us > 1000000u) return FA_ERR_INVALID_ARG;
     int* err = nullptr;

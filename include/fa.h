@@ -196,6 +196,10 @@ fa_status fa_backward_noalloc(const void* q, const void* k, const void* v, const
                               int B, int H, int N, int d, int causal, float scale,
                               struct CUstream_st* stream);
 
+/* FA_NOALLOC_SCRATCH_BYTES as compiled into this libfa.so: the size of the workspace array
+ * fa_backward_noalloc uses (a binding can read it instead of repeating the macro). */
+size_t fa_noalloc_scratch_bytes(void);
+
 /*
  * One forward + backward step on host-resident tensors (no counterpart in the pages: an
  * integration convenience for callers whose activations live in host memory). Copies Q, K, V
