@@ -31,6 +31,17 @@ sys.path.insert(0, ROOT)
 
 WORKLOAD = dict(name="B4 H16 N2048 d64 non-causal fwd+bwd", B=4, H=16, N=2048, d=64,
                 causal=False, seed=1002)
+# The five attention configurations the forward/backward targets are stated on, timed one by
+# one after the main step (CUDA-event median of --config-reps repetitions, L2 flushed between
+# repetitions). Q, K ~ N(0, qk_sigma^2), V, dO ~ N(0, 1), scale 1/sqrt(d).
+CONFIGS = [
+    dict(name="1: B1 H1 N256 d64 non-causal", B=1, H=1, N=256, d=64, causal=False, qk_sigma=1.0, seed=1001),
+    dict(name="2: B4 H16 N2048 d64 non-causal", B=4, H=16, N=2048, d=64, causal=False, qk_sigma=1.0, seed=1002),
+    dict(name="3: B8 H32 N8192 d128 causal", B=8, H=32, N=8192, d=128, causal=True, qk_sigma=1.0, seed=1003),
+    dict(name="4: B1 H64 N16384 d128 causal, QK sd 3", B=1, H=64, N=16384, d=128, causal=True, qk_sigma=3.0, seed=1004),
+    dict(name="4r: B1 H64 N16000 d128 causal, QK sd 3", B=1, H=64, N=16000, d=128, causal=True, qk_sigma=3.0, seed=1004),
+    dict(name="5: B4 H16 N4096 d128 causal", B=4, H=16, N=4096, d=128, causal=True, qk_sigma=1.0, seed=1005),
+]
 FWD_KERNEL_SRC = os.path.join(ROOT, "exact_io_aware_fa_gb300", "csrc", "fa_fwd.cu")
 BWD_KERNEL_SRC = os.path.join(ROOT, "exact_io_aware_fa_gb300", "csrc", "fa_bwd.cu")
 TRAFFIC_JSON = os.path.join(ROOT, "profiles", "traffic.json")
@@ -68,6 +79,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-configuration block")
+    ap.add_argument("--config-reps", type=int, default=20)
     return ap.parse_args()
 
 
@@ -181,6 +194,61 @@ def oracle_sample_time(heads, want_seconds=None):
     return dt, fl, cores
 
 
+def _sample_rows(N, seed, n=32):
+    """The parity tests' row sample: n seeded rows plus the tile-boundary rows."""
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    fixed = [0, 127, 128, 255, N - 129, N - 1]
+    rows = set(int(x) for x in rng.integers(0, N, size=n)) | {r for r in fixed if 0 <= r < N}
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+def oracle_config_extrapolation(cfg, heads=4, fwd_rows=128, backward=False):
+    """Time the fp64 oracle on a sample of one large configuration and extrapolate the full
+    oracle's time from the sample's FLOP rate (labelled as such). Forward: `fwd_rows` seeded
+    query rows on each of `heads` heads. Backward (optional): the parity tests' row sample as
+    query and key rows, which rebuilds every row's LSE and D."""
+    import numpy as np
+    import oracle
+    from exact_io_aware_fa_gb300 import synthetic
+    N, d, causal = cfg["N"], cfg["d"], cfg["causal"]
+    bits = synthetic.attention_inputs(1, heads, N, d, seed=cfg["seed"], qk_sigma=cfg["qk_sigma"],
+                                      with_dout=backward)
+    threads = min(heads, oracle.default_threads())
+    orc = oracle.Oracle(0, threads=threads)
+    scale = 1.0 / math.sqrt(d)
+
+    def vis(i):  # keys row i sees
+        return (i + 1) if causal else N
+
+    rows = np.sort(np.random.default_rng(cfg["seed"]).choice(N, size=min(fwd_rows, N),
+                                                              replace=False)).astype(np.int64)
+    t0 = time.perf_counter()
+    orc.forward_rows_bf16(bits["q"], bits["k"], bits["v"], causal, scale, rows)
+    t_fwd = time.perf_counter() - t0
+    f_fwd = heads * sum(4.0 * vis(int(i)) * d for i in rows)
+    full_f = fwd_flops(cfg["B"], cfg["H"], N, d, causal)
+    out = {"sample": f"{heads} heads x {len(rows)} seeded query rows (forward)",
+           "cores": threads, "fwd_sample_s": t_fwd, "fwd_tflops": f_fwd / t_fwd / 1e12,
+           "fwd_full_s_extrapolated": full_f / (f_fwd / t_fwd),
+           "label": "extrapolated: full-configuration FLOPs / the sample's FLOP rate"}
+    if backward:
+        rb = _sample_rows(N, cfg["seed"])
+        t0 = time.perf_counter()
+        orc.backward_rows_bf16(bits["q"], bits["k"], bits["v"], bits["do"], causal, scale, rb, rb)
+        t_bwd = time.perf_counter() - t0
+        # every row's LSE and D (score and dP rows), then per sampled query row its P, dS and
+        # dQ rows, per sampled key row its P and dS columns, dK and dV
+        all_vis = (N * (N + 1) / 2.0) if causal else float(N) * N
+        f_bwd = heads * (4.0 * all_vis * d + sum(6.0 * vis(int(i)) * d for i in rb) +
+                         sum(8.0 * ((N - int(j)) if causal else N) * d for j in rb))
+        out["sample"] += f"; {len(rb)} query and key rows per head (backward)"
+        out.update(bwd_sample_s=t_bwd, bwd_tflops=f_bwd / t_bwd / 1e12,
+                   bwd_full_s_extrapolated=bwd_flops(cfg["B"], cfg["H"], N, d, causal) /
+                   (f_bwd / t_bwd))
+    return out
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
@@ -211,6 +279,100 @@ def run_reference(args, rank, world):
 
 
 # ---- GPU arm -------------------------------------------------------------------------------------
+
+def _traffic_record(kernel, workload):
+    """A traffic.json record of `kernel` on `workload` whose kernel source is unchanged since
+    the counters were taken, else None."""
+    if not os.path.exists(TRAFFIC_JSON):
+        return None
+    with open(TRAFFIC_JSON) as f:
+        tj = json.load(f)
+    src = BWD_KERNEL_SRC if kernel == "fa_bwd" else FWD_KERNEL_SRC
+    for ent in tj.get("records", []):
+        if (ent.get("kernel") == kernel and ent.get("workload") == workload and
+                ent.get("source_sha") == file_sha(src)):
+            return ent
+    return None
+
+
+def time_configs(api, dev, reps, peaks):
+    """Median fwd / bwd times of every configuration (CUDA events on the launching stream, L2
+    flushed before each repetition, outside the events). Inputs: seeded device normals of each
+    configuration's distribution, rounded to bf16."""
+    import torch
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    s = stream.cuda_stream
+    peak = peaks["bf16_tflops"]
+    out = []
+    for cfg in CONFIGS:
+        B, H, N, d, causal = cfg["B"], cfg["H"], cfg["N"], cfg["d"], cfg["causal"]
+        g = torch.Generator(device=dev)
+        g.manual_seed(cfg["seed"])
+
+        def normal(sigma):
+            return (torch.randn((B, H, N, d), generator=g, device=dev) * sigma).to(torch.bfloat16)
+
+        q, k = normal(cfg["qk_sigma"]), normal(cfg["qk_sigma"])
+        v, do = normal(1.0), normal(1.0)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+        ws = torch.empty(api.backward_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
+        scale = 1.0 / math.sqrt(d)
+        ci = int(causal)
+
+        def fwd():
+            st = api.forward_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                 lse.data_ptr(), B, H, N, d, ci, scale, s)
+            assert st == 0, api.status_string(st)
+
+        def bwd():
+            st = api.backward_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                  lse.data_ptr(), do.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                  dv.data_ptr(), B, H, N, d, ci, scale, ws.data_ptr(), s)
+            assert st == 0, api.status_string(st)
+
+        def run(reps_, flushed):
+            for _ in range(3):
+                fwd()
+                bwd()
+            ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps_)]
+            for e in ev:
+                if flushed:
+                    flush.zero_()
+                e[0].record(stream)
+                fwd()
+                e[1].record(stream)
+                bwd()
+                e[2].record(stream)
+            torch.cuda.synchronize()
+            return (statistics.median(e[0].elapsed_time(e[1]) for e in ev),
+                    statistics.median(e[1].elapsed_time(e[2]) for e in ev))
+
+        fms, bms = run(reps, True)
+        assert api.device_error() == 0
+        ff, bf = fwd_flops(B, H, N, d, causal), bwd_flops(B, H, N, d, causal)
+        ent = {"config": cfg["name"],
+               "fwd": {"ms": fms, "tflops": ff / fms / 1e9, "frac_of_peak": ff / fms / 1e9 / peak},
+               "bwd": {"ms": bms, "tflops": bf / bms / 1e9, "frac_of_peak": bf / bms / 1e9 / peak},
+               "timing": f"median of {reps}, L2 flushed"}
+        for kern, key, ms, fl in (("fa_fwd", "fwd", fms, ff), ("fa_bwd", "bwd", bms, bf)):
+            rec = _traffic_record(kern, cfg["name"])
+            if rec is not None:
+                ent[key]["traffic"] = rec["bytes_per_launch"]
+                ent[key]["hbm_gbs"] = rec["bytes_per_launch"] / (ms * 1e-3) / 1e9
+                ent[key]["hbm_frac"] = ent[key]["hbm_gbs"] / peaks["hbm_gbs"]
+        if cfg["seed"] == WORKLOAD["seed"]:
+            wf, wb = run(reps, False)
+            ent["warm_l2"] = {"fwd_ms": wf, "bwd_ms": wb, "fwd_tflops": ff / wf / 1e9,
+                              "bwd_tflops": bf / wb / 1e9,
+                              "timing": f"median of {reps}, L2 not flushed"}
+        out.append(ent)
+        del q, k, v, do, o, lse, dq, dk, dv, ws
+        torch.cuda.empty_cache()
+    return out
+
 
 def run_ours(args, rank, world, local):
     import numpy as np
@@ -290,21 +452,16 @@ def run_ours(args, rank, world, local):
     bf = bwd_flops(B, H, N, d, causal)
     value = fadist.weak_scaling_value(ff + bf, args.steps, world, total_ms * 1e-3)
     peaks = load_peaks()
-    fwd_avg = sum(fwd_ms) / len(fwd_ms)
-    bwd_avg = sum(bwd_ms) / len(bwd_ms)
-    fwd_tf = ff / (fwd_avg * 1e-3) / 1e12
-    bwd_tf = bf / (bwd_avg * 1e-3) / 1e12
-    dominant = "fa_bwd" if bwd_avg >= fwd_avg else "fa_fwd"
+    fwd_med = statistics.median(fwd_ms)
+    bwd_med = statistics.median(bwd_ms)
+    fwd_tf = ff / (fwd_med * 1e-3) / 1e12
+    bwd_tf = bf / (bwd_med * 1e-3) / 1e12
+    dominant = "fa_bwd" if bwd_med >= fwd_med else "fa_fwd"
     dom_tf = bwd_tf if dominant == "fa_bwd" else fwd_tf
+    dom_ms = bwd_med if dominant == "fa_bwd" else fwd_med
 
-    traffic = None
-    if os.path.exists(TRAFFIC_JSON):
-        with open(TRAFFIC_JSON) as f:
-            tj = json.load(f)
-        ent = tj.get(dominant)
-        src = BWD_KERNEL_SRC if dominant == "fa_bwd" else FWD_KERNEL_SRC
-        if ent and ent.get("source_sha") == file_sha(src) and ent.get("workload") == w["name"]:
-            traffic = ent.get("bytes_per_launch")
+    rec = _traffic_record(dominant, CONFIGS[1]["name"])
+    traffic = rec["bytes_per_launch"] if rec else None
 
     # ---- end to end through the public API with host buffers ----------------------------------
     e2e = None
@@ -343,12 +500,19 @@ def run_ours(args, rank, world, local):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_ms / args.steps}
 
+    configs = None
+    if not args.no_configs:
+        configs = time_configs(api, dev, args.config_reps, peaks)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         heads = 8
         dt, fl, cores = oracle_sample_time(heads)
         cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                "sample": f"{heads} of 64 heads of the workload, fwd+bwd, {dt:.1f} s"}
+        if not args.no_configs:
+            cpu["configs"] = {c["name"]: oracle_config_extrapolation(c, backward=c["name"][0] == "5")
+                              for c in CONFIGS if c["name"][:2] in ("3:", "4:", "5:")}
 
     if rank != 0:
         return
@@ -359,12 +523,16 @@ def run_ours(args, rank, world, local):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": dict(workload_config(world),
                        l2="flushed between timed steps (512 MiB write outside the events)"),
-        "fwd": {"ms": fwd_avg, "tflops": fwd_tf, "frac_of_peak": fwd_tf / peaks["bf16_tflops"]},
-        "bwd": {"ms": bwd_avg, "tflops": bwd_tf, "frac_of_peak": bwd_tf / peaks["bf16_tflops"]},
+        "fwd": {"ms": fwd_med, "tflops": fwd_tf, "frac_of_peak": fwd_tf / peaks["bf16_tflops"],
+                "timing": f"median of {args.steps} timed steps"},
+        "bwd": {"ms": bwd_med, "tflops": bwd_tf, "frac_of_peak": bwd_tf / peaks["bf16_tflops"],
+                "timing": f"median of {args.steps} timed steps"},
         "roofline": {"kernel": KERNEL_LABEL[dominant], "bound": "tensor", "achieved": dom_tf,
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": dom_tf / peaks["bf16_tflops"], "traffic": traffic,
+                     "hbm_gbs": (traffic / (dom_ms * 1e-3) / 1e9) if traffic else None,
                      "peak_source": f"{peaks['source']} bf16 burst"},
+        "configs": configs,
         "e2e": e2e,
         "gpu_launches": args.steps * 4,
         "clocks": clocks,
