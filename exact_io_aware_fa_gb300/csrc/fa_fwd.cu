@@ -81,11 +81,21 @@ struct FwdCfg {
     }
 };
 
-// The reference max moves as soon as the row max grows (threshold 0): the largest score of a
-// row then gets p = exp2(0) = 1 exactly, so a peaked row's dominant weight carries no bf16
-// rounding. (A stale reference, allowed to lag the max by a few units of log2, skips more
-// O rescales but measurably loosens O in peaked rows.)
-constexpr float kTau = 0.0f;
+// Reference max of the online softmax (log2 domain of the scaled scores).
+// d = 128: the reference moves as soon as the row max grows (threshold 0), so the largest score
+// of a row gets p = exp2(0) = 1 exactly and a peaked row's dominant weight carries no bf16
+// rounding; O is rescaled whenever some row of a warp raised its max.
+// d = 64: the reference moves only when the row max exceeds it by more than 8, so after the
+// first key tile of a unit O is almost never rescaled (p <= 2^8 stays far from fp32 overflow).
+// The largest weight p_M = exp2(c s_M - m_ref) is then not 1, and its bf16 rounding would carry
+// into O in peaked rows; the epilogue divides O by l + (bf16(p_M) - p_M), the sum with that
+// weight taken as the PV product used it, which cancels the dominant weight's error (to first
+// order the output error becomes w_M (1 - w_M) eps_M (v_M - v_rest), eps_M its relative rounding).
+template <int D>
+struct Tau {
+    static constexpr float value = (D == 64) ? 8.0f : 0.0f;
+    static constexpr bool lagging = (D == 64);
+};
 
 struct FwdBars {
     uint64_t q_full[2], q_free[2];
@@ -592,6 +602,16 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const uint32_t t_s = tbase + lane_off + C::s_col(t);
         const uint32_t t_p = tbase + lane_off + C::p_col(t);
         const uint32_t t_o = tbase + lane_off + C::o_col(t);
+        // Q buffer whose staged output is still being read by its TMA store (thread r == 0
+        // only; -1: none). The buffer is released to the producer once the read is done.
+        int rel_pending = -1;
+        auto release_staging = [&]() {
+            if (rel_pending >= 0) {
+                ptx::bulk_wait_read_all();
+                ptx::mbar_arrive(ptx::smem_addr(&bars->q_free[rel_pending]));
+                rel_pending = -1;
+            }
+        };
         const uint32_t b_s_full = ptx::smem_addr(&bars->s_full[t]);
         const uint32_t b_s_free = ptx::smem_addr(&bars->s_free[t]);
         const uint32_t b_p_full = ptx::smem_addr(&bars->p_full[t]);
@@ -635,13 +655,17 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->q_full[b]), qph,
                                                         abort_flag, err, kDevTimeoutLoad));
                 if (!ok) break;
-                if (r == 0) ptx::mbar_arrive(ptx::smem_addr(&bars->q_free[b]));
+                if (r == 0) {
+                    release_staging();
+                    ptx::mbar_arrive(ptx::smem_addr(&bars->q_free[b]));
+                }
                 continue;
             }
             // Online softmax: m_ref (scaled log2 domain) moves when the row max exceeds it by
-            // more than kTau; when it moves, both l and the accumulator are rescaled by
+            // more than the threshold (Tau); when it moves, both l and the accumulator are rescaled by
             // alpha = exp2(m_old - m_new). O is rescaled only when some row of the warp moved.
             float m_ref = -INFINITY;  // reference (scaled log2 domain)
+            float m_raw = -INFINITY;  // lagging reference: largest visible raw score of the row
             float l = 0.f;            // running sum of exp2(c*s - m_ref)
             if (!live) {
                 // rows all past Tq: only the barrier steps (see above)
@@ -679,6 +703,12 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     ptx::tmem_wait_ld(u1);
                     ptx::tmem_wait_ld(u2);
                     ptx::tmem_wait_ld(u3);
+                    if (C::P_SEPARATE) {
+                        // S_t is in registers: the next S_t may be computed into its columns
+                        // while this step's softmax runs.
+                        ptx::tc_fence_before();
+                        ptx::mbar_arrive(b_s_free);
+                    }
 #pragma unroll
                     for (int k = 0; k < 32; ++k) {
                         s[k] = __uint_as_float(u0[k]);
@@ -711,14 +741,25 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 }
                 a0 = ptx::fmax3(a0, s[C::BN - 4], s[C::BN - 3]);
                 a1 = ptx::fmax3(a1, s[C::BN - 2], s[C::BN - 1]);
-                const float mc = ptx::fmax3(a0, a1, fmaxf(a2, a3)) * c;
-                const bool upd = mc > m_ref + kTau;  // false when the tile is fully masked
+                const float mx = ptx::fmax3(a0, a1, fmaxf(a2, a3));
+                const float mc = mx * c;
+                const bool upd = mc > m_ref + Tau<D>::value;  // false when the tile is fully masked
+                if (Tau<D>::lagging) m_raw = fmaxf(m_raw, mx);
                 float alpha = 1.f;
                 if (upd) {
                     alpha = ptx::ex2_approx(m_ref - mc);  // 0 on the first visible tile
                     m_ref = mc;
                 }
                 const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;  // safe reference
+                if (Tau<D>::lagging && j > jb) {
+                    // P_t's columns are free and O_t stable once O_t += P_t(j-1) V is complete
+                    // (issued at the end of the previous step, so normally done by now): P is
+                    // then written to TMEM piece by piece while the exponentials are computed.
+                    ok = __all_sync(0xffffffffu, wait_phase(b_o_done, (uint32_t)(it - 1) & 1u,
+                                                            abort_flag, err, kDevTimeoutMma));
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+                }
                 // p = exp2(c*s - m_ref) (packed FMA, then ex2), row sum over eight partials.
                 float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f, r4 = 0.f, r5 = 0.f, r6 = 0.f, r7 = 0.f;
                 uint32_t pk[C::BN / 2];
@@ -736,16 +777,33 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     ptx::fadd2(r6, r7, r6, r7, s[k + 6], s[k + 7]);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) pk[k / 2 + i] = ptx::pack_bf16x2(s[k + 2 * i], s[k + 2 * i + 1]);
+                    if (Tau<D>::lagging && (k & 31) == 24) {
+                        // 32 keys done: their 16 packed columns of P go to TMEM now
+                        uint32_t chunk[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) chunk[i] = pk[k / 2 - 12 + i];
+                        ptx::tmem_st16(t_p + (k / 2 - 12), chunk);
+                    }
                 }
                 l = l * alpha + (((r0 + r1) + (r2 + r3)) + ((r4 + r5) + (r6 + r7)));
-                if (C::P_SEPARATE) {
-                    // S_t (in registers since the loads) may be overwritten now. Signalled after
-                    // the exp2 phase, not before the row max: the next S_t has ample slack, and
-                    // the fence and arrival off the max -> exp2 chain gave +2-4 % at d = 64.
-                    ptx::tc_fence_before();
-                    ptx::mbar_arrive(b_s_free);
-                }
-                if (j > jb) {
+                if (Tau<D>::lagging) {
+                    // rare: some row of the warp moved its reference, so O_t is rescaled
+                    if (j > jb && __any_sync(0xffffffffu, upd)) {
+#pragma unroll
+                        for (int cc = 0; cc < D / 32; ++cc) {
+                            uint32_t o[32];
+                            ptx::tmem_ld32(t_o + cc * 32, o);
+#pragma unroll
+                            for (int i = 0; i < 32; i += 2) {
+                                float x0, x1;
+                                ptx::fmul2(x0, x1, __uint_as_float(o[i]), __uint_as_float(o[i + 1]), alpha, alpha);
+                                o[i] = __float_as_uint(x0);
+                                o[i + 1] = __float_as_uint(x1);
+                            }
+                            ptx::tmem_st32(t_o + cc * 32, o);
+                        }
+                    }
+                } else if (j > jb) {
                     // O_t += P_t(j-1) V must be complete before P_t is overwritten (separate P
                     // columns) and before O_t is rescaled.
                     ok = __all_sync(0xffffffffu, wait_phase(b_o_done, (uint32_t)(it - 1) & 1u,
@@ -768,18 +826,28 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                         }
                     }
                 }
+                if (!Tau<D>::lagging) {
 #pragma unroll
-                for (int g = 0; g < C::BN / 32; ++g) {
-                    uint32_t chunk[16];
+                    for (int g = 0; g < C::BN / 32; ++g) {
+                        uint32_t chunk[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) chunk[i] = pk[16 * g + i];
-                    ptx::tmem_st16(t_p + 16 * g, chunk);
+                        for (int i = 0; i < 16; ++i) chunk[i] = pk[16 * g + i];
+                        ptx::tmem_st16(t_p + 16 * g, chunk);
+                    }
                 }
                 ptx::tmem_wait_st();
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(b_p_full);
+                if (j == jb) release_staging();
             }
             if (!ok) break;
+            // Lagging reference: normalise O by the sum of the weights as the PV product used
+            // them, l with the dominant weight p_M replaced by its bf16 value (see Tau).
+            float l_o = l;
+            if (Tau<D>::lagging && m_ref != -INFINITY) {
+                const float p_m = ptx::ex2_approx(fmaf(m_raw, c, -m_ref));
+                l_o = l + (__bfloat162float(__float2bfloat16_rn(p_m)) - p_m);
+            }
             // ---- epilogue: O = a / l as bf16 into this tile's part of the Q buffer, TMA store ----
             ok = __all_sync(0xffffffffu, wait_phase(b_o_done, (uint32_t)(it - 1) & 1u, abort_flag,
                                                     err, kDevTimeoutMma));
@@ -803,7 +871,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 // sees no key of the chunk gets LSE_s = -inf (the merge skips it).
                 if (live && row < sh.Tq) {
                     const bool any = l > 0.f;
-                    const float inv_l = any ? 1.f / l : 0.f;
+                    const float inv_l = any ? 1.f / l_o : 0.f;
                     float4* dst = reinterpret_cast<float4*>(part_o + prow * D);
 #pragma unroll
                     for (int e = 0; e < D; e += 4)
@@ -817,7 +885,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 if (r == 0) ptx::mbar_arrive(ptx::smem_addr(&bars->q_free[b]));
                 continue;
             }
-            const float inv_l = 1.f / l;
+            const float inv_l = 1.f / l_o;
             uint8_t* stage = smem + C::OFF_Q + (b * 2 + t) * C::TILE_BYTES;
 #pragma unroll
             for (int cc = 0; cc < D / 32; ++cc) {
@@ -841,11 +909,16 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     ptx::tma_store_3d(&tm_o, ptx::smem_addr(stage + ch * C::CHUNK_BYTES), ch * 64,
                                       row0, w.bh_q);
                 ptx::bulk_commit();
-                ptx::bulk_wait_read_all();
-                // the staging area (this tile's half of Q buffer b) may be reloaded now
-                ptx::mbar_arrive(ptx::smem_addr(&bars->q_free[b]));
+                // The staging area (this tile's half of Q buffer b) may be reloaded once the
+                // store has read it. With two Q buffers the next unit's Q is already in the
+                // other one, so the release waits until after this tile's next step (or its
+                // next unit without keys, or the end) and the store's read is not waited for
+                // here; with one Q buffer the next unit's Q load needs the release now.
+                rel_pending = b;
+                if (C::NQB < 2) release_staging();
             }
         }
+        release_staging();
     }
 
     ptx::tc_fence_before();

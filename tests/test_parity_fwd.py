@@ -199,3 +199,58 @@ def test_long_sequence_sampled(env):
     """N = 131072 keys and queries (causal, d=64): 1024 key tiles per row block, positions and
     row offsets well past 2^16; 32 seeded rows plus the tile-boundary rows against the oracle."""
     _sampled(env, 1, 1, 131072, 64, True, 4099, 1.0)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [700, 2048])
+def test_softmax_stress_peaked_rows(env, d, causal, N):
+    """Q, K ~ N(0, 3^2): scaled scores with a spread of ~9 make many rows peaked (one weight
+    close to 1), where the rounding of the dominant weight to bf16 matters."""
+    from exact_io_aware_fa_gb300 import synthetic
+    api, orc = env
+    bits = synthetic.attention_inputs(1, 4, N, d, seed=300 + N + d, qk_sigma=3.0)
+    o, lse = run_fwd(api, bits, causal, default_scale(d))
+    o_ref, lse_ref = orc.forward_bf16(bits["q"], bits["k"], bits["v"], causal, default_scale(d))
+    assert_close_o(o, o_ref, f"stress N={N} d={d} causal={causal}")
+    assert_close_lse(lse, lse_ref, f"stress N={N} d={d} causal={causal}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_row_max_growing_along_the_keys(env, d, causal):
+    """Key rows scaled by a factor growing from 1 to 8 along the sequence: every row's maximum
+    keeps growing from key tile to key tile, by more than exp2(8) over a few tiles, so the
+    online rescale runs many times within one row."""
+    from exact_io_aware_fa_gb300 import synthetic
+    api, orc = env
+    N = 1500
+    bits = synthetic.attention_inputs(1, 2, N, d, seed=77 + d)
+    k = synthetic.bf16_bits_to_float64(bits["k"])
+    k = k * (1.0 + 7.0 * np.arange(N) / N)[None, None, :, None]
+    bits["k"] = synthetic.float32_to_bf16_bits(k.astype(np.float32))
+    o, lse = run_fwd(api, bits, causal, default_scale(d))
+    o_ref, lse_ref = orc.forward_bf16(bits["q"], bits["k"], bits["v"], causal, default_scale(d))
+    assert_close_o(o, o_ref, f"growing max d={d} causal={causal}")
+    assert_close_lse(lse, lse_ref, f"growing max d={d} causal={causal}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_single_dominant_key(env, d):
+    """One key per row far above the others (its weight ~1): O must be that key's value row
+    up to output rounding, whichever tile it sits in."""
+    from exact_io_aware_fa_gb300 import synthetic
+    api, orc = env
+    N = 1000
+    bits = synthetic.attention_inputs(1, 1, N, d, seed=91 + d)
+    q = synthetic.bf16_bits_to_float64(bits["q"])
+    k = synthetic.bf16_bits_to_float64(bits["k"]) * 0.25
+    for i in range(N):
+        # key (7919 i) mod N (a permutation) aligned with query i: its scaled score is about
+        # 6 |q_i|^2 / (max|q_i| sqrt(d)) ~ 15-20 above the others' spread of ~0.25
+        k[0, 0, (i * 7919) % N] += 6.0 * q[0, 0, i] / max(1.0, np.abs(q[0, 0, i]).max())
+    bits["k"] = synthetic.float32_to_bf16_bits(k.astype(np.float32))
+    o, lse = run_fwd(api, bits, False, default_scale(d))
+    o_ref, lse_ref = orc.forward_bf16(bits["q"], bits["k"], bits["v"], False, default_scale(d))
+    assert_close_o(o, o_ref, f"dominant key d={d}")
+    assert_close_lse(lse, lse_ref, f"dominant key d={d}")
