@@ -847,8 +847,14 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     }
 }
 
-// L2 budget for one chunk of the causal unit order (about the size of the L2 cache).
-constexpr long long kChunkL2Bytes = 128LL << 20;
+// L2 budget for one chunk of the causal unit order: the chunk's Q, dO and fp32 dQ accumulator
+// rows, which its units re-read and re-add while they sweep their query steps. Measured on
+// B4 H16 N4096 d128 causal (GB300, main kernel): budgeting Q and dO alone at 128 MB put all 64
+// heads in one chunk, a 256 MB working set, and the kernel moved 2.97 GB of DRAM per launch
+// (4.4x the algorithmic 0.67 GB); this budget gives three equal chunks of 21-22 heads and
+// 0.77 GB, at 1.5 % more kernel time (more units of one head run at once, and their
+// reduce-adds meet on the same accumulator rows).
+constexpr long long kChunkL2Bytes = 96LL << 20;
 
 template <int D, bool CAUSAL, bool WINDOW>
 cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t stream) {
@@ -886,12 +892,16 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t stream) {
         sh.nkb = (a.Tk + C::KT - 1) / C::KT;
         const long long units = (long long)sh.nkb * a.BHkv;
         if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-        // Causal: as many KV heads per chunk as keep the chunk's Q and dO (all query heads of
-        // each KV head) within kChunkL2Bytes of L2.
+        // Causal: as many KV heads per chunk as keep the chunk's Q and dO (bf16) and dQ
+        // accumulator (fp32) rows -- all query heads of each KV head -- within kChunkL2Bytes,
+        // with the heads spread evenly over the chunks (a small last chunk would run few heads
+        // on many SMs, all adding into the same accumulator rows).
         sh.kv_chunk = 1;
         if (CAUSAL) {
-            const long long per_head = (long long)sh.group * a.Tq * D * 2 * (long long)sizeof(uint16_t);
+            const long long per_head = (long long)sh.group * a.Tq * D * (2 * 2 + 4);
             sh.kv_chunk = (int)std::max(1LL, std::min<long long>(a.BHkv, kChunkL2Bytes / std::max(1LL, per_head)));
+            const int nchunks = (a.BHkv + sh.kv_chunk - 1) / sh.kv_chunk;
+            sh.kv_chunk = (a.BHkv + nchunks - 1) / nchunks;
         }
         // Persistent grid: one CTA per SM walking units (the shared memory admits one CTA).
         const int grid = (int)std::min<long long>(units, (long long)std::max(1, a.num_sms));

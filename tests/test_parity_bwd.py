@@ -138,11 +138,12 @@ def test_persistent_many_units_per_cta(env, d, causal):
 
 def test_causal_unit_order_in_several_head_chunks(env):
     """Causal launches order their units key tile by key tile inside chunks of KV heads whose
-    Q/dO fit in 128 MB of L2. B1 H40 N8192 d128 needs 4 MB per head: chunks of 32 and 8 heads
-    (the last one ragged). dQ on seeded query rows, dK/dV on seeded key rows."""
+    Q, dO and fp32 dQ accumulator rows fit in 96 MB of L2, spread evenly over the chunks.
+    B1 H42 N8192 d128 needs 8 MB per head: four chunks of 11, 11, 11 and 9 heads (the last one
+    ragged). dQ on seeded query rows, dK/dV on seeded key rows."""
     from exact_io_aware_fa_gb300 import synthetic
     api, orc = env
-    B, H, N, d = 1, 40, 8192, 128
+    B, H, N, d = 1, 42, 8192, 128
     bits = synthetic.attention_inputs(B, H, N, d, seed=4040, with_dout=True)
     dq, dk, dv = run_fwd_bwd(api, bits, True, default_scale(d))
     rq = synthetic.sample_rows(N, 16, 4040)
