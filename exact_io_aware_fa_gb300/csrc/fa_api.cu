@@ -518,7 +518,11 @@ fa_status fa_backward_ex(const void* q, const void* k, const void* v, const void
     a.folds = ws;
     a.dq_acc = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + 2 * (size_t)sh.BHq * (size_t)Npad * 16u);
     a.sched = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(ws) + ws_bytes - kSchedBytes);
-    if ((st = make_map(&a.tm_dqacc, a.dq_acc, sh.BHq, Npad, d, q_rows, true)) != FA_OK) {
+    // dQ accumulator: [B*Hq, Npad, d] at d = 64; at d = 128 the main kernel computes dQ
+    // transposed and accumulates it as [B*Hq, d, Npad] (boxes of 32 queries x 128 rows).
+    st = (d == 128) ? make_map(&a.tm_dqacc, a.dq_acc, sh.BHq, d, Npad, 128, true)
+                    : make_map(&a.tm_dqacc, a.dq_acc, sh.BHq, Npad, d, q_rows, true);
+    if (st != FA_OK) {
         if (owned) cudaFreeAsync(ws, s);
         return st;
     }

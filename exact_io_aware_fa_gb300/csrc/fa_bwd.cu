@@ -161,6 +161,35 @@ fa_bwd_dq_kernel(const float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ d
     *reinterpret_cast<uint4*>(dq + ((size_t)bh * N + n) * D + col8 * 8) = w;
 }
 
+// dQ convert for d = 128, whose main kernel accumulates dQ transposed, [B*H][d][Npad] (each
+// drain thread then owns a contiguous row). A block transposes a tile of 64 queries x 128
+// head-dim columns through shared memory: reads along the queries, writes bf16 rows.
+__global__ void __launch_bounds__(256)
+fa_bwd_dqt_kernel(const float* __restrict__ dq_acc_t, __nv_bfloat16* __restrict__ dq, int N,
+                  int Npad, int tiles, float scale) {
+    constexpr int D = 128, TQ = 64;
+    __shared__ float tile[D][TQ + 1];
+    ptx::griddep_wait();  // the main kernel's dQ sums (this kernel may launch during its tail)
+    const int bh = (int)(blockIdx.x / (unsigned)tiles);
+    const int n0 = (int)(blockIdx.x % (unsigned)tiles) * TQ;
+    const float* src = dq_acc_t + (size_t)bh * D * Npad + n0;
+#pragma unroll 4
+    for (int i = 0; i < D * TQ / 256; ++i) {
+        const int idx = i * 256 + (int)threadIdx.x;
+        const int e = idx / TQ, q = idx % TQ;
+        tile[e][q] = src[(size_t)e * Npad + q];  // n0 + q < Npad (Npad is a multiple of 128)
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int i = 0; i < D * TQ / 512; ++i) {
+        const int idx = i * 256 + (int)threadIdx.x;
+        const int q = idx / (D / 2), e = 2 * (idx % (D / 2));
+        if (n0 + q < N)
+            *reinterpret_cast<uint32_t*>(dq + ((size_t)bh * N + n0 + q) * D + e) =
+                ptx::pack_bf16x2(tile[e][q] * scale, tile[e + 1][q] * scale);
+    }
+}
+
 // ----------------------------------------------------------------------------------------
 // Main backward kernel.
 // ----------------------------------------------------------------------------------------
@@ -188,9 +217,10 @@ struct BwdCfg {
     static constexpr uint32_t DS_BYTES = (uint32_t)BMQ * 128u * 2u;
     static constexpr uint32_t DSREG = 128u * 128u;           // one 64-query region
     static constexpr uint32_t DQBOX = (uint32_t)BMQ * 128u;  // one 32-column fp32 box
+    static constexpr uint32_t DQBOX_T = 128u * 128u;         // d = 128: 32 queries x 128 e rows
     // fp32 dQ staging: d=64 drains one box at a time through one box of staging (the shared
     // memory goes to the second dS buffer); d=128 stages all four boxes at once.
-    static constexpr uint32_t DQS_BYTES = (D == 64) ? DQBOX : (uint32_t)BMQ * D * 4u;
+    static constexpr uint32_t DQS_BYTES = (D == 64) ? DQBOX : 2u * DQBOX_T;
     static constexpr uint32_t OFF_K = 0;
     static constexpr uint32_t OFF_V = OFF_K + KTILE;
     static constexpr uint32_t OFF_ST = OFF_V + KTILE;
@@ -744,22 +774,24 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 ptx::mbar_arrive(ptx::smem_addr(&bars->dq_free));
                 staging_free();
                 if (D == 128) {
-                    // lane r = head-dim column e; a/b hold query rows 0-31 / 32-63.
-                    // fp32 box (e / 32): [BMQ rows x 128 B], element e at byte 4 (e % 32).
-                    uint8_t* box = dqs + (r >> 5) * C::DQBOX;
-                    const uint32_t uu = (uint32_t)((r & 31) >> 2);
-                    const uint32_t wb = (uint32_t)(r & 3) * 4u;
+                    // lane r = head-dim column e; a/b hold query rows 0-31 / 32-63 of the step.
+                    // The accumulator is kept transposed ([e][query], see the dQ conversion), so
+                    // each thread's values are one contiguous row: box bx holds queries
+                    // [32 bx, 32 bx + 32) of all 128 e rows, 128 B per row, written with
+                    // 16-byte stores (a row per thread instead of one element per row).
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        *reinterpret_cast<uint32_t*>(box + sw128_offset((uint32_t)j, uu) + wb) = a[j];
-                        *reinterpret_cast<uint32_t*>(box + sw128_offset((uint32_t)(32 + j), uu) + wb) = b[j];
+                    for (int uu = 0; uu < 8; ++uu) {
+                        *reinterpret_cast<uint4*>(dqs + sw128_offset((uint32_t)r, (uint32_t)uu)) =
+                            make_uint4(a[4 * uu], a[4 * uu + 1], a[4 * uu + 2], a[4 * uu + 3]);
+                        *reinterpret_cast<uint4*>(dqs + C::DQBOX_T + sw128_offset((uint32_t)r, (uint32_t)uu)) =
+                            make_uint4(b[4 * uu], b[4 * uu + 1], b[4 * uu + 2], b[4 * uu + 3]);
                     }
                     ptx::fence_proxy_async_smem();
                     ptx::named_bar_sync(2, 128);
                     if (r == 0) {
-                        for (int bx = 0; bx < D / 32; ++bx)
-                            ptx::tma_reduce_add_3d(&tm_dqacc, ptx::smem_addr(dqs + bx * C::DQBOX), bx * 32,
-                                                   q0, bhq);
+                        for (int bx = 0; bx < 2; ++bx)
+                            ptx::tma_reduce_add_3d(&tm_dqacc, ptx::smem_addr(dqs + bx * C::DQBOX_T),
+                                                   q0 + 32 * bx, 0, bhq);
                         ptx::bulk_commit();
                     }
                 } else {
@@ -912,7 +944,14 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
     }
     // 3. dQ convert (query heads)
-    {
+    if constexpr (D == 128) {
+        const long long tiles = ((long long)a.Tq + 63) / 64;
+        const long long blocks = tiles * a.BHq;
+        if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+        return launch_dependent(fa_bwd_dqt_kernel, dim3((unsigned)blocks), dim3(256), 0, stream,
+                                static_cast<const float*>(a.dq_acc),
+                                static_cast<__nv_bfloat16*>(a.dq), a.Tq, a.Npad, (int)tiles, a.scale);
+    } else {
         const long long total8 = (long long)a.BHq * a.Tq * (D / 8);
         const long long blocks = (total8 + 255) / 256;
         if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;

@@ -39,14 +39,15 @@ struct BwdLaunch {
     CUtensorMap tm_q, tm_do;              // [B*Hq, Tq, d] loads, box {64, query rows, 1}
     CUtensorMap tm_k, tm_v;               // [B*Hkv, Tk, d] loads, box {64, 128, 1}
     CUtensorMap tm_dk, tm_dv;             // [B*Hkv, Tk, d] stores, box {64, 128, 1}
-    CUtensorMap tm_dqacc;                 // fp32 [B*Hq, Npad, d] accumulator, box {32, rows, 1}
+    CUtensorMap tm_dqacc;                 // fp32 dQ accumulator: d = 64 [B*Hq, Npad, d], box {32, rows, 1};
+                                          // d = 128 transposed [B*Hq, d, Npad], box {32, 128, 1}
     const void* o;                        // bf16 [B*Hq, Tq, d]
     const void* dout;                     // bf16 [B*Hq, Tq, d]
     const float* lse;                     // fp32 [B*Hq, Tq]
     void* dq;                             // bf16 [B*Hq, Tq, d]
-    void* folds;                          // workspace: per query row, 32-byte records of
+    void* folds;                          // workspace: per query row, 16-byte records of
                                           // -LSE/scale then of -D ([B*Hq, Npad] each)
-    float* dq_acc;                        // workspace: fp32 [B*Hq, Npad, d]
+    float* dq_acc;                        // workspace: fp32 B*Hq*Npad*d (layout: tm_dqacc)
     unsigned* sched;                      // workspace: the main kernel's unit counter
     int Tq, Tk, Npad, Hq, Hkv, BHq, BHkv, d, window;
     float scale;

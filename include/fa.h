@@ -128,7 +128,7 @@ fa_status fa_forward_splitkv(const void* q, const void* k, const void* v, void* 
 /*
  * Bytes of device workspace fa_backward needs for these sizes: two 16-byte records per query
  * row holding -LSE/scale and -D_i (D_i = O_i . dO_i) as exact three-part bf16 sums, [B*H, Npad]
- * each, an fp32 dQ accumulator [B*H, Npad, d] (Npad = N rounded up to 128) and 256 bytes for
+ * each, an fp32 dQ accumulator of B*H*Npad*d elements (Npad = N rounded up to 128) and 256 bytes for
  * the counter that hands out the main kernel's work units. In total B*H*Npad*(32 + 4d) + 256
  * bytes. Returns 0 for invalid sizes or when B*H*N == 0.
  */
