@@ -55,6 +55,20 @@ METRIC = ("attention fwd+bwd TFLOPS (bf16 in, fp32 accumulate), 1 step = fa_forw
           " on B4 H16 N2048 d64")
 
 
+def select_workload(key):
+    """The main step's workload: configuration 2 by default (the one the metric is quoted on);
+    `--config K` runs another configuration's fwd + bwd step instead (for profiling)."""
+    global WORKLOAD, METRIC
+    if key == "2":
+        return
+    cfg = next(c for c in CONFIGS if c["name"].split(":")[0] == key)
+    WORKLOAD = dict(name=cfg["name"].split(": ", 1)[1] + " fwd+bwd", B=cfg["B"], H=cfg["H"],
+                    N=cfg["N"], d=cfg["d"], causal=cfg["causal"], seed=cfg["seed"],
+                    qk_sigma=cfg["qk_sigma"])
+    METRIC = ("attention fwd+bwd TFLOPS (bf16 in, fp32 accumulate), 1 step = fa_forward + "
+              "fa_backward on " + WORKLOAD["name"])
+
+
 def workload_config(world=1):
     w = WORKLOAD
     return {"workload": w["name"], "global_batch": w["B"] * world, "seq_len": w["N"],
@@ -81,6 +95,10 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-configuration block")
     ap.add_argument("--config-reps", type=int, default=20)
+    ap.add_argument("--config", default="2", choices=["1", "2", "3", "4", "4r", "5"],
+                    help="configuration of the main timed step (default 2)")
+    ap.add_argument("--naive-only", action="store_true",
+                    help="only the naive-vs-fused forward comparison (one JSON line; profiling)")
     return ap.parse_args()
 
 
@@ -278,6 +296,50 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+# ---- naive (materialised) attention as the comparison point -----------------------------
+
+def naive_vs_fused(api, dev, reps=10):
+    """Forward time and peak device memory of naive materialised attention (S and P written to
+    HBM; exact_io_aware_fa_gb300.naive) against the fused forward, on configuration 2 and on
+    T = 4096 ("15. FlashAttention", "Stretch exercises" item 1). Context only."""
+    import torch
+    from exact_io_aware_fa_gb300 import naive
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    out = []
+    for (B, H, N, d) in ((4, 16, 2048, 64), (1, 16, 4096, 64)):
+        g = torch.Generator(device=dev)
+        g.manual_seed(4242)
+        q, k, v = (torch.randn((B, H, N, d), generator=g, device=dev).to(torch.bfloat16)
+                   for _ in range(3))
+        res = {"workload": f"B{B} H{H} N{N} d{d} non-causal forward"}
+        for name, fn in (("naive", lambda: naive.forward(q, k, v)),
+                         ("fused", lambda: api.forward(q, k, v))):
+            fn()
+            torch.cuda.synchronize()
+            base = torch.cuda.memory_allocated(dev)
+            torch.cuda.reset_peak_memory_stats(dev)
+            fn()
+            torch.cuda.synchronize()
+            peak = torch.cuda.max_memory_allocated(dev) - base
+            ts = []
+            for _ in range(reps):
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                fn()
+                b.record()
+                torch.cuda.synchronize()
+                ts.append(a.elapsed_time(b))
+            ms = statistics.median(ts)
+            res[name] = {"ms": ms, "tflops": fwd_flops(B, H, N, d, False) / ms / 1e9,
+                         "peak_bytes_beyond_inputs": int(peak)}
+        res["speedup"] = res["naive"]["ms"] / res["fused"]["ms"]
+        out.append(res)
+        del q, k, v
+        torch.cuda.empty_cache()
+    return out
+
+
 # ---- GPU arm -------------------------------------------------------------------------------------
 
 def _traffic_record(kernel, workload):
@@ -392,7 +454,7 @@ def run_ours(args, rank, world, local):
     # Weak scaling: every rank runs the full workload on its own heads (its own seed).
     from exact_io_aware_fa_gb300 import dist as fadist
     bits = synthetic.attention_inputs(B, H, N, d, seed=fadist.rank_seed(w["seed"], rank),
-                                      with_dout=True)
+                                      qk_sigma=w.get("qk_sigma", 1.0), with_dout=True)
 
     def dev_t(b):
         return torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).to(dev)
@@ -460,7 +522,9 @@ def run_ours(args, rank, world, local):
     dom_tf = bwd_tf if dominant == "fa_bwd" else fwd_tf
     dom_ms = bwd_med if dominant == "fa_bwd" else fwd_med
 
-    rec = _traffic_record(dominant, CONFIGS[1]["name"])
+    cfg_name = next((c["name"] for c in CONFIGS
+                     if (c["B"], c["H"], c["N"], c["d"], c["causal"]) == (B, H, N, d, causal)), None)
+    rec = _traffic_record(dominant, cfg_name) if cfg_name else None
     traffic = rec["bytes_per_launch"] if rec else None
 
     # ---- end to end through the public API with host buffers ----------------------------------
@@ -501,8 +565,10 @@ def run_ours(args, rank, world, local):
                "ms_per_step": e2e_ms / args.steps}
 
     configs = None
+    naive_cmp = None
     if not args.no_configs:
         configs = time_configs(api, dev, args.config_reps, peaks)
+        naive_cmp = naive_vs_fused(api, dev)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -533,6 +599,7 @@ def run_ours(args, rank, world, local):
                      "hbm_gbs": (traffic / (dom_ms * 1e-3) / 1e9) if traffic else None,
                      "peak_source": f"{peaks['source']} bf16 burst"},
         "configs": configs,
+        "naive_vs_fused": naive_cmp,
         "e2e": e2e,
         "gpu_launches": args.steps * 4,
         "clocks": clocks,
@@ -541,8 +608,24 @@ def run_ours(args, rank, world, local):
     print(json.dumps(line), flush=True)
 
 
+def run_naive_only(args):
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from exact_io_aware_fa_gb300 import api
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    print(json.dumps({"naive_vs_fused": naive_vs_fused(api, dev, reps=max(1, args.steps))}),
+          flush=True)
+
+
 def main():
     args = parse_args()
+    select_workload(args.config)
+    if args.naive_only:
+        run_naive_only(args)
+        return
     rank, world, local = dist_init(args.gpus)
     if args.impl == "reference":
         run_reference(args, rank, world)

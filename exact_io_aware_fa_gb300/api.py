@@ -27,7 +27,7 @@ EXPORTS = ("fa_forward", "fa_forward_ex", "fa_forward_splitkv_workspace_bytes",
            "fa_forward_splitkv", "fa_forward_choose_splits", "fa_backward_workspace_bytes",
            "fa_backward",
            "fa_backward_ex", "fa_backward_noalloc", "fa_noalloc_scratch_bytes",
-           "fa_forward_backward_host_device_bytes",
+           "fa_forward_backward_host_device_bytes", "fa_naive_softmax",
            "fa_forward_backward_host", "fa_selftest_wait_timeout", "fa_status_string",
            "fa_last_cuda_error", "fa_device_error")
 
@@ -80,6 +80,8 @@ def library(path: str | None = None):
         lib.fa_backward_ex.restype = I
         lib.fa_backward_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, P]
         lib.fa_backward_noalloc.restype = I
+        lib.fa_naive_softmax.argtypes = [P, P, P, ctypes.c_longlong, I, I, F, P]
+        lib.fa_naive_softmax.restype = I
         lib.fa_noalloc_scratch_bytes.argtypes = []
         lib.fa_noalloc_scratch_bytes.restype = Z
         lib.fa_forward_backward_host_device_bytes.argtypes = [I, I, I, I, I, I, I]

@@ -19,7 +19,8 @@ LIB = os.path.join(PKG, "libfa.so")
 SOURCES = [("fa_api.cu", "fa_api.o", []),
            ("fa_fwd.cu", "fa_fwd_d64.o", ["-DFA_FWD_D=64"]),
            ("fa_fwd.cu", "fa_fwd_d128.o", ["-DFA_FWD_D=128"]),
-           ("fa_bwd.cu", "fa_bwd.o", [])]
+           ("fa_bwd.cu", "fa_bwd.o", []),
+           ("fa_naive.cu", "fa_naive.o", [])]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2",
                  "-I", os.path.join(ROOT, "include"), "-Xptxas", "-v"]

@@ -572,6 +572,20 @@ fa_status fa_backward_noalloc(const void* q, const void* k, const void* v, const
 
 size_t fa_noalloc_scratch_bytes(void) { return (size_t)FA_NOALLOC_SCRATCH_BYTES; }
 
+fa_status fa_naive_softmax(const float* s, void* p, float* lse, long long rows, int N, int causal,
+                           float scale, struct CUstream_st* stream) {
+    if (rows < 0 || N < 0 || (causal != 0 && causal != 1)) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+    if (rows == 0 || N == 0) return FA_OK;
+    if (!s || !p || !lse) return FA_ERR_INVALID_ARG;
+    if (!aligned(s, 4) || !aligned(p, 2) || !aligned(lse, 4)) return FA_ERR_ALIGNMENT;
+    fa_status st = bind_context();
+    if (st != FA_OK) return st;
+    cudaError_t e = fa::launch_naive_softmax(s, p, lse, rows, N, causal, scale,
+                                             reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
 fa_status fa_selftest_wait_timeout(unsigned int limit_us, struct CUstream_st* stream) {
     if (limit_us == 0 || limit_us > 1000000u) return FA_ERR_INVALID_ARG;
     int* err = nullptr;

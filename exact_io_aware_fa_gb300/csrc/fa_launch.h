@@ -58,4 +58,8 @@ struct BwdLaunch {
 
 cudaError_t launch_backward(const BwdLaunch& a, bool causal, cudaStream_t stream);
 
+// Naive (materialised) attention's row softmax over a stored score matrix (comparison only).
+cudaError_t launch_naive_softmax(const float* s, void* p, float* lse, long long rows, int N,
+                                 int causal, float scale, cudaStream_t stream);
+
 }  // namespace fa

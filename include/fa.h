@@ -242,6 +242,22 @@ fa_status fa_forward_backward_host(const void* q, const void* k, const void* v, 
                                    struct CUstream_st* stream);
 
 /*
+ * Row softmax of naive (materialised) attention -- the comparison point the IO-aware method is
+ * measured against, not part of it ("15. FlashAttention", section "The score matrix is the
+ * problem" and "Stretch exercises" item 1; "FlashAttention V1", the standard-attention
+ * baseline). A GEMM writes the full score matrix to HBM; this call reads it back and writes
+ * the probabilities and the row log-sum-exp; a second GEMM forms O = P V.
+ *   s    in : fp32 [rows, N], rows = B*H*N, raw dot products q_i . k_j of each head
+ *   p    out: bf16 [rows, N], P_ij = exp(scale s_ij - m_i) / l_i for visible j, else 0
+ *   lse  out: fp32 [rows],   m_i + ln l_i (natural log of the scaled scores)
+ *   With causal = 1, row r sees keys j <= r mod N. Safe softmax (max subtracted), fp32.
+ * Errors: FA_ERR_INVALID_ARG (negative sizes, causal not 0/1, scale not finite or not > 0,
+ * NULL pointers with work), FA_ERR_ALIGNMENT, FA_ERR_CUDA. rows * N == 0 launches nothing.
+ */
+fa_status fa_naive_softmax(const float* s, void* p, float* lse, long long rows, int N, int causal,
+                           float scale, struct CUstream_st* stream);
+
+/*
  * Diagnostic of the failure path (no counterpart in the pages). Launches one warp that waits,
  * through the same bounded mbarrier wait the attention kernels use, on a barrier nothing ever
  * arrives on; after `limit_us` microseconds (1 .. 1000000) the wait gives up, records code 1

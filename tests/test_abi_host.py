@@ -1,5 +1,9 @@
 """Host-side checks of the C ABI (no GPU): the library loads, exports every symbol the
-header declares, and rejects bad arguments before launching anything."""
+header declares, and rejects bad arguments before launching anything.
+
+The device pointers here are fake addresses. Every call must stop at argument validation or at
+an empty-shape early return, so that none reaches a launch or a copy even where a GPU is
+present: a call that passed validation would hand the fake address to a kernel."""
 import os
 import re
 
@@ -147,7 +151,10 @@ def test_ex_empty_is_ok(lib):
     assert fwd_ex(lib, Tq=0) == 0
     assert fwd_ex(lib, B=0) == 0
     assert fwd_ex(lib, Hq=0, Hkv=0, q=0, k=0, v=0, o=0, lse=0) == 0
-    assert fwd_ex(lib, causal=0, Tq=500, Tk=200) != 1  # non-causal: Tq > Tk is fine
+    # non-causal Tq > Tk is a valid shape: it passes the shape checks and stops at the next
+    # one, the misaligned output pointer (FA_ERR_ALIGNMENT, not FA_ERR_INVALID_ARG). A call with
+    # a valid shape and well-formed fake pointers would launch a kernel on a machine with a GPU.
+    assert fwd_ex(lib, causal=0, Tq=500, Tk=200, o=A + 2) == 3
     assert bwd_ex(lib, B=0) == 0
     assert bwd_ex(lib, Tq=0, Tk=0) == 0
 
@@ -237,3 +244,16 @@ def test_host_step_device_bytes():
     assert api.host_step_device_bytes(1, 2, 1, 128, 256, 64, 0) == 411136
     assert api.host_step_device_bytes(1, 2, 1, 128, 256, 64, 17) == 0
     assert api.host_step_device_bytes(1, 2, 1, 128, 256, 96, 0) == 0
+
+
+def test_naive_softmax_argument_checks(lib):
+    """fa_naive_softmax validates before launching anything (no GPU needed)."""
+    from exact_io_aware_fa_gb300 import api
+    A = 1 << 20
+    assert lib.fa_naive_softmax(A, A, A, -1, 16, 0, 0.125, None) == api.FA_ERR_INVALID_ARG
+    assert lib.fa_naive_softmax(A, A, A, 16, 16, 2, 0.125, None) == api.FA_ERR_INVALID_ARG
+    assert lib.fa_naive_softmax(A, A, A, 16, 16, 0, 0.0, None) == api.FA_ERR_INVALID_ARG
+    assert lib.fa_naive_softmax(A, A, A, 16, 16, 0, float("nan"), None) == api.FA_ERR_INVALID_ARG
+    assert lib.fa_naive_softmax(None, A, A, 16, 16, 0, 0.125, None) == api.FA_ERR_INVALID_ARG
+    assert lib.fa_naive_softmax(A + 2, A, A, 16, 16, 0, 0.125, None) == api.FA_ERR_ALIGNMENT
+    assert lib.fa_naive_softmax(None, None, None, 0, 16, 0, 0.125, None) == api.FA_OK
