@@ -56,6 +56,19 @@ def test_naive_causal_small(env, N):
     assert_close_lse(lse, lse_ref, f"naive causal N={N}")
 
 
+@pytest.mark.parametrize("N,causal", [(4096, True), (4500, False), (4500, True)],
+                         ids=["4096-causal", "4500", "4500-causal"])
+def test_naive_long_rows(env, N, causal):
+    """Rows of 4096 keys (the widest held in registers) and of 4500 (the two-pass kernel)."""
+    from exact_io_aware_fa_gb300 import synthetic
+    naive, orc = env
+    bits = synthetic.attention_inputs(1, 1, N, 64, seed=700 + N + int(causal))
+    o, lse = _run(naive, bits, causal, default_scale(64))
+    o_ref, lse_ref = orc.forward_bf16(bits["q"], bits["k"], bits["v"], causal, default_scale(64))
+    assert_close_o(o, o_ref, f"naive N={N} causal={causal}")
+    assert_close_lse(lse, lse_ref, f"naive N={N} causal={causal}")
+
+
 def test_naive_worked_example(env):
     """Scores [0,1,2,-1] against values [2,4,1,3] give 1.8619 ("15. FlashAttention", section
     "Worked example"), computed the materialised way."""
