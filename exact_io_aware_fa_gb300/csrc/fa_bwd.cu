@@ -932,7 +932,27 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t stream) {
         if (CAUSAL) {
             const long long per_head = (long long)sh.group * a.Tq * D * (2 * 2 + 4);
             sh.kv_chunk = (int)std::max(1LL, std::min<long long>(a.BHkv, kChunkL2Bytes / std::max(1LL, per_head)));
-            const int nchunks = (a.BHkv + sh.kv_chunk - 1) / sh.kv_chunk;
+            int nchunks = (a.BHkv + sh.kv_chunk - 1) / sh.kv_chunk;
+            // A chunk starts with its costliest units; if a chunk holds less work per SM than
+            // its costliest unit, the last chunk's long units outlast everything else. So there
+            // are at most (steps of the launch) / (SMs * steps of the costliest unit) chunks.
+            const int nq_total = (a.Tq + C::BMQ - 1) / C::BMQ;
+            long long steps_per_kv = 0, max_unit = 0;
+            for (int kb = 0; kb < sh.nkb; ++kb) {
+                const int key0 = kb * C::KT;
+                const int i0 = std::max(0, key0 - sh.offset) / C::BMQ;
+                int i1 = nq_total - 1;
+                if (WINDOW) {
+                    const int reach = key0 + C::KT - 1 + sh.window - sh.offset;
+                    i1 = (reach < 0) ? -1 : std::min(i1, reach / C::BMQ);
+                }
+                const long long n = (long long)std::max(0, i1 - i0 + 1) * sh.group;
+                steps_per_kv += n;
+                max_unit = std::max(max_unit, n);
+            }
+            const long long cap = (steps_per_kv * a.BHkv) /
+                                  std::max(1LL, (long long)std::max(1, a.num_sms) * max_unit);
+            nchunks = (int)std::max(1LL, std::min<long long>(nchunks, cap));
             sh.kv_chunk = (a.BHkv + nchunks - 1) / nchunks;
         }
         // Persistent grid: one CTA per SM walking units (the shared memory admits one CTA).

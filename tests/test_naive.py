@@ -56,10 +56,13 @@ def test_naive_causal_small(env, N):
     assert_close_lse(lse, lse_ref, f"naive causal N={N}")
 
 
-@pytest.mark.parametrize("N,causal", [(4096, True), (4500, False), (4500, True)],
-                         ids=["4096-causal", "4500", "4500-causal"])
+@pytest.mark.parametrize("N,causal", [(4096, True), (4500, False), (4500, True), (1030, True),
+                                     (8200, False)],
+                         ids=["4096-causal", "4500", "4500-causal", "1030-causal", "8200"])
 def test_naive_long_rows(env, N, causal):
-    """Rows of 4096 keys (the widest held in registers) and of 4500 (the two-pass kernel)."""
+    """Each softmax kernel of the naive path: a block per row for 1024 < N <= 8192 with N a
+    multiple of 4 (4096, and 4500 with a ragged last vector), the two-pass warp kernel for
+    N = 1030 (not a multiple of 4) and N = 8200 (beyond 8192)."""
     from exact_io_aware_fa_gb300 import synthetic
     naive, orc = env
     bits = synthetic.attention_inputs(1, 1, N, 64, seed=700 + N + int(causal))
