@@ -664,70 +664,153 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 const int p0 = sh.offset + q0;
                 const bool need_mask = CAUSAL && ((p0 < key0 + C::KT - 1) ||
                                                   (WINDOW && p0 + C::BMQ - 1 - sh.window > key0));
+                if constexpr (NCH_H == 1) {
+                    // P^T (to TMEM) and dS (to shared memory) of one 32-query chunk cc
+                    auto compute_chunk = [&](int cc, const uint32_t (&sv)[32], const uint32_t (&dpv)[32],
+                                             uint32_t (&pk)[16], uint32_t (&dk)[16]) {
 #pragma unroll
-                for (int ci = 0; ci < NCH_H; ++ci) {
-                    const int cc = h * NCH_H + ci;
-                    uint32_t sv[32], dpv[32];
-                    ptx::tmem_ld32_nowait(t_s + 32 * cc, sv);
-                    ptx::tmem_ld32_nowait(t_dp + 32 * cc, dpv);
-                    ptx::tmem_wait_ld(sv);
-                    ptx::tmem_wait_ld(dpv);
-                    if (ci == NCH_H - 1) {
-                        // this half's S^T/dP^T columns are in registers: release them
-                        ptx::tc_fence_before();
-                        ptx::mbar_arrive(ptx::smem_addr(&bars->s_free));
-                    }
-                    uint32_t pk[16], dk[16];
-#pragma unroll
-                    for (int j = 0; j < 32; j += 4) {
-                        const int qi = 32 * cc + j;
-                        // x = c * S' = c * S - LSE * log2(e)
-                        float x0, x1, x2, x3;
-                        ptx::fmul2(x0, x1, __uint_as_float(sv[j]), __uint_as_float(sv[j + 1]), c, c);
-                        ptx::fmul2(x2, x3, __uint_as_float(sv[j + 2]), __uint_as_float(sv[j + 3]), c, c);
-                        float pe0 = ptx::ex2_approx(x0), pe1 = ptx::ex2_approx(x1);
-                        float pe2 = ptx::ex2_approx(x2), pe3 = ptx::ex2_approx(x3);
-                        if (need_mask) {
-                            // visible iff key <= p <= key + window, i.e. p - key in [0, vspan]
-                            const uint32_t dp = (uint32_t)(p0 + qi - key);
-                            if (dp > vspan) pe0 = 0.f;
-                            if (dp + 1u > vspan) pe1 = 0.f;
-                            if (dp + 2u > vspan) pe2 = 0.f;
-                            if (dp + 3u > vspan) pe3 = 0.f;
+                        for (int j = 0; j < 32; j += 4) {
+                            const int qi = 32 * cc + j;
+                            // x = c * S' = c * S - LSE * log2(e)
+                            float x0, x1, x2, x3;
+                            ptx::fmul2(x0, x1, __uint_as_float(sv[j]), __uint_as_float(sv[j + 1]), c, c);
+                            ptx::fmul2(x2, x3, __uint_as_float(sv[j + 2]), __uint_as_float(sv[j + 3]), c, c);
+                            float pe0 = ptx::ex2_approx(x0), pe1 = ptx::ex2_approx(x1);
+                            float pe2 = ptx::ex2_approx(x2), pe3 = ptx::ex2_approx(x3);
+                            if (need_mask) {
+                                // visible iff key <= p <= key + window, i.e. p - key in [0, vspan]
+                                const uint32_t dp = (uint32_t)(p0 + qi - key);
+                                if (dp > vspan) pe0 = 0.f;
+                                if (dp + 1u > vspan) pe1 = 0.f;
+                                if (dp + 2u > vspan) pe2 = 0.f;
+                                if (dp + 3u > vspan) pe3 = 0.f;
+                            }
+                            // dS = P (dP - D) = P dP'
+                            float d0, d1, d2, d3;
+                            ptx::fmul2(d0, d1, pe0, pe1, __uint_as_float(dpv[j]), __uint_as_float(dpv[j + 1]));
+                            ptx::fmul2(d2, d3, pe2, pe3, __uint_as_float(dpv[j + 2]), __uint_as_float(dpv[j + 3]));
+                            pk[j / 2] = ptx::pack_bf16x2(pe0, pe1);
+                            pk[j / 2 + 1] = ptx::pack_bf16x2(pe2, pe3);
+                            dk[j / 2] = ptx::pack_bf16x2(d0, d1);
+                            dk[j / 2 + 1] = ptx::pack_bf16x2(d2, d3);
                         }
-                        // dS = P (dP - D) = P dP'
-                        float d0, d1, d2, d3;
-                        ptx::fmul2(d0, d1, pe0, pe1, __uint_as_float(dpv[j]), __uint_as_float(dpv[j + 1]));
-                        ptx::fmul2(d2, d3, pe2, pe3, __uint_as_float(dpv[j + 2]), __uint_as_float(dpv[j + 3]));
-                        pk[j / 2] = ptx::pack_bf16x2(pe0, pe1);
-                        pk[j / 2 + 1] = ptx::pack_bf16x2(pe2, pe3);
-                        dk[j / 2] = ptx::pack_bf16x2(d0, d1);
-                        dk[j / 2 + 1] = ptx::pack_bf16x2(d2, d3);
-                    }
-                    if (ci == 0) {
-                        if (g > 0) {
-                            // dV of step g - 1 must have read P^T before it is overwritten.
+                    };
+                    auto store_chunk = [&](int cc, const uint32_t (&pk)[16], const uint32_t (&dk)[16]) {
+                        ptx::tmem_st16(t_pt + 16 * cc, pk);
+                        // dS row k (queries contiguous) into the 128B-swizzled dS tile.
+                        uint8_t* region = dsbuf + (cc >> 1) * C::DSREG;
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const uint4 wv = make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
+                            *reinterpret_cast<uint4*>(region + sw128_offset((uint32_t)k, (uint32_t)((cc & 1) * 4 + u))) = wv;
+                        }
+                    };
+                    // The waits before the first P^T / dS store: dV of step g - 1 has read P^T, and
+                    // dK and dQ of step g - NDS have read this dS buffer.
+                    auto wait_buffers = [&]() {
+                        if (g > 0)
                             ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->mma_done),
                                                                     (uint32_t)(g - 1) & 1u, abort_flag,
                                                                     err, kDevTimeoutMma));
-                            if (!ok) break;
-                        }
-                        if (g >= C::NDS) {
-                            // dK and dQ of step g - NDS must have read this dS buffer.
+                        if (ok && g >= C::NDS)
                             ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->ds_free[g % C::NDS]),
                                                                     (uint32_t)(g / C::NDS - 1) & 1u,
                                                                     abort_flag, err, kDevTimeoutMma));
-                            if (!ok) break;
-                        }
                         ptx::tc_fence_after();
+                    };
+                    auto release_s = [&]() {  // this half's S^T/dP^T are in registers
+                        ptx::tc_fence_before();
+                        ptx::mbar_arrive(ptx::smem_addr(&bars->s_free));
+                    };
+                    // Where S^T/dP^T are released decides whether the next step's S^T/dP^T MMAs run
+                    // ahead of this step's dV/dK/dQ MMAs in the tensor pipe. Measured (backward
+                    // TFLOP/s, GB300): d=128 (one 32-query chunk per warpgroup) releases after the
+                    // chunk's exp2 phase and before the buffer waits (configuration 5: 975 with the
+                    // release right after the load, 1011 here, 934 after the waits); d=64 (two chunks)
+                    // releases after loading its second chunk, behind the waits (B4 H16 N2048: 880;
+                    // 853 with both chunks loaded before the waits, 864 after them).
+                    const int cc0 = h;
+                    uint32_t pk[16], dk[16];
+                    {
+                        uint32_t sv[32], dpv[32];
+                        ptx::tmem_ld32_nowait(t_s + 32 * cc0, sv);
+                        ptx::tmem_ld32_nowait(t_dp + 32 * cc0, dpv);
+                        ptx::tmem_wait_ld(sv);
+                        ptx::tmem_wait_ld(dpv);
+                        compute_chunk(cc0, sv, dpv, pk, dk);
                     }
-                    ptx::tmem_st16(t_pt + 16 * cc, pk);
-                    // dS row k (queries contiguous) into the 128B-swizzled dS tile.
-                    uint8_t* region = dsbuf + (cc >> 1) * C::DSREG;
+                    release_s();
+                    wait_buffers();
+                    if (!ok) break;
+                    store_chunk(cc0, pk, dk);
+                } else {
+                    // d=64: the same steps, written as a loop over the two chunks (the compiler
+                    // generates ~2 % faster code for this form than for the d=128 branch's lambdas)
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const uint4 wv = make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
-                        *reinterpret_cast<uint4*>(region + sw128_offset((uint32_t)k, (uint32_t)((cc & 1) * 4 + u))) = wv;
+                    for (int ci = 0; ci < NCH_H; ++ci) {
+                        const int cc = h * NCH_H + ci;
+                        uint32_t sv[32], dpv[32];
+                        ptx::tmem_ld32_nowait(t_s + 32 * cc, sv);
+                        ptx::tmem_ld32_nowait(t_dp + 32 * cc, dpv);
+                        ptx::tmem_wait_ld(sv);
+                        ptx::tmem_wait_ld(dpv);
+                        if (ci == NCH_H - 1) {
+                            // this half's S^T/dP^T columns are in registers: release them
+                            ptx::tc_fence_before();
+                            ptx::mbar_arrive(ptx::smem_addr(&bars->s_free));
+                        }
+                        uint32_t pk[16], dk[16];
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4) {
+                            const int qi = 32 * cc + j;
+                            // x = c * S' = c * S - LSE * log2(e)
+                            float x0, x1, x2, x3;
+                            ptx::fmul2(x0, x1, __uint_as_float(sv[j]), __uint_as_float(sv[j + 1]), c, c);
+                            ptx::fmul2(x2, x3, __uint_as_float(sv[j + 2]), __uint_as_float(sv[j + 3]), c, c);
+                            float pe0 = ptx::ex2_approx(x0), pe1 = ptx::ex2_approx(x1);
+                            float pe2 = ptx::ex2_approx(x2), pe3 = ptx::ex2_approx(x3);
+                            if (need_mask) {
+                                // visible iff key <= p <= key + window, i.e. p - key in [0, vspan]
+                                const uint32_t dp = (uint32_t)(p0 + qi - key);
+                                if (dp > vspan) pe0 = 0.f;
+                                if (dp + 1u > vspan) pe1 = 0.f;
+                                if (dp + 2u > vspan) pe2 = 0.f;
+                                if (dp + 3u > vspan) pe3 = 0.f;
+                            }
+                            // dS = P (dP - D) = P dP'
+                            float d0, d1, d2, d3;
+                            ptx::fmul2(d0, d1, pe0, pe1, __uint_as_float(dpv[j]), __uint_as_float(dpv[j + 1]));
+                            ptx::fmul2(d2, d3, pe2, pe3, __uint_as_float(dpv[j + 2]), __uint_as_float(dpv[j + 3]));
+                            pk[j / 2] = ptx::pack_bf16x2(pe0, pe1);
+                            pk[j / 2 + 1] = ptx::pack_bf16x2(pe2, pe3);
+                            dk[j / 2] = ptx::pack_bf16x2(d0, d1);
+                            dk[j / 2 + 1] = ptx::pack_bf16x2(d2, d3);
+                        }
+                        if (ci == 0) {
+                            if (g > 0) {
+                                // dV of step g - 1 must have read P^T before it is overwritten.
+                                ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->mma_done),
+                                                                        (uint32_t)(g - 1) & 1u, abort_flag,
+                                                                        err, kDevTimeoutMma));
+                                if (!ok) break;
+                            }
+                            if (g >= C::NDS) {
+                                // dK and dQ of step g - NDS must have read this dS buffer.
+                                ok = __all_sync(0xffffffffu, wait_phase(ptx::smem_addr(&bars->ds_free[g % C::NDS]),
+                                                                        (uint32_t)(g / C::NDS - 1) & 1u,
+                                                                        abort_flag, err, kDevTimeoutMma));
+                                if (!ok) break;
+                            }
+                            ptx::tc_fence_after();
+                        }
+                        ptx::tmem_st16(t_pt + 16 * cc, pk);
+                        // dS row k (queries contiguous) into the 128B-swizzled dS tile.
+                        uint8_t* region = dsbuf + (cc >> 1) * C::DSREG;
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const uint4 wv = make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
+                            *reinterpret_cast<uint4*>(region + sw128_offset((uint32_t)k, (uint32_t)((cc & 1) * 4 + u))) = wv;
+                        }
                     }
                 }
                 if (!ok) break;
