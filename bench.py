@@ -56,7 +56,7 @@ METRIC = ("attention fwd+bwd TFLOPS (bf16 in, fp32 accumulate), 1 step = fa_forw
 
 
 def select_workload(key):
-    """The main step's workload: configuration 2 by default (the one the metric is quoted on);
+    """The main step's workload: B4 H16 N2048 d64 non-causal by default (the metric's workload);
     `--config K` runs another configuration's fwd + bwd step instead (for profiling)."""
     global WORKLOAD, METRIC
     if key == "2":
@@ -300,7 +300,7 @@ def run_reference(args, rank, world):
 
 def naive_vs_fused(api, dev, reps=10):
     """Forward time and peak device memory of naive materialised attention (S and P written to
-    HBM; exact_io_aware_fa_gb300.naive) against the fused forward, on configuration 2 and on
+    HBM; exact_io_aware_fa_gb300.naive) against the fused forward, on B4 H16 N2048 d64 and on
     T = 4096 ("15. FlashAttention", "Stretch exercises" item 1). Context only."""
     import torch
     from exact_io_aware_fa_gb300 import naive

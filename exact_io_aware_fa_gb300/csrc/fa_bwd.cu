@@ -576,7 +576,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                         const uint64_t dsk = ptx::sdesc_add(ds_kmaj, ds_off);
                         if constexpr (D == 128) {
                             // dV (then P^T is free), the dQ partial (the drain starts on it),
-                            // then dK: measured 1014 -> 1033 TFLOP/s on configuration 5 against
+                            // then dK: measured 1014 -> 1033 TFLOP/s on B4 H16 N4096 causal against
                             // dV, dK, dQ (no change at d=64, which keeps that order).
                             if (ptx::elect_one()) {
 #pragma unroll
@@ -771,7 +771,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     // Where S^T/dP^T are released decides whether the next step's S^T/dP^T MMAs run
                     // ahead of this step's dV/dK/dQ MMAs in the tensor pipe. Measured (backward
                     // TFLOP/s, GB300): d=128 (one 32-query chunk per warpgroup) releases after the
-                    // chunk's exp2 phase and before the buffer waits (configuration 5: 975 with the
+                    // chunk's exp2 phase and before the buffer waits (B4 H16 N4096 causal: 975 with the
                     // release right after the load, 1011 here, 934 after the waits); d=64 (two chunks)
                     // releases after loading its second chunk, behind the waits (B4 H16 N2048: 880;
                     // 853 with both chunks loaded before the waits, 864 after them).

@@ -33,8 +33,8 @@ def _run(naive, bits, causal, scale):
 
 
 @pytest.mark.parametrize("cfg", [(1, 1, 256, 64, 1001), (4, 16, 2048, 64, 1002)],
-                         ids=["config1", "config2"])
-def test_naive_matches_oracle_on_configs_1_2(env, cfg):
+                         ids=["B1H1N256d64", "B4H16N2048d64"])
+def test_naive_matches_oracle(env, cfg):
     from exact_io_aware_fa_gb300 import synthetic
     naive, orc = env
     B, H, N, d, seed = cfg

@@ -89,24 +89,24 @@ def test_gradient_bounds_untouched(env):
         assert torch.all(b[n_el:] == 5.0)
 
 
-def test_config2_backward_full(env):
+def test_backward_full_b4_h16_n2048_d64(env):
     """B=4 H=16 N=2048 d=64, non-causal (the benchmark workload's backward), in full."""
     from exact_io_aware_fa_gb300 import synthetic
     api, orc = env
     bits = synthetic.attention_inputs(4, 16, 2048, 64, seed=1002, with_dout=True)
-    check_full(api, orc, bits, False, default_scale(64), "config 2 backward")
+    check_full(api, orc, bits, False, default_scale(64), "B4 H16 N2048 d64 backward")
 
 
-def test_config2_causal_backward_full(env):
+def test_backward_full_b4_h16_n2048_d64_causal(env):
     """B=4 H=16 N=2048 d=64 under the causal mask, in full: every fold record and dQ accumulator
     row of 64 heads, with units of very unequal cost on the persistent grid."""
     from exact_io_aware_fa_gb300 import synthetic
     api, orc = env
     bits = synthetic.attention_inputs(4, 16, 2048, 64, seed=1012, with_dout=True)
-    check_full(api, orc, bits, True, default_scale(64), "config 2 causal backward")
+    check_full(api, orc, bits, True, default_scale(64), "B4 H16 N2048 d64 causal backward")
 
 
-def test_config5_sampled(env):
+def test_backward_sampled_b4_h16_n4096_d128_causal(env):
     """B=4 H=16 N=4096 d=128, causal; dQ on seeded query rows, dK/dV on seeded key rows."""
     from exact_io_aware_fa_gb300 import synthetic
     api, orc = env
@@ -117,9 +117,9 @@ def test_config5_sampled(env):
     rk = synthetic.sample_rows(N, 32, 2005)
     ref_q, ref_k, ref_v = orc.backward_rows_bf16(bits["q"], bits["k"], bits["v"], bits["do"], True,
                                                  default_scale(d), rq, rk)
-    assert_close_grad(dq[:, :, rq], ref_q, "dQ", "config 5")
-    assert_close_grad(dk[:, :, rk], ref_k, "dK", "config 5")
-    assert_close_grad(dv[:, :, rk], ref_v, "dV", "config 5")
+    assert_close_grad(dq[:, :, rq], ref_q, "dQ", "B4 H16 N4096 d128 causal")
+    assert_close_grad(dk[:, :, rk], ref_k, "dK", "B4 H16 N4096 d128 causal")
+    assert_close_grad(dv[:, :, rk], ref_v, "dV", "B4 H16 N4096 d128 causal")
     for g in (dq, dk, dv):
         assert np.all(np.isfinite(g))
 

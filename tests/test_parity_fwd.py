@@ -103,26 +103,26 @@ def test_output_bounds_untouched(env):
     assert torch.all(lbuf[B * H * N:] == 7.0)
 
 
-def test_config1_full(env):
+def test_forward_full_b1_h1_n256_d64(env):
     """B=1 H=1 N=256 d=64, non-causal, N(0,1), scale 1/8."""
     from exact_io_aware_fa_gb300 import synthetic
     api, orc = env
     bits = synthetic.attention_inputs(1, 1, 256, 64, seed=1001)
     o, lse = run_fwd(api, bits, False, 0.125)
     o_ref, lse_ref = orc.forward_bf16(bits["q"], bits["k"], bits["v"], False, 0.125)
-    assert_close_o(o, o_ref, "config 1")
-    assert_close_lse(lse, lse_ref, "config 1")
+    assert_close_o(o, o_ref, "B1 H1 N256 d64")
+    assert_close_lse(lse, lse_ref, "B1 H1 N256 d64")
 
 
-def test_config2_full(env):
+def test_forward_full_b4_h16_n2048_d64(env):
     """B=4 H=16 N=2048 d=64, non-causal, N(0,1), scale 1/sqrt(d): compared in full."""
     from exact_io_aware_fa_gb300 import synthetic
     api, orc = env
     bits = synthetic.attention_inputs(4, 16, 2048, 64, seed=1002)
     o, lse = run_fwd(api, bits, False, default_scale(64))
     o_ref, lse_ref = orc.forward_bf16(bits["q"], bits["k"], bits["v"], False, default_scale(64))
-    assert_close_o(o, o_ref, "config 2")
-    assert_close_lse(lse, lse_ref, "config 2")
+    assert_close_o(o, o_ref, "B4 H16 N2048 d64")
+    assert_close_lse(lse, lse_ref, "B4 H16 N2048 d64")
 
 
 def _sampled(env, B, H, N, d, causal, seed, qk_sigma):
@@ -139,13 +139,13 @@ def _sampled(env, B, H, N, d, causal, seed, qk_sigma):
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
 
 
-def test_config3_sampled(env):
+def test_forward_sampled_b8_h32_n8192_d128_causal(env):
     """B=8 H=32 N=8192 d=128, causal, N(0,1)."""
     _sampled(env, 8, 32, 8192, 128, True, 1003, 1.0)
 
 
 @pytest.mark.parametrize("N", [16384, 16000])
-def test_config4_sampled(env, N):
+def test_forward_sampled_b1_h64_d128_causal_qk_sd3(env, N):
     """B=1 H=64 d=128 causal, Q and K ~ N(0, 3^2) (large score ranges), V ~ N(0,1)."""
     _sampled(env, 1, 64, N, 128, True, 1004, 3.0)
 
