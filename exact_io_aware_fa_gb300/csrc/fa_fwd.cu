@@ -81,21 +81,16 @@ struct FwdCfg {
     }
 };
 
-// Reference max of the online softmax (log2 domain of the scaled scores).
-// d = 128: the reference moves as soon as the row max grows (threshold 0), so the largest score
-// of a row gets p = exp2(0) = 1 exactly and a peaked row's dominant weight carries no bf16
-// rounding; O is rescaled whenever some row of a warp raised its max.
-// d = 64: the reference moves only when the row max exceeds it by more than 8, so after the
-// first key tile of a unit O is almost never rescaled (p <= 2^8 stays far from fp32 overflow).
+// Reference max of the online softmax (log2 domain of the scaled scores), kRefLag:
+// the reference moves only when the row max exceeds it by more than 8, so after the first key
+// tile of a unit O is almost never rescaled (p <= 2^8 stays far from fp32 overflow). (Moving it
+// whenever the max grows, so that the largest weight is exactly 1, rescaled O on many more
+// steps: 2-3 % slower at d = 128, more at d = 64.)
 // The largest weight p_M = exp2(c s_M - m_ref) is then not 1, and its bf16 rounding would carry
 // into O in peaked rows; the epilogue divides O by l + (bf16(p_M) - p_M), the sum with that
 // weight taken as the PV product used it, which cancels the dominant weight's error (to first
 // order the output error becomes w_M (1 - w_M) eps_M (v_M - v_rest), eps_M its relative rounding).
-template <int D>
-struct Tau {
-    static constexpr float value = (D == 64) ? 8.0f : 0.0f;
-    static constexpr bool lagging = (D == 64);
-};
+constexpr float kRefLag = 8.0f;
 
 struct FwdBars {
     uint64_t q_full[2], q_free[2];
@@ -662,7 +657,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 continue;
             }
             // Online softmax: m_ref (scaled log2 domain) moves when the row max exceeds it by
-            // more than the threshold (Tau); when it moves, both l and the accumulator are rescaled by
+            // more than the threshold (kRefLag); when it moves, both l and the accumulator are rescaled by
             // alpha = exp2(m_old - m_new). O is rescaled only when some row of the warp moved.
             float m_ref = -INFINITY;  // reference (scaled log2 domain)
             float m_raw = -INFINITY;  // lagging reference: largest visible raw score of the row
@@ -743,19 +738,19 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 a1 = ptx::fmax3(a1, s[C::BN - 2], s[C::BN - 1]);
                 const float mx = ptx::fmax3(a0, a1, fmaxf(a2, a3));
                 const float mc = mx * c;
-                const bool upd = mc > m_ref + Tau<D>::value;  // false when the tile is fully masked
+                const bool upd = mc > m_ref + kRefLag;  // false when the tile is fully masked
                 // the warp's rare-rescale decision, taken here rather than after the exponentials:
                 // the vote at that point cost 3-7 % of d=64 forward time (B4 H16 N2048: 899 -> 924
                 // TFLOP/s, B2 H16 N8192: 1094 -> 1170) by constraining the exp loop's schedule
-                const bool warp_upd = Tau<D>::lagging && __any_sync(0xffffffffu, upd);
-                if (Tau<D>::lagging) m_raw = fmaxf(m_raw, mx);
+                const bool warp_upd = __any_sync(0xffffffffu, upd);
+                m_raw = fmaxf(m_raw, mx);
                 float alpha = 1.f;
                 if (upd) {
                     alpha = ptx::ex2_approx(m_ref - mc);  // 0 on the first visible tile
                     m_ref = mc;
                 }
                 const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;  // safe reference
-                if (Tau<D>::lagging && j > jb) {
+                if (j > jb) {
                     // P_t's columns are free and O_t stable once O_t += P_t(j-1) V is complete
                     // (issued at the end of the previous step, so normally done by now): P is
                     // then written to TMEM piece by piece while the exponentials are computed.
@@ -781,7 +776,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     ptx::fadd2(r6, r7, r6, r7, s[k + 6], s[k + 7]);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) pk[k / 2 + i] = ptx::pack_bf16x2(s[k + 2 * i], s[k + 2 * i + 1]);
-                    if (Tau<D>::lagging && (k & 31) == 24) {
+                    if ((k & 31) == 24) {
                         // 32 keys done: their 16 packed columns of P go to TMEM now
                         uint32_t chunk[16];
 #pragma unroll
@@ -790,53 +785,20 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     }
                 }
                 l = l * alpha + (((r0 + r1) + (r2 + r3)) + ((r4 + r5) + (r6 + r7)));
-                if (Tau<D>::lagging) {
-                    // rare: some row of the warp moved its reference, so O_t is rescaled
-                    if (j > jb && warp_upd) {
+                // rare: some row of the warp moved its reference, so O_t is rescaled
+                if (j > jb && warp_upd) {
 #pragma unroll
-                        for (int cc = 0; cc < D / 32; ++cc) {
-                            uint32_t o[32];
-                            ptx::tmem_ld32(t_o + cc * 32, o);
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        uint32_t o[32];
+                        ptx::tmem_ld32(t_o + cc * 32, o);
 #pragma unroll
-                            for (int i = 0; i < 32; i += 2) {
-                                float x0, x1;
-                                ptx::fmul2(x0, x1, __uint_as_float(o[i]), __uint_as_float(o[i + 1]), alpha, alpha);
-                                o[i] = __float_as_uint(x0);
-                                o[i + 1] = __float_as_uint(x1);
-                            }
-                            ptx::tmem_st32(t_o + cc * 32, o);
+                        for (int i = 0; i < 32; i += 2) {
+                            float x0, x1;
+                            ptx::fmul2(x0, x1, __uint_as_float(o[i]), __uint_as_float(o[i + 1]), alpha, alpha);
+                            o[i] = __float_as_uint(x0);
+                            o[i + 1] = __float_as_uint(x1);
                         }
-                    }
-                } else if (j > jb) {
-                    // O_t += P_t(j-1) V must be complete before P_t is overwritten (separate P
-                    // columns) and before O_t is rescaled.
-                    ok = __all_sync(0xffffffffu, wait_phase(b_o_done, (uint32_t)(it - 1) & 1u,
-                                                            abort_flag, err, kDevTimeoutMma));
-                    if (!ok) break;
-                    ptx::tc_fence_after();
-                    if (__any_sync(0xffffffffu, upd)) {
-#pragma unroll
-                        for (int cc = 0; cc < D / 32; ++cc) {
-                            uint32_t o[32];
-                            ptx::tmem_ld32(t_o + cc * 32, o);
-#pragma unroll
-                            for (int i = 0; i < 32; i += 2) {
-                                float x0, x1;
-                                ptx::fmul2(x0, x1, __uint_as_float(o[i]), __uint_as_float(o[i + 1]), alpha, alpha);
-                                o[i] = __float_as_uint(x0);
-                                o[i + 1] = __float_as_uint(x1);
-                            }
-                            ptx::tmem_st32(t_o + cc * 32, o);
-                        }
-                    }
-                }
-                if (!Tau<D>::lagging) {
-#pragma unroll
-                    for (int g = 0; g < C::BN / 32; ++g) {
-                        uint32_t chunk[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) chunk[i] = pk[16 * g + i];
-                        ptx::tmem_st16(t_p + 16 * g, chunk);
+                        ptx::tmem_st32(t_o + cc * 32, o);
                     }
                 }
                 ptx::tmem_wait_st();
@@ -846,9 +808,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             }
             if (!ok) break;
             // Lagging reference: normalise O by the sum of the weights as the PV product used
-            // them, l with the dominant weight p_M replaced by its bf16 value (see Tau).
+            // them, l with the dominant weight p_M replaced by its bf16 value (see kRefLag).
             float l_o = l;
-            if (Tau<D>::lagging && m_ref != -INFINITY) {
+            if (m_ref != -INFINITY) {
                 const float p_m = ptx::ex2_approx(fmaf(m_raw, c, -m_ref));
                 l_o = l + (__bfloat162float(__float2bfloat16_rn(p_m)) - p_m);
             }
