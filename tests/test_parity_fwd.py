@@ -84,6 +84,27 @@ def test_zero_q_closed_form(env, causal):
     assert_close_o(o, o_ref, "zero q")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_row_max_jump_beyond_exp2_range(env, d, causal):
+    """Keys of the last quarter scaled by 100: the first key tile there raises a row's max by
+    hundreds (log2 units of the scaled scores), far past the lagging reference's threshold and
+    the fp32 exponent range of exp2, so that tile's weights are taken against the moved
+    reference and O is rescaled by a factor that underflows to 0. N = 1000 (ragged)."""
+    from exact_io_aware_fa_gb300 import synthetic
+    api, orc = env
+    N = 1000
+    bits = synthetic.attention_inputs(1, 2, N, d, seed=300 + d + int(causal))
+    k = synthetic.bf16_bits_to_float64(bits["k"])
+    k[:, :, 3 * N // 4:] *= 100.0
+    bits["k"] = synthetic.float32_to_bf16_bits(k.astype(np.float32))
+    o, lse = run_fwd(api, bits, causal, default_scale(d))
+    o_ref, lse_ref = orc.forward_bf16(bits["q"], bits["k"], bits["v"], causal, default_scale(d))
+    what = f"key jump d={d} causal={causal}"
+    assert_close_o(o, o_ref, what, small_case=True)
+    assert_close_lse(lse, lse_ref, what)
+
+
 def test_output_bounds_untouched(env):
     """Ragged N: nothing is written past the end of O or LSE."""
     import torch
