@@ -10,6 +10,10 @@ in HBM; L2 is flushed (a 512 MiB write) between timed steps, outside the timed e
 Q, K, V, dO in and of O, LSE, dQ, dK, dV out inside the timed region, pipelined by the library
 over chunks of heads so that copies overlap kernels.
 
+After the timed step: ``configs`` (the five attention configurations, forward and backward),
+``extensions`` (grouped KV heads, chunked prefill, sliding window, split-KV decode) and
+``naive_vs_fused``, each timed alone with L2 flushed.
+
 ``--impl reference`` times the fp64 CPU oracle (the reference arm of this repository) on a
 bounded sample of the same workload instead.
 """
@@ -41,6 +45,20 @@ CONFIGS = [
     dict(name="4: B1 H64 N16384 d128 causal, QK sd 3", B=1, H=64, N=16384, d=128, causal=True, qk_sigma=3.0, seed=1004),
     dict(name="4r: B1 H64 N16000 d128 causal, QK sd 3", B=1, H=64, N=16000, d=128, causal=True, qk_sigma=3.0, seed=1004),
     dict(name="5: B4 H16 N4096 d128 causal", B=4, H=16, N=4096, d=128, causal=True, qk_sigma=1.0, seed=1005),
+]
+# Workloads of the extensions (grouped KV heads, a query offset, a sliding window, split-KV
+# decode), timed after the configurations the same way. Q, K, V, dO ~ N(0, 1), scale 1/sqrt(d).
+EXTENSIONS = [
+    dict(name="GQA B1 Hq32 Hkv8 N8192 d128 causal", B=1, Hq=32, Hkv=8, Tq=8192, Tk=8192, d=128,
+         causal=True, window=-1, bwd=True, seed=2001),
+    dict(name="chunked prefill Tq1024 of Tk16384 B1 Hq32 Hkv8 d128 causal", B=1, Hq=32, Hkv=8,
+         Tq=1024, Tk=16384, d=128, causal=True, window=-1, bwd=True, seed=2002),
+    dict(name="sliding window 4095 B1 Hq32 Hkv8 N16384 d128", B=1, Hq=32, Hkv=8, Tq=16384,
+         Tk=16384, d=128, causal=True, window=4095, bwd=True, seed=2003),
+    dict(name="decode Tq1 Tk16384 B1 Hq32 Hkv8 d128", B=1, Hq=32, Hkv=8, Tq=1, Tk=16384, d=128,
+         causal=True, window=-1, bwd=False, seed=2004),
+    dict(name="decode Tq1 Tk16384 B8 Hq32 Hkv8 d128", B=8, Hq=32, Hkv=8, Tq=1, Tk=16384, d=128,
+         causal=True, window=-1, bwd=False, seed=2005),
 ]
 FWD_KERNEL_SRC = os.path.join(ROOT, "exact_io_aware_fa_gb300", "csrc", "fa_fwd.cu")
 BWD_KERNEL_SRC = os.path.join(ROOT, "exact_io_aware_fa_gb300", "csrc", "fa_bwd.cu")
@@ -93,7 +111,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-configs", action="store_true", help="skip the per-configuration block")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-configuration, extension and naive-comparison blocks")
     ap.add_argument("--config-reps", type=int, default=20)
     ap.add_argument("--config", default="2", choices=["1", "2", "3", "4", "4r", "5"],
                     help="configuration of the main timed step (default 2)")
@@ -436,6 +455,90 @@ def time_configs(api, dev, reps, peaks):
     return out
 
 
+def visible_pairs(Tq, Tk, causal, window):
+    """Query-key pairs a launch computes: query row i at key position Tk - Tq + i sees the keys
+    up to it (causal) and, with a window, no more than `window` positions before it."""
+    total = 0
+    for i in range(Tq):
+        p = Tk - Tq + i
+        hi = min(p, Tk - 1) if causal else Tk - 1
+        lo = max(0, p - window) if window >= 0 else 0
+        total += max(0, hi - lo + 1)
+    return total
+
+
+def time_extensions(api, dev, reps, peaks):
+    """Median fwd (and bwd) times of the extension workloads, through the Python API with
+    preallocated outputs and workspaces (CUDA events on the launching stream, L2 flushed before
+    each repetition). FLOPs 4 * B * Hq * (visible pairs) * d, x2.5 for the backward; decode
+    also reports its K and V bytes over the forward's time against the measured copy rate."""
+    import torch
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    peak = peaks["bf16_tflops"]
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    out = []
+    for ext in EXTENSIONS:
+        B, Hq, Hkv, Tq, Tk, d = ext["B"], ext["Hq"], ext["Hkv"], ext["Tq"], ext["Tk"], ext["d"]
+        causal, window = ext["causal"], ext["window"]
+        g = torch.Generator(device=dev)
+        g.manual_seed(ext["seed"])
+
+        def normal(h, n):
+            return torch.randn((B, h, n, d), generator=g, device=dev).to(torch.bfloat16)
+
+        q, k, v, do = normal(Hq, Tq), normal(Hkv, Tk), normal(Hkv, Tk), normal(Hq, Tq)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, Hq, Tq), dtype=torch.float32, device=dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        nsplit = api.choose_splits(B, Hq, Hkv, Tq, Tk, sms)
+        fws = None
+        if nsplit > 1:
+            fws = torch.empty(api.splitkv_workspace_bytes(B, Hq, Tq, d, nsplit),
+                              dtype=torch.uint8, device=dev)
+        bws = torch.empty(api.backward_workspace_bytes(B, Hq, Tq, d), dtype=torch.uint8,
+                          device=dev) if ext["bwd"] else None
+
+        def fwd():
+            api.forward(q, k, v, causal=causal, window=window, out=o, lse=lse, nsplit=nsplit,
+                        workspace=fws)
+
+        def bwd():
+            api.backward(q, k, v, o, lse, do, causal=causal, window=window, dq=dq, dk=dk, dv=dv,
+                         workspace=bws)
+
+        def timed(fn):
+            for _ in range(3):
+                fn()
+            ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(reps)]
+            for e in ev:
+                flush.zero_()
+                e[0].record(stream)
+                fn()
+                e[1].record(stream)
+            torch.cuda.synchronize()
+            return statistics.median(e[0].elapsed_time(e[1]) for e in ev)
+
+        fl = 4.0 * B * Hq * visible_pairs(Tq, Tk, causal, window) * d
+        fms = timed(fwd)
+        ent = {"workload": ext["name"], "nsplit": nsplit,
+               "fwd": {"ms": fms, "tflops": fl / fms / 1e9, "frac_of_peak": fl / fms / 1e9 / peak},
+               "timing": f"median of {reps}, L2 flushed"}
+        if not ext["bwd"]:
+            kv_bytes = 2 * B * Hkv * Tk * d * 2
+            ent["fwd"]["kv_gbs"] = kv_bytes / (fms * 1e-3) / 1e9
+            ent["fwd"]["kv_frac_of_hbm"] = ent["fwd"]["kv_gbs"] / peaks["hbm_gbs"]
+        else:
+            bms = timed(bwd)
+            ent["bwd"] = {"ms": bms, "tflops": 2.5 * fl / bms / 1e9,
+                          "frac_of_peak": 2.5 * fl / bms / 1e9 / peak}
+        assert api.device_error() == 0
+        out.append(ent)
+        del q, k, v, do, o, lse, dq, dk, dv, fws, bws
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, rank, world, local):
     import numpy as np
     import torch
@@ -565,9 +668,11 @@ def run_ours(args, rank, world, local):
                "ms_per_step": e2e_ms / args.steps}
 
     configs = None
+    extensions = None
     naive_cmp = None
     if not args.no_configs:
         configs = time_configs(api, dev, args.config_reps, peaks)
+        extensions = time_extensions(api, dev, args.config_reps, peaks)
         naive_cmp = naive_vs_fused(api, dev)
 
     cpu = None
@@ -599,6 +704,7 @@ def run_ours(args, rank, world, local):
                      "hbm_gbs": (traffic / (dom_ms * 1e-3) / 1e9) if traffic else None,
                      "peak_source": f"{peaks['source']} bf16 burst"},
         "configs": configs,
+        "extensions": extensions,
         "naive_vs_fused": naive_cmp,
         "e2e": e2e,
         "gpu_launches": args.steps * 4,
