@@ -14,6 +14,8 @@
 #include "fa_common.cuh"
 #include "fa_launch.h"
 
+static_assert(FA_MAX_SPLITS <= 64, "the split merge holds at most two LSEs per lane");
+
 namespace {
 
 thread_local int t_last_cuda_error = 0;

@@ -900,7 +900,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 // flash-decoding"): with normalised partials O_s and LSE_s = m_s + ln l_s the page's rule
 // m = max m_s, l = sum e^(m_s - m) l_s, a = sum e^(m_s - m) a_s, O = a / l becomes
 // LSE = M + ln sum_s e^(LSE_s - M) and O = sum_s e^(LSE_s - LSE) O_s (M = max_s LSE_s).
-// One warp per query row; each lane owns D/32 columns. Splits with LSE_s = -inf saw no key.
+// One warp per query row; each lane owns D/32 columns. Splits with LSE_s = -inf saw no key
+// (their partial O is not written). Lane s % 32 loads LSE_s (nsplit <= 64, two per lane), so the
+// max and the weights need no chain of dependent loads, and the partial rows of all splits are
+// loaded independently of one another (a loop that read LSE_s before each row's partial took
+// ~11 us for 16 splits of 32 rows).
 // ----------------------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(256)
@@ -912,21 +916,39 @@ fa_fwd_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ 
     const int lane = threadIdx.x & 31;
     ptx::griddep_wait();  // the partials of the attention kernel (this one may launch early)
     if (row >= rows) return;
-    float mx = -INFINITY;
-    for (int sp = 0; sp < nsplit; ++sp) mx = fmaxf(mx, part_lse[(size_t)sp * rows + row]);
+    const float ls0 = lane < nsplit ? part_lse[(size_t)lane * rows + row] : -INFINITY;
+    const float ls1 = lane + 32 < nsplit ? part_lse[(size_t)(lane + 32) * rows + row] : -INFINITY;
+    float mx = fmaxf(ls0, ls1);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
     float acc[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[e] = 0.f;
     float sum = 0.f;
     if (mx != -INFINITY) {
-        for (int sp = 0; sp < nsplit; ++sp) {
-            const float ls = part_lse[(size_t)sp * rows + row];
-            if (ls == -INFINITY) continue;
-            const float wgt = expf(ls - mx);
-            sum += wgt;
-            const float* src = part_o + ((size_t)sp * rows + row) * D + lane * E;
+        const float w0 = (ls0 == -INFINITY) ? 0.f : expf(ls0 - mx);
+        const float w1 = (ls1 == -INFINITY) ? 0.f : expf(ls1 - mx);
+        sum = w0 + w1;
 #pragma unroll
-            for (int e = 0; e < E; ++e) acc[e] = fmaf(wgt, src[e], acc[e]);
+        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+#pragma unroll 4
+        for (int sp = 0; sp < nsplit; ++sp) {
+            const float wgt = __shfl_sync(0xffffffffu, sp < 32 ? w0 : w1, sp & 31);
+            const float* src = part_o + ((size_t)sp * rows + row) * D + lane * E;
+            float x[E];
+            if constexpr (E == 4) {
+                const float4 t4 = *reinterpret_cast<const float4*>(src);
+                x[0] = t4.x;
+                x[1] = t4.y;
+                x[2] = t4.z;
+                x[3] = t4.w;
+            } else {
+#pragma unroll
+                for (int e = 0; e < E; ++e) x[e] = src[e];
+            }
+            // a split without keys contributes nothing (its row of partials is not written)
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[e] = fmaf(wgt, wgt != 0.f ? x[e] : 0.f, acc[e]);
         }
     }
     const float inv = (sum > 0.f) ? 1.f / sum : 0.f;
