@@ -36,6 +36,15 @@ CASES = [
     (1, 2, 2, 129, 200, 64, True, -1, 7),     # more splits than key tiles: empty chunks
     (1, 4, 2, 64, 4096, 128, True, -1, 16),   # short query block, many splits
     (2, 2, 2, 256, 256, 128, True, -1, 2),    # causal square: tile 0 empty in split 1
+    # at most 8 query rows per KV head (group * Tq <= 8): decode shapes
+    (1, 8, 1, 1, 5000, 128, True, -1, 7),     # 8 rows per KV head, ragged cache
+    (1, 5, 1, 1, 3000, 64, False, -1, 4),     # 5 rows (padded to 8), non-causal
+    (2, 4, 2, 3, 1000, 128, True, 100, 3),    # 6 rows at 3 positions, window
+    (1, 2, 2, 1, 20, 64, True, -1, 1),        # cache shorter than one 32-key tile, no split
+    (1, 4, 1, 2, 90, 128, True, 5, 64),       # 64 splits of 3 tiles: empty chunks, window 5
+    (3, 6, 3, 4, 4097, 64, True, -1, 16),     # 8 rows at 4 positions
+    (1, 1, 1, 8, 512, 128, True, -1, 5),      # one head, 8 consecutive causal rows
+    (1, 2, 1, 4, 300, 64, False, -1, 2),      # 8 rows, non-causal
 ]
 
 
