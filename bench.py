@@ -116,6 +116,9 @@ def parse_args():
     ap.add_argument("--config-reps", type=int, default=20)
     ap.add_argument("--config", default="2", choices=["1", "2", "3", "4", "4r", "5"],
                     help="configuration of the main timed step (default 2)")
+    ap.add_argument("--extensions-only", metavar="SUBSTRING", default=None,
+                    help="only the extension workloads whose name contains SUBSTRING (one JSON "
+                         "line; profiling)")
     ap.add_argument("--naive-only", action="store_true",
                     help="only the naive-vs-fused forward comparison (one JSON line; profiling)")
     return ap.parse_args()
@@ -467,7 +470,7 @@ def visible_pairs(Tq, Tk, causal, window):
     return total
 
 
-def time_extensions(api, dev, reps, peaks):
+def time_extensions(api, dev, reps, peaks, name_filter=None):
     """Median fwd (and bwd) times of the extension workloads, through the Python API with
     preallocated outputs and workspaces (CUDA events on the launching stream, L2 flushed before
     each repetition). FLOPs 4 * B * Hq * (visible pairs) * d, x2.5 for the backward; decode
@@ -479,6 +482,8 @@ def time_extensions(api, dev, reps, peaks):
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     out = []
     for ext in EXTENSIONS:
+        if name_filter is not None and name_filter not in ext["name"]:
+            continue
         B, Hq, Hkv, Tq, Tk, d = ext["B"], ext["Hq"], ext["Hkv"], ext["Tq"], ext["Tk"], ext["d"]
         causal, window = ext["causal"], ext["window"]
         g = torch.Generator(device=dev)
@@ -714,6 +719,18 @@ def run_ours(args, rank, world, local):
     print(json.dumps(line), flush=True)
 
 
+def run_extensions_only(args):
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from exact_io_aware_fa_gb300 import api
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    ext = time_extensions(api, dev, args.config_reps, load_peaks(), args.extensions_only)
+    print(json.dumps({"extensions": ext}), flush=True)
+
+
 def run_naive_only(args):
     import torch
 
@@ -731,6 +748,9 @@ def main():
     select_workload(args.config)
     if args.naive_only:
         run_naive_only(args)
+        return
+    if args.extensions_only is not None:
+        run_extensions_only(args)
         return
     rank, world, local = dist_init(args.gpus)
     if args.impl == "reference":
