@@ -80,3 +80,54 @@ def test_random_shape(env, case):
                                      window)
     for name, a, b, s in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref, sens):
         assert_close_grad(to_f64(a), b, name, ids(case), sens=s)
+
+
+def _medium_cases(n=8, seed=20261203):
+    """(B, H, N, d, causal): multi-head shapes with many persistent units per CTA, ragged N and
+    both unit orders of the causal launches."""
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        B = int(rng.integers(1, 5))
+        H = int(rng.integers(3, 41))
+        if B * H > 48:
+            continue
+        N = int(rng.integers(700, 4097))
+        out.append((B, H, N, int(rng.choice([64, 128])), bool(rng.integers(0, 2))))
+    return out
+
+
+MEDIUM = _medium_cases()
+
+
+def mid_ids(c):
+    B, H, N, d, causal = c
+    return f"B{B}H{H}N{N}d{d}{'c' if causal else 'n'}"
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("case", MEDIUM, ids=mid_ids)
+def test_random_medium_shape_sampled(env, case):
+    """Forward on seeded query rows; dQ on seeded query rows and dK, dV on seeded key rows."""
+    import torch
+    from exact_io_aware_fa_gb300 import synthetic
+    api, orc = env
+    B, H, N, d, causal = case
+    bits = synthetic.attention_inputs(B, H, N, d, seed=N + 13 * H + d, with_dout=True)
+    q, k, v, do = (to_dev(bits[n]) for n in ("q", "k", "v", "do"))
+    scale = default_scale(d)
+    o, lse = api.forward(q, k, v, causal=causal, scale=scale)
+    dq, dk, dv = api.backward(q, k, v, o, lse, do, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert api.device_error() == 0
+    rq = synthetic.sample_rows(N, 16, N + 1)
+    rk = synthetic.sample_rows(N, 16, N + 2)
+    o_ref, lse_ref = orc.forward_rows_bf16(bits["q"], bits["k"], bits["v"], causal, scale, rq)
+    what = mid_ids(case)
+    assert_close_o(to_f64(o)[:, :, rq], o_ref, what)
+    assert_close_lse(to_f64(lse)[:, :, rq], lse_ref, what)
+    ref_q, ref_k, ref_v = orc.backward_rows_bf16(bits["q"], bits["k"], bits["v"], bits["do"], causal,
+                                                 scale, rq, rk)
+    assert_close_grad(to_f64(dq)[:, :, rq], ref_q, "dQ", what)
+    assert_close_grad(to_f64(dk)[:, :, rk], ref_k, "dK", what)
+    assert_close_grad(to_f64(dv)[:, :, rk], ref_v, "dV", what)
